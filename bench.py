@@ -1,0 +1,440 @@
+#!/usr/bin/env python
+"""Benchmark of the GB300 attention library on the pages' workloads (synthetic, seeded).
+
+One step is one attn_fwd call on the headline workload: causal GQA prefill,
+bf16, batch 4, 32 query / 8 kv heads, 4096 tokens, head_dim 128.  The same run
+also times the KV-cache decode workload (batch 64, 32/8 heads, 8192 cached
+keys, head_dim 128) and the two smaller prefill workloads, and reports each
+against its roofline.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun each rank runs the same workload on its own GPU (replicas, weak
+scaling); rank 0 prints one JSON line with the whole-job throughput.
+`--impl reference` times the fp64 CPU oracle on bounded samples of the same
+workload (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from head_attention_attn_gb300.inputs import WORKLOADS, make_inputs  # noqa: E402
+
+METRIC = "attention TFLOP/s (prefill) and KV GB/s (decode) on 1 GB300, % of roofline"
+HEADLINE = "causal_gqa_bf16_4x32q8kv_4096x128"
+DECODE = "decode_bf16_64x32q8kv_8192x128"
+EXTRA_PREFILL = ["bidir_keypad_bf16_8x12x512x64", "window128_bf16_4x12x8192x64"]
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+# DRAM bytes per launch measured by ncu (dram__bytes_read.sum + dram__bytes_write.sum) for a
+# kernel source state; the entry stops applying as soon as the kernel source changes.
+NCU_TRAFFIC = {}
+
+
+# ----------------------------------------------------------------------------- distributed plumbing
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1 and not torch.distributed.is_initialized():
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        torch.distributed.init_process_group(backend=backend)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        torch.distributed.barrier()
+
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    if world == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(x: float, world: int, device=None) -> float:
+    if world == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.SUM)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------- algorithmic work
+
+def visible_pairs(c, key_lens=None) -> int:
+    """Number of (query row, visible key) pairs of one head, summed over the batch."""
+    total = 0
+    for b in range(c.B):
+        klen = c.Lk if key_lens is None else int(max(0, min(c.Lk, int(key_lens[b]))))
+        for_rows = np.arange(c.Lq, dtype=np.int64) + c.pos_offset
+        lo = np.zeros_like(for_rows)
+        hi = np.full_like(for_rows, klen)
+        if c.mask_mode == 1:
+            hi = np.minimum(hi, for_rows + 1)
+        elif c.mask_mode == 2 and c.window > 0:
+            lo = np.maximum(lo, for_rows - c.window // 2)
+            hi = np.minimum(hi, for_rows + c.window // 2 + 1)
+        elif c.mask_mode == 3:
+            hi = np.minimum(hi, for_rows + 1)
+            if c.window > 0:
+                lo = np.maximum(lo, for_rows - c.window + 1)
+        total += int(np.maximum(hi - lo, 0).sum())
+    return total
+
+
+def flops_of(c, key_lens=None) -> float:
+    """4 * D flops per visible (row, key) pair (QK^T and PV), over every query head."""
+    return 4.0 * c.D * c.Hq * visible_pairs(c, key_lens)
+
+
+def bytes_of(c, key_lens=None) -> float:
+    """Q and O once, plus the K and V rows the workload can see (each kv head read once)."""
+    esz = 2 if c.dtype == "bf16" else 4
+    qo = 2.0 * c.B * c.Hq * c.Lq * c.D * esz
+    if key_lens is None:
+        kv_rows = c.B * c.Lk
+    else:
+        kv_rows = int(sum(max(0, min(c.Lk, int(x))) for x in key_lens))
+    return qo + 2.0 * c.Hkv * kv_rows * c.D * esz
+
+
+# ----------------------------------------------------------------------------- measurement helpers
+
+def read_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            with open(path) as f:
+                d = json.load(f)
+            out = {}
+            for key in ("hbm_gbs", "bf16_tflops", "bf16_tflops_sustained"):
+                if key in d and isinstance(d[key], (int, float)):
+                    out[key] = float(d[key])
+            if "hbm_gbs" in out and "bf16_tflops" in out:
+                out.setdefault("bf16_tflops_sustained", out["bf16_tflops"])
+                return out, "measured"
+        except Exception:
+            pass
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms while running."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        import tempfile
+        fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        rows = []
+        try:
+            with open(self.path) as f:
+                for line in f:
+                    parts = [p.strip() for p in line.split(",")]
+                    if len(parts) >= 9:
+                        rows.append(parts)
+        except Exception:
+            pass
+        finally:
+            try:
+                os.remove(self.path)
+            except Exception:
+                pass
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "", 1).isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "", 1).isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha1()
+    for rel in ("head_attention_attn_gb300/csrc/prefill_tc.cu", "head_attention_attn_gb300/csrc/common.cuh"):
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:12]
+
+
+def time_device(fn, steps: int, warmup: int, world: int, device) -> float:
+    """Seconds per call: CUDA events on the launching stream, synced on both sides, max over ranks."""
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    barrier(world)
+    stream = torch.cuda.current_stream()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for _ in range(steps):
+        fn()
+    end.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    sec = start.elapsed_time(end) / 1e3 / steps
+    return max_over_ranks(sec, world, device)
+
+
+# ----------------------------------------------------------------------------- our arm
+
+def run_ours(args, rank, world, local):
+    import head_attention_attn_gb300 as attn
+    from head_attention_attn_gb300 import build
+    if rank == 0 or world == 1:
+        build.build_library()
+    barrier(world)
+    attn.load()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    peaks, peak_src = read_peaks()
+
+    def setup(name):
+        c = WORKLOADS[name]
+        q, k, v, kl = make_inputs(c)
+        qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+        kld = None if kl is None else kl.to(dev)
+        out = torch.empty_like(qd)
+        scale = float(torch.tensor(1.0 / math.sqrt(c.D), dtype=torch.float32))
+
+        def call(o=out, qq=qd, kk=kd, vv=vd):
+            attn.attn_fwd(qq, kk, vv, o, pos_offset=c.pos_offset, mask_mode=c.mask_mode, window=c.window,
+                          key_lens=kld, scale=scale)
+        return c, (q, k, v, kl), (qd, kd, vd, kld, out), call
+
+    # ---- headline: causal GQA prefill
+    c, host, devt, call = setup(HEADLINE)
+    flops = flops_of(c)
+    with ClockSampler(local) as clk:
+        sec = time_device(call, args.steps, args.warmup, world, dev)
+    clocks = clk.summary()
+    if attn.sync_status() != attn.ATTN_OK:
+        raise RuntimeError("device status after prefill: " + attn.last_error())
+    tflops = flops / sec / 1e12
+    value = tflops * world  # replicas: every rank processes one full workload per step
+    roof = {"bound": "tensor", "achieved": round(tflops, 2), "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+            "frac": round(tflops / peaks["bf16_tflops"], 4), "peak_source": f"{peak_src} bf16 dense (burst)",
+            "traffic": NCU_TRAFFIC.get(kernel_source_hash()), "kernel": "prefill_tc_kernel<128>",
+            "algorithmic_flops_per_launch": flops}
+
+    # ---- end to end through the public call with pinned host buffers
+    q, k, v, kl = host
+    qh, kh, vh = q.pin_memory(), k.pin_memory(), v.pin_memory()
+    qd, kd, vd, kld, out = devt
+    out_h = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    e2e_steps = max(1, min(args.steps, 200))
+
+    def e2e_step():
+        qd.copy_(qh, non_blocking=True)
+        kd.copy_(kh, non_blocking=True)
+        vd.copy_(vh, non_blocking=True)
+        call()
+        out_h.copy_(out, non_blocking=True)
+
+    e2e_sec = time_device(e2e_step, e2e_steps, min(args.warmup, 3), world, dev)
+    h2d = (qh.numel() + kh.numel() + vh.numel()) * qh.element_size()
+    d2h = out_h.numel() * out_h.element_size()
+    e2e = {"value": round(flops / e2e_sec / 1e12 * world, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+           "d2h_bytes_per_step": d2h, "steps": e2e_steps, "ms_per_step": round(e2e_sec * 1e3, 4)}
+    del host, devt, qh, kh, vh, out_h
+    torch.cuda.empty_cache()
+
+    # ---- decode leg
+    c_d, host_d, devt_d, call_d = setup(DECODE)
+    dec_bytes = bytes_of(c_d)
+    dec_steps = max(3, min(args.steps, 500))
+    dsec = time_device(call_d, dec_steps, args.warmup, world, dev)
+    gbs = dec_bytes / dsec / 1e9
+    decode = {"workload": DECODE, "value": round(gbs * world, 1), "unit": "GB/s", "steps": dec_steps,
+              "ms_per_step": round(dsec * 1e3, 4),
+              "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                           "frac": round(gbs / peaks["hbm_gbs"], 4), "peak_source": f"{peak_src} HBM copy",
+                           "traffic": None, "kernel": "decode_splitkv_kernel<128,4>",
+                           "algorithmic_bytes_per_launch": dec_bytes},
+              "l2": f"inputs {dec_bytes / 1e6:.0f} MB > {L2_BYTES / 1e6:.0f} MB L2, no flush"}
+    del host_d, devt_d
+    torch.cuda.empty_cache()
+
+    # ---- the other prefill workloads (smaller; context)
+    per_config = []
+    for name in EXTRA_PREFILL:
+        c_x, host_x, devt_x, call_x = setup(name)
+        kl_x = host_x[3]
+        f_x, b_x = flops_of(c_x, kl_x), bytes_of(c_x, kl_x)
+        # flush L2 between iterations only where the inputs fit in it
+        flush = None
+        if b_x < 2 * L2_BYTES:
+            flush = torch.empty(int(2 * L2_BYTES), dtype=torch.uint8, device=dev)
+
+            def call_xf(cx=call_x):
+                flush.zero_()
+                cx()
+            tsec_with = time_device(call_xf, min(args.steps, 200), args.warmup, world, dev)
+            tsec_flush = time_device(lambda: flush.zero_(), min(args.steps, 200), args.warmup, world, dev)
+            xs = max(tsec_with - tsec_flush, 1e-9)
+        else:
+            xs = time_device(call_x, min(args.steps, 200), args.warmup, world, dev)
+        per_config.append({"workload": name, "ms_per_step": round(xs * 1e3, 4),
+                           "tflops": round(f_x / xs / 1e12, 2), "gbs": round(b_x / xs / 1e9, 1),
+                           "frac_hbm": round(b_x / xs / 1e9 / peaks["hbm_gbs"], 4),
+                           "frac_tensor": round(f_x / xs / 1e12 / peaks["bf16_tflops"], 4),
+                           "l2": "flushed (2x L2 write between calls)" if flush is not None else "inputs > L2"})
+        del host_x, devt_x, flush
+        torch.cuda.empty_cache()
+
+    if attn.sync_status() != attn.ATTN_OK:
+        raise RuntimeError("device status: " + attn.last_error())
+
+    result = {
+        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(sec * 1e3, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": HEADLINE, "batch": c.B, "q_heads": c.Hq, "kv_heads": c.Hkv, "seq_len": c.Lq,
+                   "head_dim": c.D, "mask": "causal", "pos_offset": c.pos_offset,
+                   "l2": f"inputs {bytes_of(c) / 1e6:.0f} MB > {L2_BYTES / 1e6:.0f} MB L2, no flush",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": roof, "e2e": e2e, "gpu_launches": args.steps, "clocks": clocks, "decode": decode,
+        "per_config": per_config,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
+    return result
+
+
+# ----------------------------------------------------------------------------- oracle (CPU) arms
+
+def _oracle_sample_flops(c, rows):
+    i = rows % c.Lq
+    pos = i + c.pos_offset
+    vis = np.minimum(pos + 1, c.Lk) if c.mask_mode == 1 else np.full_like(pos, c.Lk)
+    return float(4.0 * c.D * vis.sum())
+
+
+def cpu_baseline(target_seconds: float):
+    """The oracle as it stands, on a bounded random sample of query rows of the headline workload."""
+    import oracle
+    c = WORKLOADS[HEADLINE]
+    q, k, v, kl = make_inputs(c)
+    qf, kf, vf = q.float().numpy(), k.float().numpy(), v.float().numpy()
+    rng = np.random.default_rng(0)
+    cores = len(os.sched_getaffinity(0))
+    n = 256
+    total_rows, total_flops, total_sec = 0, 0.0, 0.0
+    while total_sec < target_seconds:
+        rows = np.sort(rng.integers(0, c.B * c.Hq * c.Lq, size=n))
+        t0 = time.perf_counter()
+        oracle.attention(qf, kf, vf, mask_mode=c.mask_mode, pos_offset=c.pos_offset, rows=rows, nthreads=cores)
+        dt = time.perf_counter() - t0
+        total_rows += n
+        total_flops += _oracle_sample_flops(c, rows)
+        total_sec += dt
+        n = int(min(65536, max(256, n * min(4.0, max(1.0, (target_seconds - total_sec) / max(dt, 1e-3))))))
+    return {"value": round(total_flops / total_sec / 1e12, 6), "unit": "TFLOP/s", "cores": cores,
+            "kind": "oracle",
+            "sample": f"{total_rows} random query rows of {HEADLINE} (fp64 C oracle, {total_sec:.1f} s)"}
+
+
+def run_reference(args, rank, world):
+    import oracle
+    if rank != 0:
+        return None
+    c = WORKLOADS[HEADLINE]
+    q, k, v, kl = make_inputs(c)
+    qf, kf, vf = q.float().numpy(), k.float().numpy(), v.float().numpy()
+    cores = len(os.sched_getaffinity(0))
+    rng = np.random.default_rng(1)
+    rows_per_step = args.ref_rows
+
+    def step():
+        rows = np.sort(rng.integers(0, c.B * c.Hq * c.Lq, size=rows_per_step))
+        oracle.attention(qf, kf, vf, mask_mode=c.mask_mode, pos_offset=c.pos_offset, rows=rows, nthreads=cores)
+        return _oracle_sample_flops(c, rows)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    flops = sum(step() for _ in range(args.steps))
+    sec = time.perf_counter() - t0
+    value = flops / sec / 1e12
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(sec / args.steps * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": HEADLINE, "batch": c.B, "q_heads": c.Hq, "kv_heads": c.Hkv, "seq_len": c.Lq,
+                   "head_dim": c.D, "mask": "causal", "parallelism": "host cores"},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{rows_per_step} random query rows per step of {HEADLINE}"},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ref-rows", type=int, default=64)
+    args = ap.parse_args(argv)
+    args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps
+    rank, world, local = dist_setup()
+    if args.impl == "reference":
+        res = run_reference(args, rank, world)
+    else:
+        res = run_ours(args, rank, world, local)
+    if rank == 0 and res is not None:
+        print(json.dumps(res), flush=True)
+    if world > 1 and torch.distributed.is_initialized():
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,156 @@
+"""ctypes binding of libattn.so (include/attn.h): argument marshalling only.
+
+Every step of attention runs in the library's CUDA kernels.  If the library is
+missing the first call raises: there is no Python or CPU fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+from .build import LIB_PATH
+
+ATTN_OK, ATTN_ERR_INVALID_ARG, ATTN_ERR_UNSUPPORTED, ATTN_ERR_CUDA, ATTN_ERR_TIMEOUT = range(5)
+MASK_NONE, MASK_CAUSAL, MASK_WINDOW, MASK_CAUSAL_WINDOW = 0, 1, 2, 3
+ATTN_BF16, ATTN_F32 = 0, 1
+
+EXPORTED = ("attn_fwd", "attn_last_error", "attn_sync_status", "attn_selftest_timeout", "attn_version")
+
+_STATUS_NAMES = {0: "ATTN_OK", 1: "ATTN_ERR_INVALID_ARG", 2: "ATTN_ERR_UNSUPPORTED", 3: "ATTN_ERR_CUDA",
+                 4: "ATTN_ERR_TIMEOUT"}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class AttnError(RuntimeError):
+    """A non-OK status from the library; .status holds the attn_status code."""
+
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{_STATUS_NAMES.get(status, status)}: {message}")
+        self.status = status
+
+
+def library_path() -> str:
+    return LIB_PATH
+
+
+def load(path: str | None = None):
+    """Load libattn.so (default: the in-tree build) and declare its signatures."""
+    global _lib
+    with _lock:
+        if _lib is not None and path is None:
+            return _lib
+        p = path or LIB_PATH
+        if not os.path.exists(p):
+            raise RuntimeError(f"libattn.so not found at {p}; build it with "
+                               "head_attention_attn_gb300.build.build_library()")
+        lib = ctypes.CDLL(p)
+        vp, ci = ctypes.c_void_p, ctypes.c_int
+        lib.attn_fwd.restype = ci
+        lib.attn_fwd.argtypes = [vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, ci, ci, ci, vp, ctypes.c_float, ci, vp]
+        lib.attn_last_error.restype = ctypes.c_char_p
+        lib.attn_last_error.argtypes = []
+        lib.attn_sync_status.restype = ci
+        lib.attn_sync_status.argtypes = [vp]
+        lib.attn_selftest_timeout.restype = ci
+        lib.attn_selftest_timeout.argtypes = [ci, vp]
+        lib.attn_version.restype = ci
+        lib.attn_version.argtypes = []
+        if path is None:
+            _lib = lib
+        return lib
+
+
+def last_error() -> str:
+    return load().attn_last_error().decode()
+
+
+def _check(status: int):
+    if status != ATTN_OK:
+        raise AttnError(status, last_error())
+
+
+def _stream_handle(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if hasattr(stream, "cuda_stream"):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def attn_fwd_raw(q_ptr, k_ptr, v_ptr, out_ptr, batch, q_heads, kv_heads, q_len, kv_len, head_dim,
+                 pos_offset, mask_mode, window, key_lens_ptr, scale, dtype, stream_handle) -> int:
+    """Direct call of the C entry point with integer pointers; returns the status code."""
+    return load().attn_fwd(q_ptr, k_ptr, v_ptr, out_ptr, batch, q_heads, kv_heads, q_len, kv_len, head_dim,
+                           pos_offset, mask_mode, window, key_lens_ptr, ctypes.c_float(scale), dtype,
+                           stream_handle)
+
+
+def attn_fwd(q, k, v, out=None, *, pos_offset: int = 0, mask_mode: int = MASK_NONE, window: int = 0,
+             key_lens=None, scale: float | None = None, stream=None):
+    """Attention forward on CUDA tensors (head-major, contiguous).
+
+    q [B, Hq, Lq, D], k and v [B, Hkv, Lk, D] (bf16 or fp32, same dtype),
+    key_lens: int32 CUDA tensor [B] or None; out: preallocated [B, Hq, Lq, D] or None.
+    scale None means 1/sqrt(D) rounded to fp32.  Enqueues on `stream`
+    (default: torch's current stream) and returns out without synchronising.
+    """
+    import torch
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+        if t.dim() != 4:
+            raise ValueError(f"{name} must be 4-D")
+    if q.dtype != k.dtype or q.dtype != v.dtype:
+        raise ValueError("q, k, v must share a dtype")
+    if q.dtype == torch.bfloat16:
+        dtype = ATTN_BF16
+    elif q.dtype == torch.float32:
+        dtype = ATTN_F32
+    else:
+        raise ValueError(f"unsupported dtype {q.dtype}")
+    B, Hq, Lq, D = q.shape
+    Bk, Hkv, Lk, Dk = k.shape
+    if tuple(v.shape) != tuple(k.shape) or Bk != B or Dk != D:
+        raise ValueError("shape mismatch between q, k and v")
+    if out is None:
+        out = torch.empty_like(q)
+    elif out.shape != q.shape or out.dtype != q.dtype or not out.is_contiguous() or not out.is_cuda:
+        raise ValueError("out must be a contiguous CUDA tensor shaped and typed like q")
+    kl_ptr = None
+    if key_lens is not None:
+        if key_lens.dtype != torch.int32 or not key_lens.is_cuda or key_lens.numel() != B:
+            raise ValueError("key_lens must be an int32 CUDA tensor with B entries")
+        kl_ptr = key_lens.data_ptr()
+    if scale is None:
+        scale = float(torch.tensor(1.0 / math.sqrt(D), dtype=torch.float32).item())
+    status = attn_fwd_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), B, Hq, Hkv, Lq, Lk, D,
+                          int(pos_offset), int(mask_mode), int(window), kl_ptr, float(scale), dtype,
+                          _stream_handle(stream))
+    _check(status)
+    return out
+
+
+def sync_status(stream=None) -> int:
+    """Synchronise the stream and return (and clear) the library's device status code."""
+    return load().attn_sync_status(_stream_handle(stream))
+
+
+def check_device_status(stream=None):
+    """sync_status(), raising AttnError on a non-OK code."""
+    _check(sync_status(stream))
+
+
+def selftest_timeout(limit_us: int, stream=None) -> int:
+    """Enqueue the bounded-wait self test (see attn_selftest_timeout); returns the launch status."""
+    return load().attn_selftest_timeout(int(limit_us), _stream_handle(stream))
+
+
+def version() -> int:
+    return load().attn_version()

@@ -1,0 +1,179 @@
+// attn_api.cu -- the exported C ABI (attn.h): argument checks, kernel choice,
+// the device status word of the bounded waits, and per-thread error messages.
+//
+// Kernel choice:
+//   f32                          -> K3 (SIMT fp32, any head_dim 1..256)
+//   bf16, q_len == 1, group 1/2/4/8 -> K2 (split-KV decode)
+//   bf16 otherwise               -> K1 (tcgen05 + TMA fused prefill)
+// There is no host fallback: an unsupported shape is refused (ferrum-kernels:
+// CUDA ops fail rather than copy data through host memory).
+#include <math.h>
+#include <stdarg.h>
+#include <stdio.h>
+
+#include <mutex>
+#include <string>
+
+#include "attn.h"
+#include "kernels.h"
+
+// Device status word: a bounded wait that gives up writes its code here.
+__device__ unsigned int g_attn_status = 0;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s per device-side wait
+
+thread_local std::string t_last_error;
+
+attn_status fail(attn_status s, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    t_last_error = buf;
+    return s;
+}
+
+struct DeviceState {
+    bool ready = false;
+    unsigned* status = nullptr;
+    int num_sms = 0;
+};
+DeviceState g_dev[kMaxDevices];
+std::mutex g_dev_mu;
+
+attn_status device_state(DeviceState** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+    if (dev < 0 || dev >= kMaxDevices) return fail(ATTN_ERR_UNSUPPORTED, "device ordinal %d out of range", dev);
+    std::lock_guard<std::mutex> g(g_dev_mu);
+    DeviceState& st = g_dev[dev];
+    if (!st.ready) {
+        void* ptr = nullptr;
+        e = cudaGetSymbolAddress(&ptr, g_attn_status);
+        if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "cudaGetSymbolAddress: %s", cudaGetErrorString(e));
+        int sms = 0;
+        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "cudaDeviceGetAttribute: %s", cudaGetErrorString(e));
+        st.status = static_cast<unsigned*>(ptr);
+        st.num_sms = sms;
+        st.ready = true;
+    }
+    *out = &st;
+    return ATTN_OK;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+}  // namespace
+
+extern "C" {
+
+attn_status attn_fwd(const void* q, const void* k, const void* v, void* out, int batch, int q_heads, int kv_heads,
+                     int q_len, int kv_len, int head_dim, int pos_offset, int mask_mode, int window,
+                     const int32_t* key_lens, float scale, int dtype, void* cuda_stream) {
+    t_last_error.clear();
+    if (batch < 0 || q_len < 0 || kv_len < 0)
+        return fail(ATTN_ERR_INVALID_ARG, "negative size (batch=%d, q_len=%d, kv_len=%d)", batch, q_len, kv_len);
+    if (q_heads <= 0 || kv_heads <= 0 || head_dim <= 0)
+        return fail(ATTN_ERR_INVALID_ARG, "q_heads, kv_heads and head_dim must be positive (%d, %d, %d)", q_heads,
+                    kv_heads, head_dim);
+    if (q_heads % kv_heads != 0)
+        return fail(ATTN_ERR_INVALID_ARG, "q_heads (%d) is not a multiple of kv_heads (%d)", q_heads, kv_heads);
+    if (mask_mode < ATTN_MASK_NONE || mask_mode > ATTN_MASK_CAUSAL_WINDOW)
+        return fail(ATTN_ERR_INVALID_ARG, "mask_mode %d out of range", mask_mode);
+    if (dtype != ATTN_BF16 && dtype != ATTN_F32) return fail(ATTN_ERR_INVALID_ARG, "dtype %d out of range", dtype);
+    if (window < 0) return fail(ATTN_ERR_INVALID_ARG, "negative window %d", window);
+    if (pos_offset < 0) return fail(ATTN_ERR_INVALID_ARG, "negative pos_offset %d", pos_offset);
+    if (!isfinite(scale)) return fail(ATTN_ERR_INVALID_ARG, "scale is not finite");
+    if (dtype == ATTN_BF16 && head_dim != 64 && head_dim != 128)
+        return fail(ATTN_ERR_UNSUPPORTED, "bf16 supports head_dim 64 and 128, not %d", head_dim);
+    if (dtype == ATTN_F32 && head_dim > 256)
+        return fail(ATTN_ERR_UNSUPPORTED, "f32 supports head_dim up to 256, not %d", head_dim);
+    if ((long long)batch * q_heads > 0x7fffffffLL || (long long)batch * kv_heads > 0x7fffffffLL)
+        return fail(ATTN_ERR_UNSUPPORTED, "batch * heads exceeds 2^31-1");
+    if (batch == 0 || q_len == 0) return ATTN_OK;  // nothing to compute
+
+    if (!q || !out) return fail(ATTN_ERR_INVALID_ARG, "null q or out pointer");
+    const size_t esize = (dtype == ATTN_BF16) ? 2 : 4;
+    cudaStream_t stream = static_cast<cudaStream_t>(cuda_stream);
+    if (kv_len == 0) {
+        // Every row sees no key: the defined result is all zeros.
+        const size_t bytes = (size_t)batch * q_heads * q_len * head_dim * esize;
+        cudaError_t e = cudaMemsetAsync(out, 0, bytes, stream);
+        if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "cudaMemsetAsync: %s", cudaGetErrorString(e));
+        return ATTN_OK;
+    }
+    if (!k || !v) return fail(ATTN_ERR_INVALID_ARG, "null k or v pointer");
+    const uintptr_t align = (dtype == ATTN_BF16) ? 16 : 4;
+    if (!aligned(q, align) || !aligned(k, align) || !aligned(v, align) || !aligned(out, align))
+        return fail(ATTN_ERR_INVALID_ARG, "q, k, v and out must be %u-byte aligned", (unsigned)align);
+    if (key_lens && !aligned(key_lens, 4)) return fail(ATTN_ERR_INVALID_ARG, "key_lens must be 4-byte aligned");
+
+    DeviceState* st = nullptr;
+    attn_status s = device_state(&st);
+    if (s != ATTN_OK) return s;
+    attn::WaitCtl wc{st->status, kWaitLimitNs};
+    attn::Problem p{q, k, v, out, batch, q_heads, kv_heads, q_len, kv_len, head_dim,
+                    pos_offset, mask_mode, window, key_lens, scale};
+
+    cudaError_t e;
+    const char* which;
+    if (dtype == ATTN_F32) {
+        if (q_heads > 65535 || batch > 65535)
+            return fail(ATTN_ERR_UNSUPPORTED, "f32 path limits q_heads and batch to 65535");
+        which = "simt_f32";
+        e = attn::launch_simt_f32(p, wc, stream);
+    } else if (attn::decode_supported(p) && kv_heads <= 65535 && batch <= 65535) {
+        which = "decode_splitkv";
+        e = attn::launch_decode_splitkv(p, wc, stream, st->num_sms);
+    } else {
+        which = "prefill_tc";
+        e = attn::launch_prefill_tc(p, wc, stream);
+    }
+    if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "%s launch: %s", which, cudaGetErrorString(e));
+    return ATTN_OK;
+}
+
+const char* attn_last_error(void) { return t_last_error.c_str(); }
+
+attn_status attn_sync_status(void* cuda_stream) {
+    t_last_error.clear();
+    cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(cuda_stream));
+    if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "stream: %s", cudaGetErrorString(e));
+    DeviceState* st = nullptr;
+    attn_status s = device_state(&st);
+    if (s != ATTN_OK) return s;
+    unsigned word = 0;
+    e = cudaMemcpy(&word, st->status, sizeof word, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "reading the status word: %s", cudaGetErrorString(e));
+    if (word != 0) {
+        const unsigned zero = 0;
+        e = cudaMemcpy(st->status, &zero, sizeof zero, cudaMemcpyHostToDevice);
+        if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "clearing the status word: %s", cudaGetErrorString(e));
+        if (word == attn::kStatusTimeout) return fail(ATTN_ERR_TIMEOUT, "a device-side wait timed out");
+        return fail(ATTN_ERR_CUDA, "device status word %u", word);
+    }
+    return ATTN_OK;
+}
+
+attn_status attn_selftest_timeout(int limit_us, void* cuda_stream) {
+    t_last_error.clear();
+    if (limit_us < 1 || limit_us > 1000000)
+        return fail(ATTN_ERR_INVALID_ARG, "limit_us %d outside [1, 1000000]", limit_us);
+    DeviceState* st = nullptr;
+    attn_status s = device_state(&st);
+    if (s != ATTN_OK) return s;
+    attn::WaitCtl wc{st->status, (unsigned long long)limit_us * 1000ull};
+    cudaError_t e = attn::launch_timeout_selftest(wc, static_cast<cudaStream_t>(cuda_stream));
+    if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "selftest launch: %s", cudaGetErrorString(e));
+    return ATTN_OK;
+}
+
+int attn_version(void) { return 100; }
+
+}  // extern "C"

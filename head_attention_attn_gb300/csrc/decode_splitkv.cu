@@ -1,0 +1,424 @@
+// decode_splitkv.cu -- K2: single-query (q_len == 1) attention against a KV cache, bf16,
+// head_dim 64 or 128, bound by HBM bandwidth.
+//
+// Work unit: (batch b, kv head hk).  Its G = q_heads/kv_heads query heads are
+// served together, so every K and V byte is read from HBM once.  The visible key
+// range of a decode query is one interval [lo, hi) (causal at pos_offset,
+// windows, key padding); a cluster of S CTAs splits it into S contiguous chunks.
+//
+// Inside a CTA (4 warps) each warp takes batches of keys in turn:
+//   - a key row (head_dim bf16) is spread over D/8 lanes, 16 bytes per lane, read
+//     with 128-bit non-caching loads, so a warp reads 2 (D=128) or 4 (D=64)
+//     whole rows per load instruction;
+//   - q (pre-scaled by scale*log2(e)) lives in registers; the per-lane partial
+//     dot products of all (head, key) pairs are summed across the lanes of a
+//     row with a shuffle reduce-scatter (each level halves the values a lane
+//     keeps), so every lane ends with complete scores for a few pairs;
+//   - a lane-group running max and sum per head (base-2 exponent, O rescaled
+//     only when the max grows by more than 2^8) and fp32 accumulators of P V
+//     for the lane's 8 head dims, with packed f32x2 FMAs.
+// Combine: the two lane groups of a warp merge with shuffles, the 4 warps merge
+// through shared memory, and the S CTAs of the cluster merge through
+// distributed shared memory in CTA rank 0, which normalises and stores bf16.
+// No global scratch memory is used.
+//
+// The operation is the q_len = 1 case of ferrum-kernels Backend::flash_attention
+// and the per-cache decode of Backend::flash_attention_batched_per_cache (one
+// launch for all items, device-side lengths, sliding window = last w positions).
+#include "kernels.h"
+
+#include <mutex>
+
+namespace attn {
+namespace {
+
+constexpr int kWarps = 4;
+constexpr int kThreads = kWarps * 32;
+constexpr int kMaxSplits = 8;   // portable cluster size
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kRescaleThreshold = 8.0f;
+
+struct DecodeParams {
+    const __nv_bfloat16* q;
+    const __nv_bfloat16* k;
+    const __nv_bfloat16* v;
+    __nv_bfloat16* out;
+    const int32_t* key_lens;
+    int Hq, Hkv, Lk, P, mode, window;
+    float scale_log2;
+    WaitCtl wc;
+};
+
+template <int D, int G>
+struct DCfg {
+    static constexpr int LPK = D / 8;           // lanes per key row (16 bytes each)
+    static constexpr int KPP = 32 / LPK;        // key rows per warp load instruction
+    static constexpr int NP = (D == 128) ? 4 : 2;  // load instructions (passes) per batch
+    static constexpr int KB = NP * KPP;         // keys per warp batch (8)
+    static constexpr int NV = NP * G;           // partial dot products per lane per batch
+    static constexpr int LEVELS = (LPK == 16) ? 4 : 3;
+};
+
+__device__ __forceinline__ uint4 ldg_stream(const void* p) {
+    uint4 r;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
+    return r;
+}
+
+// 8 bf16 (one 16-byte load) -> 4 float2 pairs (element 2i in .x, 2i+1 in .y).
+__device__ __forceinline__ void bf16x8_to_f2(const uint4& u, float2 (&f)[4]) {
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        f[i].x = __uint_as_float(w[i] << 16);
+        f[i].y = __uint_as_float(w[i] & 0xffff0000u);
+    }
+}
+
+__device__ __forceinline__ float safe_ex2_diff(float a, float m) {
+    // 2^(a - m) with -inf handling: a == -inf -> 0; m == -inf (nothing seen) -> 0.
+    return (m == -INFINITY) ? 0.f : ex2_approx(a - m);
+}
+
+template <int D, int G>
+__global__ void __launch_bounds__(kThreads, 3) decode_splitkv_kernel(const DecodeParams p) {
+    using C = DCfg<D, G>;
+    constexpr int LPK = C::LPK, KPP = C::KPP, NP = C::NP, KB = C::KB, NV = C::NV;
+
+    __shared__ float s_p[kWarps][KPP][NV];          // per-group probabilities of the current batch
+    __shared__ float s_wm[kWarps][G], s_wl[kWarps][G];
+    __shared__ __align__(16) float s_wacc[kWarps][G][D];
+    __shared__ float s_cm[G], s_cl[G];
+    __shared__ __align__(16) float s_cacc[G][D];
+
+    const int split = blockIdx.x;          // == rank in the cluster
+    const int nsplit = gridDim.x;
+    const int hk = blockIdx.y;
+    const int b = blockIdx.z;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int grp = lane / LPK;            // which key row of a load instruction this lane reads
+    const int gl = lane % LPK;             // position inside the row: dims [8*gl, 8*gl+8)
+
+    // Visible interval of the single query at position P, split over the cluster.
+    const int klen = valid_keys(p.key_lens, b, p.Lk);
+    long long lo, hi;
+    key_interval(p.mode, p.window, klen, p.P, p.P, &lo, &hi);
+    if (hi < lo) hi = lo;
+    const long long span = hi - lo;
+    long long chunk = (span + nsplit - 1) / nsplit;
+    chunk = (chunk + KB - 1) / KB * KB;
+    const long long kbeg = lo + (long long)split * chunk;
+    const long long kend = min(hi, kbeg + chunk);
+
+    // q of the G heads, my 8 dims, pre-scaled by scale*log2(e).
+    float2 qf[G][4];
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+        const __nv_bfloat16* qp = p.q + ((size_t)b * p.Hq + (size_t)hk * G + g) * D + 8 * gl;
+        const uint4 u = *reinterpret_cast<const uint4*>(qp);
+        bf16x8_to_f2(u, qf[g]);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            qf[g][i].x *= p.scale_log2;
+            qf[g][i].y *= p.scale_log2;
+        }
+    }
+
+    const size_t head_off = ((size_t)b * p.Hkv + hk) * (size_t)p.Lk * D;
+    const __nv_bfloat16* kh = p.k + head_off + 8 * gl;
+    const __nv_bfloat16* vh = p.v + head_off + 8 * gl;
+
+    float m_run[G], l_run[G];
+    float2 acc[G][4];
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+        m_run[g] = -INFINITY;
+        l_run[g] = 0.f;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc[g][i] = make_float2(0.f, 0.f);
+    }
+
+    // Value index layout of a batch: i = g * NP + pass.  The reduce-scatter
+    // halves on the high index bit first (head bits, then pass bits), so after
+    // RS levels a lane keeps KEEP consecutive passes of a single head.  Levels
+    // beyond RS (when NV < LPK) become all-reduce levels and leave identical
+    // copies in the lanes that differ only in those bits.
+    constexpr int LOG_NV = (NV >= 32) ? 5 : (NV >= 16) ? 4 : (NV >= 8) ? 3 : (NV >= 4) ? 2 : 1;
+    constexpr int RS = (LOG_NV < C::LEVELS) ? LOG_NV : C::LEVELS;
+    constexpr int KEEP = NV >> RS;                                   // values per lane after RS
+    constexpr int LOG_G = (G >= 8) ? 3 : (G >= 4) ? 2 : (G >= 2) ? 1 : 0;
+    constexpr int HEAD_LEVELS = LOG_G;                               // first RS levels: head bits
+    static_assert(KEEP >= 1 && NP % KEEP == 0, "values of a lane stay within one head");
+    static_assert(HEAD_LEVELS <= RS, "head bits are spread by reduce-scatter levels");
+
+    for (long long kb = kbeg + (long long)warp * KB; kb < kend; kb += (long long)kWarps * KB) {
+        // ---- loads (keys past the chunk end are not read)
+        uint4 kr[NP], vr[NP];
+#pragma unroll
+        for (int ps = 0; ps < NP; ++ps) {
+            const long long key = kb + ps * KPP + grp;
+            if (key < kend) {
+                kr[ps] = ldg_stream(kh + key * D);
+                vr[ps] = ldg_stream(vh + key * D);
+            } else {
+                kr[ps] = make_uint4(0, 0, 0, 0);
+                vr[ps] = make_uint4(0, 0, 0, 0);
+            }
+        }
+        // ---- partial dots over my 8 dims
+        float val[NV];
+#pragma unroll
+        for (int ps = 0; ps < NP; ++ps) {
+            float2 kf[4];
+            bf16x8_to_f2(kr[ps], kf);
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                float2 t = __fmul2_rn(qf[g][0], kf[0]);
+                t = __ffma2_rn(qf[g][1], kf[1], t);
+                t = __ffma2_rn(qf[g][2], kf[2], t);
+                t = __ffma2_rn(qf[g][3], kf[3], t);
+                val[g * NP + ps] = t.x + t.y;
+            }
+        }
+        // ---- reduce-scatter, then all-reduce, over the LPK lanes of the row
+        int base = 0;
+#pragma unroll
+        for (int lev = 0; lev < RS; ++lev) {
+            const int mask = LPK >> (lev + 1);
+            const int half = NV >> (lev + 1);
+            const bool upper = (gl & mask) != 0;
+#pragma unroll
+            for (int t = 0; t < half; ++t) {
+                const float send = upper ? val[t] : val[t + half];
+                const float keep = upper ? val[t + half] : val[t];
+                val[t] = keep + __shfl_xor_sync(0xffffffffu, send, mask);
+            }
+            if (upper) base += half;
+        }
+#pragma unroll
+        for (int lev = RS; lev < C::LEVELS; ++lev) {
+            const int mask = LPK >> (lev + 1);
+#pragma unroll
+            for (int t = 0; t < KEEP; ++t) val[t] += __shfl_xor_sync(0xffffffffu, val[t], mask);
+        }
+        // ---- this lane's values: head gh, passes p0 .. p0+KEEP-1; mask keys past the chunk
+        const int gh = base / NP;
+        const int p0 = base % NP;
+        float bm = -INFINITY;
+#pragma unroll
+        for (int t = 0; t < KEEP; ++t) {
+            const long long key = kb + (long long)(p0 + t) * KPP + grp;
+            if (key >= kend) val[t] = -INFINITY;
+            bm = fmaxf(bm, val[t]);
+        }
+        // batch max of my head: reduce over the pass-bit levels (RS levels after the head levels)
+#pragma unroll
+        for (int lev = HEAD_LEVELS; lev < RS; ++lev)
+            bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, LPK >> (lev + 1)));
+        // every lane gathers the batch max of every head and updates the running max
+        float alpha[G];
+        bool any_rescale = false;
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+            int src_gl = 0;  // a lane whose head bits spell g
+#pragma unroll
+            for (int lev = 0; lev < HEAD_LEVELS; ++lev)
+                if ((g >> (HEAD_LEVELS - 1 - lev)) & 1) src_gl |= LPK >> (lev + 1);
+            const float bmg = (G > 1) ? __shfl_sync(0xffffffffu, bm, grp * LPK + src_gl) : bm;
+            alpha[g] = 1.f;
+            if (bmg != -INFINITY) {
+                if (m_run[g] == -INFINITY) {
+                    m_run[g] = bmg;
+                } else if (bmg > m_run[g] + kRescaleThreshold) {
+                    alpha[g] = ex2_approx(m_run[g] - bmg);
+                    m_run[g] = bmg;
+                    any_rescale = true;
+                }
+            }
+        }
+        // ---- probabilities of my values -> shared memory (copies write identical values)
+        {
+            float mh = m_run[0];
+#pragma unroll
+            for (int g = 1; g < G; ++g) mh = (gh == g) ? m_run[g] : mh;
+#pragma unroll
+            for (int t = 0; t < KEEP; ++t) s_p[warp][grp][base + t] = safe_ex2_diff(val[t], mh);
+        }
+        __syncwarp();
+        // ---- rescale + accumulate P V for my 8 dims, every probability read from shared memory
+        if (any_rescale) {
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                l_run[g] *= alpha[g];
+                const float2 a2 = make_float2(alpha[g], alpha[g]);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) acc[g][i] = __fmul2_rn(acc[g][i], a2);
+            }
+        }
+#pragma unroll
+        for (int ps = 0; ps < NP; ++ps) {
+            float2 vf[4];
+            bf16x8_to_f2(vr[ps], vf);
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                const float pv = s_p[warp][grp][g * NP + ps];
+                l_run[g] += pv;
+                const float2 p2 = make_float2(pv, pv);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) acc[g][i] = __ffma2_rn(p2, vf[i], acc[g][i]);
+            }
+        }
+        __syncwarp();  // s_p is rewritten by the next batch
+    }
+
+    // ---------------------------------------------------------------- combine
+    // (1) the KPP row groups of the warp (same dims, different keys)
+#pragma unroll
+    for (int off = LPK; off < 32; off <<= 1) {
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+            const float mo = __shfl_xor_sync(0xffffffffu, m_run[g], off);
+            const float lo_ = __shfl_xor_sync(0xffffffffu, l_run[g], off);
+            const float mc = fmaxf(m_run[g], mo);
+            const float fa = safe_ex2_diff(m_run[g], mc);
+            const float fb = safe_ex2_diff(mo, mc);
+            l_run[g] = l_run[g] * fa + lo_ * fb;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                float2 other;
+                other.x = __shfl_xor_sync(0xffffffffu, acc[g][i].x, off);
+                other.y = __shfl_xor_sync(0xffffffffu, acc[g][i].y, off);
+                acc[g][i].x = acc[g][i].x * fa + other.x * fb;
+                acc[g][i].y = acc[g][i].y * fa + other.y * fb;
+            }
+            m_run[g] = mc;
+        }
+    }
+    // (2) the warps of the CTA, through shared memory
+    if (lane < LPK) {
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                *reinterpret_cast<float2*>(&s_wacc[warp][g][8 * gl + 2 * i]) = acc[g][i];
+            if (lane == 0) {
+                s_wm[warp][g] = m_run[g];
+                s_wl[warp][g] = l_run[g];
+            }
+        }
+    }
+    __syncthreads();
+    for (int t = threadIdx.x; t < G * D; t += kThreads) {
+        const int g = t / D, d = t % D;
+        float mc = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) mc = fmaxf(mc, s_wm[w][g]);
+        float o = 0.f, l = 0.f;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) {
+            const float f = safe_ex2_diff(s_wm[w][g], mc);
+            o += f * s_wacc[w][g][d];
+            l += f * s_wl[w][g];
+        }
+        s_cacc[g][d] = o;
+        if (d == 0) {
+            s_cm[g] = mc;
+            s_cl[g] = l;
+        }
+    }
+    // (3) the CTAs of the cluster, through distributed shared memory, in rank 0
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+    if (split == 0) {
+        for (int t = threadIdx.x; t < G * D; t += kThreads) {
+            const int g = t / D, d = t % D;
+            float ms[kMaxSplits], ls[kMaxSplits], os[kMaxSplits];
+            float mc = -INFINITY;
+            for (int r = 0; r < nsplit; ++r) {
+                uint32_t a_m, a_l, a_o;
+                asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a_m) : "r"(smem_u32(&s_cm[g])), "r"(r));
+                asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a_l) : "r"(smem_u32(&s_cl[g])), "r"(r));
+                asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a_o) : "r"(smem_u32(&s_cacc[g][d])), "r"(r));
+                asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(ms[r]) : "r"(a_m) : "memory");
+                asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(ls[r]) : "r"(a_l) : "memory");
+                asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(os[r]) : "r"(a_o) : "memory");
+                mc = fmaxf(mc, ms[r]);
+            }
+            float o = 0.f, l = 0.f;
+            for (int r = 0; r < nsplit; ++r) {
+                const float f = safe_ex2_diff(ms[r], mc);
+                o += f * os[r];
+                l += f * ls[r];
+            }
+            const float res = (l > 0.f) ? o / l : 0.f;
+            p.out[((size_t)b * p.Hq + (size_t)hk * G + g) * D + d] = __float2bfloat16_rn(res);
+        }
+    }
+    // keep every CTA's shared memory alive until rank 0 has read it
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+template <int D, int G>
+cudaError_t launch_dg(const DecodeParams& p, int B, int nsplit, cudaStream_t stream) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)nsplit, (unsigned)p.Hkv, (unsigned)B);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)nsplit;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, decode_splitkv_kernel<D, G>, p);
+}
+
+template <int D>
+cudaError_t launch_d(const DecodeParams& p, int G, int B, int nsplit, cudaStream_t s) {
+    switch (G) {
+        case 1: return launch_dg<D, 1>(p, B, nsplit, s);
+        case 2: return launch_dg<D, 2>(p, B, nsplit, s);
+        case 4: return launch_dg<D, 4>(p, B, nsplit, s);
+        case 8: return launch_dg<D, 8>(p, B, nsplit, s);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace
+
+bool decode_supported(const Problem& p) {
+    if (p.Lq != 1 || (p.D != 64 && p.D != 128)) return false;
+    const int G = p.Hq / p.Hkv;
+    return G == 1 || G == 2 || G == 4 || G == 8;
+}
+
+cudaError_t launch_decode_splitkv(const Problem& pr, const WaitCtl& wc, cudaStream_t stream, int num_sms) {
+    DecodeParams p;
+    p.q = reinterpret_cast<const __nv_bfloat16*>(pr.q);
+    p.k = reinterpret_cast<const __nv_bfloat16*>(pr.k);
+    p.v = reinterpret_cast<const __nv_bfloat16*>(pr.v);
+    p.out = reinterpret_cast<__nv_bfloat16*>(pr.out);
+    p.key_lens = pr.key_lens;
+    p.Hq = pr.Hq;
+    p.Hkv = pr.Hkv;
+    p.Lk = pr.Lk;
+    p.P = pr.pos_offset;
+    p.mode = pr.mode;
+    p.window = pr.window;
+    p.scale_log2 = pr.scale * kLog2e;
+    p.wc = wc;
+    if (pr.Hkv > 65535 || pr.B > 65535) return cudaErrorInvalidConfiguration;
+    // Splits: enough CTAs for several waves over the SMs, at least 256 keys per split.
+    const long long units = (long long)pr.B * pr.Hkv;
+    long long want = (8LL * (num_sms > 0 ? num_sms : 148) + units - 1) / units;
+    long long by_len = (pr.Lk + 255) / 256;
+    int nsplit = (int)std::max(1LL, std::min<long long>(kMaxSplits, std::min(want, by_len)));
+    const int G = pr.Hq / pr.Hkv;
+    if (pr.D == 64) return launch_d<64>(p, G, pr.B, nsplit, stream);
+    return launch_d<128>(p, G, pr.B, nsplit, stream);
+}
+
+}  // namespace attn

@@ -1,0 +1,67 @@
+// kernels.h -- internal (non-exported) launch interface between the C ABI layer
+// and the three attention kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace attn {
+
+// One validated attention problem (see attn.h for argument meaning).
+struct Problem {
+    const void* q;
+    const void* k;
+    const void* v;
+    void* out;
+    int B, Hq, Hkv, Lq, Lk, D;
+    int pos_offset, mode, window;
+    const int32_t* key_lens;
+    float scale;
+};
+
+// Visible key interval [lo, hi) for queries at positions [qpos_lo, qpos_hi]
+// (inclusive), given klen valid keys.  The rule per mode is the one attn.h
+// states; for a single query position the interval is exact, for a range it is
+// the union over the range.
+__host__ __device__ __forceinline__ void key_interval(int mode, int window, long long klen, long long qpos_lo,
+                                                      long long qpos_hi, long long* lo, long long* hi) {
+    long long l = 0, h = klen;
+    if (mode == 1) {
+        if (qpos_hi + 1 < h) h = qpos_hi + 1;
+    } else if (mode == 2) {
+        if (window > 0) {
+            const long long hw = window / 2;
+            if (qpos_lo - hw > l) l = qpos_lo - hw;
+            if (qpos_hi + hw + 1 < h) h = qpos_hi + hw + 1;
+        }
+    } else if (mode == 3) {
+        if (qpos_hi + 1 < h) h = qpos_hi + 1;
+        if (window > 0 && qpos_lo - window + 1 > l) l = qpos_lo - window + 1;
+    }
+    *lo = l;
+    *hi = h;
+}
+
+// Valid key count of sequence b: key_lens[b] clamped to [0, Lk], or Lk.
+__device__ __forceinline__ int valid_keys(const int32_t* key_lens, int b, int Lk) {
+    if (key_lens == nullptr) return Lk;
+    int n = __ldg(key_lens + b);
+    return n < 0 ? 0 : (n > Lk ? Lk : n);
+}
+
+// K1: tcgen05 + TMA fused prefill, bf16, head_dim 64 or 128.
+cudaError_t launch_prefill_tc(const Problem& p, const WaitCtl& wc, cudaStream_t stream);
+
+// K2: split-KV decode for q_len == 1, bf16, head_dim 64 or 128, group size 1/2/4/8.
+bool decode_supported(const Problem& p);
+cudaError_t launch_decode_splitkv(const Problem& p, const WaitCtl& wc, cudaStream_t stream, int num_sms);
+
+// K3: fp32 SIMT attention, any head_dim in [1, 256].
+cudaError_t launch_simt_f32(const Problem& p, const WaitCtl& wc, cudaStream_t stream);
+
+// Bounded-wait self test: one block waits on an mbarrier nobody signals.
+cudaError_t launch_timeout_selftest(const WaitCtl& wc, cudaStream_t stream);
+
+}  // namespace attn

@@ -1,0 +1,175 @@
+/*
+ * attn.h -- C ABI of the GB300 (sm_103a) multi-head scaled-dot-product attention library.
+ *
+ * The library is libattn.so.  Every entry point takes plain device pointers and
+ * sizes; no framework types cross this boundary.
+ *
+ * What attn_fwd computes, for every batch b, query head h and query row i:
+ *
+ *   out[b,h,i,:] = sum_j w_j * V[b, h/G, j, :]
+ *   w_j = exp(s_j - max) / sum_k exp(s_k - max)    over the keys j allowed for (b, i)
+ *   s_j = scale * <Q[b,h,i,:], K[b, h/G, j, :]>
+ *
+ * with G = q_heads / kv_heads.  A disallowed key has weight exactly 0, and a row
+ * with no allowed key is all zeros.
+ *
+ * Sources (web pages on attention back ends):
+ *   - ferrum-kernels Backend::flash_attention: the statement of the operation, taking
+ *     (q, k, v, out, batch, q_len, kv_len, pos_offset, cfg).  The cfg struct is not
+ *     given there; its fields are the flat arguments below.
+ *   - ripvec-core Driver::fused_scale_mask_softmax: softmax(scores * scale + mask).
+ *   - ripvec-core Driver::fused_scale_mask_softmax_windowed: the symmetric window.
+ *   - ripvec-core Driver::build_attn_mask: the key-padding mask.
+ *   - ferrum-kernels Backend::flash_attention_batched_per_cache: the device kv_lens
+ *     and the decode sliding window.
+ *   - realizar cached/attention.rs, parallel_multihead_attention_gpu_cached and
+ *     batched_causal_softmax: the three stages and the causal softmax.
+ */
+#ifndef ATTN_H
+#define ATTN_H
+
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define ATTN_API __attribute__((visibility("default")))
+#else
+#define ATTN_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes.  Every entry point returns one of these. */
+typedef enum {
+    ATTN_OK = 0,
+    ATTN_ERR_INVALID_ARG = 1, /* argument check failed; nothing was launched */
+    ATTN_ERR_UNSUPPORTED = 2, /* valid, but no kernel for this head_dim / dtype; nothing launched */
+    ATTN_ERR_CUDA = 3,        /* a CUDA runtime or driver call failed */
+    ATTN_ERR_TIMEOUT = 4      /* a bounded device-side wait gave up (see attn_sync_status) */
+} attn_status;
+
+/*
+ * Mask modes.  A query row i sits at absolute position pos_offset + i.  Keys sit
+ * at positions 0 .. kv_len-1.  Key padding (key_lens) applies in every mode.
+ */
+typedef enum {
+    /* Every key is visible: bidirectional encoder attention. */
+    ATTN_MASK_NONE = 0,
+
+    /* Key j is visible when j <= pos_offset + i.
+     * Source: realizar batched_causal_softmax, where row i sees 0..=i;
+     * ferrum-kernels Backend::qk_norm_rope, where token i has position pos_offset + i. */
+    ATTN_MASK_CAUSAL = 1,
+
+    /* Key j is visible when |pos_offset + i - j| <= window/2, with window/2 rounded down.
+     * window == 0 means no window.
+     * Source: ripvec-core Driver::fused_scale_mask_softmax_windowed. */
+    ATTN_MASK_WINDOW = 2,
+
+    /* Key j is visible when pos_offset + i - window < j <= pos_offset + i.
+     * window == 0 means plain causal.
+     * Source: ferrum-kernels flash_attention_batched_per_cache, sliding_window
+     * (the last w valid positions). */
+    ATTN_MASK_CAUSAL_WINDOW = 3
+} attn_mask_mode;
+
+/* Element type of q, k, v and out.  Accumulation is always fp32. */
+typedef enum { ATTN_BF16 = 0, ATTN_F32 = 1 } attn_dtype;
+
+/*
+ * attn_fwd -- enqueue one attention forward pass on cuda_stream and return.
+ *
+ * Layout.  All tensors are contiguous, row-major, head-major, in caller-owned
+ * device memory:
+ *   q, out   [batch, q_heads, q_len, head_dim]
+ *   k, v     [batch, kv_heads, kv_len, head_dim]
+ *   key_lens [batch] int32, or NULL.  key_lens[b] keys of sequence b are valid
+ *            (values outside [0, kv_len] are clamped to that range).  NULL means
+ *            all kv_len keys are valid.
+ *
+ * Query head h reads key/value head h / (q_heads / kv_heads), so each kv head
+ * serves a contiguous group of query heads (grouped-query attention).
+ *
+ * Arguments:
+ *   scale       The multiplier applied to the raw dot products.  Any finite
+ *               value is accepted; 0 gives uniform weights over the visible keys.
+ *               The usual value is 1/sqrt(head_dim).
+ *   dtype       An attn_dtype.
+ *   cuda_stream A cudaStream_t.  NULL means the legacy default stream.
+ *
+ * Supported shapes:
+ *   - bf16 needs head_dim 64 or 128, and the base addresses of q, k, v and out
+ *     aligned to 16 bytes.
+ *   - f32 accepts any head_dim from 1 to 256, with 4-byte alignment.
+ *   - batch or q_len 0: nothing is launched and ATTN_OK is returned.
+ *   - kv_len 0: no row sees a key, so out is zero-filled (cudaMemsetAsync on the stream).
+ *
+ * Ownership and lifetime.  The library keeps no pointer after the call returns,
+ * and allocates no device memory.  The buffers must stay valid until the stream
+ * work completes.  out must not alias q, k or v.  Key and value rows that are
+ * masked out must still hold finite numbers: a masked key gets weight exactly 0,
+ * but the tensor-core product 0 * V of an Inf or NaN value row is NaN.
+ *
+ * Errors.  Arguments are checked before any launch:
+ *   - null pointers, negative sizes, q_heads % kv_heads != 0, a mask_mode or dtype
+ *     out of range, a negative window or pos_offset, a non-finite scale, or a
+ *     misaligned pointer give ATTN_ERR_INVALID_ARG;
+ *   - an unsupported head_dim for the dtype gives ATTN_ERR_UNSUPPORTED;
+ *   - a failed launch gives ATTN_ERR_CUDA.
+ * After any non-OK status, attn_last_error() describes it.
+ *
+ * The call is asynchronous; errors inside the kernels are reported by
+ * attn_sync_status().  There is no host or CPU fallback: a shape with no kernel
+ * is refused.  Source: ferrum-kernels, the CUDA ops that fail rather than copy
+ * through host memory.
+ */
+ATTN_API attn_status attn_fwd(const void* q, const void* k, const void* v, void* out,
+                     int batch, int q_heads, int kv_heads, int q_len, int kv_len, int head_dim,
+                     int pos_offset, int mask_mode, int window, const int32_t* key_lens,
+                     float scale, int dtype, void* cuda_stream);
+
+/*
+ * attn_last_error -- message for the last non-OK status returned on this host thread.
+ * The string belongs to the library and stays valid until the next call on this
+ * thread.  The result is "" when there has been no error.
+ */
+ATTN_API const char* attn_last_error(void);
+
+/*
+ * attn_sync_status -- wait for cuda_stream, then read and clear the library's
+ * device status word on the current device.
+ *
+ * Every device-side wait in the kernels is bounded.  A wait that gives up
+ * records a code in this word, releases what it holds, and exits its block.
+ * Returns:
+ *   - ATTN_ERR_TIMEOUT when a wait gave up;
+ *   - ATTN_ERR_CUDA when the stream reported an error;
+ *   - ATTN_OK otherwise.
+ * Source: ferrum-kernels Backend::sync, where sync is separate from the launch.
+ */
+ATTN_API attn_status attn_sync_status(void* cuda_stream);
+
+/*
+ * attn_selftest_timeout -- exercise the bounded-wait path on the device.
+ *
+ * Launches one block that waits on a shared-memory barrier that nothing
+ * signals, with a wait limit of limit_us microseconds (1 to 1,000,000).  The
+ * wait gives up, records ATTN_ERR_TIMEOUT in the status word, and the block
+ * exits normally.  The caller then reads the code with attn_sync_status().
+ * This never faults or hangs the device.
+ * Returns ATTN_ERR_INVALID_ARG for a limit out of range, ATTN_ERR_CUDA on a
+ * launch failure, and ATTN_OK once enqueued.
+ */
+ATTN_API attn_status attn_selftest_timeout(int limit_us, void* cuda_stream);
+
+/*
+ * attn_version -- library version as major*10000 + minor*100 + patch.
+ */
+ATTN_API int attn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_H */

@@ -1,0 +1,116 @@
+"""The C-ABI library builds for sm_103a, loads, exports every declared entry
+point, and refuses bad arguments before touching the GPU (no CUDA device needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import head_attention_attn_gb300 as attn
+from head_attention_attn_gb300 import build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "attn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build_library()
+    return attn.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return re.findall(r"ATTN_API\s+[\w\s\*]+?\b(attn_\w+)\s*\(", text)
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    assert set(names) == set(attn.EXPORTED)
+    assert "attn_fwd" in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    # and nothing but the C ABI leaks out of the library
+    out = os.popen(f"nm -D --defined-only {attn.library_path()}").read()
+    exported = {line.split()[-1] for line in out.splitlines() if " T " in line}
+    assert set(declared_functions()) <= exported
+    assert not [s for s in exported if s.startswith("_ZN4attn")], "internal symbols are exported"
+
+
+def test_version(lib):
+    assert attn.version() == 100
+
+
+def _call(**kw):
+    args = dict(q_ptr=16, k_ptr=16, v_ptr=16, out_ptr=16, batch=1, q_heads=4, kv_heads=2, q_len=8, kv_len=8,
+                head_dim=64, pos_offset=0, mask_mode=0, window=0, key_lens_ptr=None, scale=0.125,
+                dtype=attn.ATTN_BF16, stream_handle=None)
+    args.update(kw)
+    return attn.attn_fwd_raw(**args)
+
+
+@pytest.mark.parametrize("change,fragment", [
+    (dict(batch=-1), "negative size"),
+    (dict(q_len=-3), "negative size"),
+    (dict(kv_len=-1), "negative size"),
+    (dict(q_heads=0), "must be positive"),
+    (dict(head_dim=0), "must be positive"),
+    (dict(q_heads=3, kv_heads=2), "not a multiple"),
+    (dict(mask_mode=4), "mask_mode"),
+    (dict(mask_mode=-1), "mask_mode"),
+    (dict(dtype=2), "dtype"),
+    (dict(window=-1), "negative window"),
+    (dict(pos_offset=-1), "negative pos_offset"),
+    (dict(scale=float("nan")), "not finite"),
+    (dict(scale=float("inf")), "not finite"),
+    (dict(q_ptr=None), "null q"),
+    (dict(out_ptr=None), "null q or out"),
+    (dict(k_ptr=None), "null k"),
+    (dict(q_ptr=18), "aligned"),
+    (dict(out_ptr=24), "aligned"),
+    (dict(dtype=attn.ATTN_F32, k_ptr=18), "aligned"),
+])
+def test_invalid_arguments_are_refused_before_launch(lib, change, fragment):
+    assert _call(**change) == attn.ATTN_ERR_INVALID_ARG
+    assert fragment in attn.last_error()
+
+
+@pytest.mark.parametrize("change", [dict(head_dim=32), dict(head_dim=96), dict(head_dim=256),
+                                    dict(dtype=attn.ATTN_F32, head_dim=257)])
+def test_unsupported_head_dims(lib, change):
+    assert _call(**change) == attn.ATTN_ERR_UNSUPPORTED
+    assert "head_dim" in attn.last_error()
+
+
+@pytest.mark.parametrize("change", [dict(batch=0), dict(q_len=0),
+                                    dict(batch=0, q_ptr=None, k_ptr=None, v_ptr=None, out_ptr=None)])
+def test_empty_problems_launch_nothing(lib, change):
+    assert _call(**change) == attn.ATTN_OK
+    assert attn.last_error() == ""
+
+
+def test_selftest_limit_is_checked(lib):
+    assert lib.attn_selftest_timeout(0, None) == attn.ATTN_ERR_INVALID_ARG
+    assert lib.attn_selftest_timeout(2_000_000, None) == attn.ATTN_ERR_INVALID_ARG
+
+
+def test_python_wrapper_rejects_cpu_tensors(lib):
+    import torch
+    q = torch.zeros(1, 2, 4, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        attn.attn_fwd(q, q, q)
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    with pytest.raises(RuntimeError, match="not found"):
+        attn.load(str(tmp_path / "libattn.so"))
+
+
+def test_library_has_no_host_fallback_symbols(lib):
+    # The product library never links the oracle.
+    out = os.popen(f"nm -D {attn.library_path()}").read()
+    assert "oracle" not in out
+    assert isinstance(ctypes.CDLL(attn.library_path()), ctypes.CDLL)
