@@ -212,6 +212,17 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float* r) {
         : "memory");
 }
 
+// Store 16 consecutive 32-bit columns of this warp's 32 TMEM lanes, then wait.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* u) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};\n\t"
+        "tcgen05.wait::st.sync.aligned;" ::"r"(taddr),
+        "r"(u[0]), "r"(u[1]), "r"(u[2]), "r"(u[3]), "r"(u[4]), "r"(u[5]), "r"(u[6]), "r"(u[7]),
+        "r"(u[8]), "r"(u[9]), "r"(u[10]), "r"(u[11]), "r"(u[12]), "r"(u[13]), "r"(u[14]), "r"(u[15])
+        : "memory");
+}
+
 // ------------------------------------------------------------------ math
 
 // 2^x on the special-function unit (PTX ex2.approx.ftz.f32); 2^-inf = 0.

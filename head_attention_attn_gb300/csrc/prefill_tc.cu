@@ -1,27 +1,29 @@
 // prefill_tc.cu -- K1: fused attention prefill on the 5th-generation tensor cores (sm_103a).
 //
-// One CTA computes one 128-row query tile of one (batch, query head):
-//   warp 0      TMA producer: the Q tile once, then K and V tiles of 128 keys
-//               through a 2-stage shared-memory ring (128-byte swizzle).
-//   warp 1      TMEM owner and single-thread MMA issuer:
-//               S = Q K^T into TMEM (M=128, N=128, K=head_dim), and
-//               O += P V into TMEM (M=128, N=head_dim, K=128).
-//   warps 2-5   softmax: one thread per query row reads its S row from TMEM,
-//               masks, keeps the running row max and sum (base-2 exponent with
-//               scale*log2(e) folded in), writes P as bf16 into shared memory
-//               (the A operand of the P V product), rescales O in TMEM when the
-//               running max grows by more than 2^8, and finally normalises O by
-//               the row sum and stores bf16 rows of out.
-// Key tiles start at the first key any row of the tile may see, and only tiles
-// that intersect the visible band are visited, so causal and windowed masks
-// skip fully masked tiles.  The S buffer is released as soon as the softmax
-// warps have copied it to registers, so the tensor core computes the next
-// S = Q K^T while the softmax of the current tile runs.
+// One CTA computes two 128-row query tiles (256 consecutive rows) of one
+// (batch, query head), sharing every K and V tile between them:
+//   warp 0       TMA producer: both Q tiles once, then 128-key K and V tiles
+//                through 2-stage shared-memory rings (128-byte swizzle).
+//   warp 1       TMEM owner (all 512 columns) and single-thread MMA issuer.
+//   warps 4-7    softmax of query tile 0, warps 8-11 softmax of query tile 1:
+//                one thread per row reads its S row from TMEM, masks, keeps the
+//                running max and sum (2^x with scale*log2(e) folded in), and
+//                writes P as packed bf16 back into the same TMEM columns.
+//   warps 2-3    idle.
+// TMEM: S0 | S1 | O0 | O1, 128 columns each; P_t aliases the first 64 columns
+// of S_t.  The MMA order is the ping-pong
+//   PV0(j-1), QK0(j), PV1(j-1), QK1(j)
+// so the tensor core works on one tile while the other tile's softmax runs:
+//   QK_t(j):  S_t  = Q_t K_j^T   (A, B from shared memory, K-major)
+//   PV_t(j):  O_t += P_t V_j     (A = P from TMEM, B = V from shared memory, MN-major)
+// A commit after QK_t(j) completes only after every earlier MMA, PV_t(j-1)
+// included, so when the softmax sees S_t(j) it may also rescale O_t and
+// overwrite P_t.  O is rescaled only when the row max grows by more than 2^8.
+// Each query tile visits only the key tiles that intersect its visible band.
 //
-// What is computed follows the ferrum-kernels Backend::flash_attention
-// statement of the operation, the ripvec-core Driver::fused_scale_mask_softmax
-// definition softmax(scores*scale + mask), and the realizar cached/attention.rs
-// causal softmax (a fully masked row gives zeros).
+// What is computed follows ferrum-kernels Backend::flash_attention, ripvec-core
+// Driver::fused_scale_mask_softmax (softmax(scores*scale + mask)) and the
+// realizar cached/attention.rs causal softmax (a fully masked row gives zeros).
 #include "kernels.h"
 
 #include <mutex>
@@ -31,41 +33,37 @@ namespace {
 
 constexpr int BM = 128;           // query rows per tile
 constexpr int BN = 128;           // keys per tile
-constexpr int kThreads = 192;     // 6 warps
+constexpr int kTiles = 2;         // query tiles per CTA
+constexpr int kThreads = 384;     // 12 warps
 constexpr int kStages = 2;        // K/V ring depth
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O only when the max grows by > 2^8
+constexpr float kRescaleThreshold = 8.0f;
 
 template <int D>
 struct Cfg {
-    static constexpr int kChunks = D / 64;           // 64-element (128-byte) swizzle atoms per row
-    static constexpr int kQBytes = BM * D * 2;
-    static constexpr int kKVBytes = BN * D * 2;
-    static constexpr int kPBytes = BM * BN * 2;
+    static constexpr int kChunks = D / 64;
+    static constexpr int kQBytes = BM * D * 2;   // one query tile
+    static constexpr int kKVBytes = BN * D * 2;  // one K or V tile
     static constexpr int kOffQ = 0;
-    static constexpr int kOffK = kOffQ + kQBytes;
+    static constexpr int kOffK = kOffQ + kTiles * kQBytes;
     static constexpr int kOffV = kOffK + kStages * kKVBytes;
-    static constexpr int kOffP = kOffV + kStages * kKVBytes;
-    static constexpr int kOffBar = kOffP + kPBytes;
-    static constexpr int kSmem = kOffBar + 256 + 1024;  // barriers + 1 KB for base alignment
-    static constexpr uint32_t kTmemCols = 256;
-    static constexpr uint32_t kColS = 0;
-    static constexpr uint32_t kColO = 128;
-    static constexpr int kMinBlocks = (D == 64) ? 2 : 1;
+    static constexpr int kOffBar = kOffV + kStages * kKVBytes;
+    static constexpr int kSmem = kOffBar + 256 + 1024;
+    static constexpr uint32_t kTmemCols = 512;
+    static constexpr uint32_t kColS = 0;    // + 128 * tile
+    static constexpr uint32_t kColO = 256;  // + 128 * tile
 };
 
-// Barrier slots (8 bytes each) inside the barrier area.
 enum : int {
     kBarQFull = 0,
-    kBarKFull = 1,                       // + stage
-    kBarVFull = kBarKFull + kStages,     // + stage
-    kBarKEmpty = kBarVFull + kStages,    // + stage
-    kBarVEmpty = kBarKEmpty + kStages,   // + stage
-    kBarSFull = kBarVEmpty + kStages,
-    kBarSFree = kBarSFull + 1,
-    kBarPFull = kBarSFree + 1,
-    kBarPVDone = kBarPFull + 1,
-    kBarMmaDone = kBarPVDone + 1,        // final commit: every MMA of the block has completed
+    kBarKFull = 1,
+    kBarVFull = kBarKFull + kStages,
+    kBarKEmpty = kBarVFull + kStages,
+    kBarVEmpty = kBarKEmpty + kStages,
+    kBarSFull = kBarVEmpty + kStages,  // + tile
+    kBarPFull = kBarSFull + kTiles,    // + tile
+    kBarOFull = kBarPFull + kTiles,    // + tile: the tile's last P V product completed
+    kBarMmaDone = kBarOFull + kTiles,
     kNumBars = kBarMmaDone + 1,
 };
 static_assert(kNumBars * 8 <= 128, "barrier area");
@@ -74,12 +72,11 @@ struct PrefillParams {
     __nv_bfloat16* out;
     const int32_t* key_lens;
     int B, Hq, Hkv, Lq, Lk, P, mode, window;
-    int num_m;          // query tiles per head
-    float scale_log2;   // scale * log2(e)
+    int num_m;          // 256-row query blocks per head
+    float scale_log2;
     WaitCtl wc;
 };
 
-// Wait that ignores the abort flag (used to drain copies still in flight), bounded in time.
 __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, const WaitCtl& wc) {
     const unsigned long long t0 = globaltimer_ns();
     while (!mbar_try_wait(bar, parity)) {
@@ -90,13 +87,28 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, const 
     }
 }
 
+// D(tmem) (+)= A(tmem) * B(smem), kind::f16.
+__device__ __forceinline__ void tc_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                          uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Key tiles of one query tile: [jb, je) in units of BN keys from kv0.
+struct TileRange {
+    int jb, je;
+};
+
 template <int D>
-__global__ void __launch_bounds__(kThreads, Cfg<D>::kMinBlocks)
+__global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV, const PrefillParams p) {
     using C = Cfg<D>;
     extern __shared__ uint8_t smem_raw[];
-    // 1024-byte alignment of the tile area (required by the 128-byte swizzle pattern).
     const uint32_t raw_s = smem_u32(smem_raw);
     uint8_t* smem = smem_raw + ((1024u - (raw_s & 1023u)) & 1023u);
     const uint32_t sbase = smem_u32(smem);
@@ -107,27 +119,49 @@ __global__ void __launch_bounds__(kThreads, Cfg<D>::kMinBlocks)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
-    // Work item: heaviest query tiles first (causal tiles near the end see the most keys).
     int idx = blockIdx.x;
     const int hq = idx % p.Hq;
     idx /= p.Hq;
     const int b = idx % p.B;
     idx /= p.B;
-    const int mblk = p.num_m - 1 - idx;
+    const int mblk = p.num_m - 1 - idx;  // heaviest blocks first
     const int hk = hq / (p.Hq / p.Hkv);
-    const int q0 = mblk * BM;
-    const int q_last = min(q0 + BM, p.Lq) - 1;
-
+    const int q0 = mblk * (kTiles * BM);
     const int klen = valid_keys(p.key_lens, b, p.Lk);
-    long long lo, hi;
-    key_interval(p.mode, p.window, klen, (long long)p.P + q0, (long long)p.P + q_last, &lo, &hi);
-    const int ntiles = (hi > lo) ? (int)((hi - lo + BN - 1) / BN) : 0;
-    const int kv0 = (int)lo;
+
+    // Visible key interval of each query tile, and the shared key-tile grid.
+    long long tlo[kTiles], thi[kTiles];
+    long long kv0 = -1;
+#pragma unroll
+    for (int t = 0; t < kTiles; ++t) {
+        const int qa = q0 + t * BM;
+        if (qa >= p.Lq) {
+            tlo[t] = 0;
+            thi[t] = 0;
+            continue;
+        }
+        const int qb = min(qa + BM, p.Lq) - 1;
+        key_interval(p.mode, p.window, klen, (long long)p.P + qa, (long long)p.P + qb, &tlo[t], &thi[t]);
+        if (thi[t] > tlo[t] && (kv0 < 0 || tlo[t] < kv0)) kv0 = tlo[t];
+    }
+    TileRange rng[kTiles];
+    int ntiles = 0;
+#pragma unroll
+    for (int t = 0; t < kTiles; ++t) {
+        if (kv0 < 0 || thi[t] <= tlo[t]) {
+            rng[t] = {0, 0};
+        } else {
+            rng[t].jb = (int)((tlo[t] - kv0) / BN);
+            rng[t].je = (int)((thi[t] - kv0 + BN - 1) / BN);
+            ntiles = max(ntiles, rng[t].je);
+        }
+    }
+    if (kv0 < 0) kv0 = 0;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kNumBars; ++i) {
             uint32_t count = 1;
-            if (i == kBarSFree || i == kBarPFull) count = 4;  // one arrival per softmax warp
+            if (i >= kBarPFull && i < kBarPFull + kTiles) count = 4;  // one arrival per softmax warp
             mbar_init(bar0 + 8 * i, count);
         }
         *abort_flag = 0;
@@ -152,14 +186,16 @@ __global__ void __launch_bounds__(kThreads, Cfg<D>::kMinBlocks)
         if (lane == 0 && ntiles > 0) {
             const int qbh = b * p.Hq + hq;
             const int kbh = b * p.Hkv + hk;
-            mbar_arrive_expect_tx(bar0 + 8 * kBarQFull, C::kQBytes);
-            for (int c = 0; c < C::kChunks; ++c)
-                tma_load_3d(sbase + C::kOffQ + c * (BM * 128), &tmQ, bar0 + 8 * kBarQFull, c * 64, q0, qbh);
+            mbar_arrive_expect_tx(bar0 + 8 * kBarQFull, kTiles * C::kQBytes);
+            for (int t = 0; t < kTiles; ++t)
+                for (int c = 0; c < C::kChunks; ++c)
+                    tma_load_3d(sbase + C::kOffQ + t * C::kQBytes + c * (BM * 128), &tmQ, bar0 + 8 * kBarQFull,
+                                c * 64, q0 + t * BM, qbh);
             int issued = 0;
             for (int j = 0; j < ntiles; ++j) {
                 const int s = j % kStages;
                 const uint32_t n = (uint32_t)(j / kStages);
-                const int krow = kv0 + j * BN;
+                const int krow = (int)kv0 + j * BN;
                 if (j >= kStages && !mbar_wait(bar0 + 8 * (kBarKEmpty + s), (n - 1) & 1, p.wc, abort_flag)) break;
                 mbar_arrive_expect_tx(bar0 + 8 * (kBarKFull + s), C::kKVBytes);
                 for (int c = 0; c < C::kChunks; ++c)
@@ -175,7 +211,6 @@ __global__ void __launch_bounds__(kThreads, Cfg<D>::kMinBlocks)
                                 bar0 + 8 * (kBarVFull + s), c * 64, krow, kbh);
                 issued = 2 * j + 2;
             }
-            // Drain: no copy may still be writing shared memory when the block exits.
             drain_wait(bar0 + 8 * kBarQFull, 0, p.wc);
             const int nk = (issued + 1) / 2, nv = issued / 2;
             for (int j = (nk > kStages ? nk - kStages : 0); j < nk; ++j)
@@ -188,87 +223,93 @@ __global__ void __launch_bounds__(kThreads, Cfg<D>::kMinBlocks)
         if (lane == 0 && ntiles > 0) {
             constexpr uint32_t kIdescQK = idesc_bf16_f32(BM, BN, 0, 0);
             constexpr uint32_t kIdescPV = idesc_bf16_f32(BM, D, 0, 1);
-            const uint32_t tS = tmem + C::kColS;
-            const uint32_t tO = tmem + C::kColO;
             bool ok = mbar_wait(bar0 + 8 * kBarQFull, 0, p.wc, abort_flag);
-            auto issue_qk = [&](int j) -> bool {
-                const int s = j % kStages;
-                if (!mbar_wait(bar0 + 8 * (kBarKFull + s), (uint32_t)(j / kStages) & 1, p.wc, abort_flag))
-                    return false;
-                if (j > 0 && !mbar_wait(bar0 + 8 * kBarSFree, (uint32_t)(j - 1) & 1, p.wc, abort_flag))
-                    return false;
-                tc_fence_after();
-                const uint32_t kbase = sbase + C::kOffK + s * C::kKVBytes;
+            int it[kTiles] = {0, 0};  // local iteration (P phases consumed) per tile
+            for (int j = 0; ok && j <= ntiles; ++j) {
+                // PV_t(j-1) then QK_t(j), tile by tile
+                bool v_waited = false, k_waited = false;
+                bool used_v = false, used_k = false;
 #pragma unroll
-                for (int ks = 0; ks < D / 16; ++ks) {
-                    const uint32_t off = (ks >> 2) * (BM * 128) + (ks & 3) * 32;
-                    const uint64_t a = smem_desc_sw128(sbase + C::kOffQ + off, 16, 1024);
-                    const uint64_t bd = smem_desc_sw128(kbase + (ks >> 2) * (BN * 128) + (ks & 3) * 32, 16, 1024);
-                    tc_mma_ss(tS, a, bd, kIdescQK, ks > 0 ? 1u : 0u);
-                }
-                tc_commit(bar0 + 8 * kBarSFull);
-                tc_commit(bar0 + 8 * (kBarKEmpty + s));
-                return true;
-            };
-            if (ok) ok = issue_qk(0);
-            for (int j = 0; ok && j < ntiles; ++j) {
-                if (j + 1 < ntiles && !issue_qk(j + 1)) break;
-                const int s = j % kStages;
-                if (!mbar_wait(bar0 + 8 * kBarPFull, (uint32_t)j & 1, p.wc, abort_flag)) break;
-                if (!mbar_wait(bar0 + 8 * (kBarVFull + s), (uint32_t)(j / kStages) & 1, p.wc, abort_flag)) break;
-                tc_fence_after();
-                const uint32_t vbase = sbase + C::kOffV + s * C::kKVBytes;
+                for (int t = 0; t < kTiles; ++t) {
+                    const int jp = j - 1;
+                    if (jp >= 0 && jp >= rng[t].jb && jp < rng[t].je) {
+                        const int s = jp % kStages;
+                        if (!mbar_wait(bar0 + 8 * (kBarPFull + t), (uint32_t)it[t] & 1, p.wc, abort_flag)) { ok = false; break; }
+                        if (!v_waited) {
+                            if (!mbar_wait(bar0 + 8 * (kBarVFull + s), (uint32_t)(jp / kStages) & 1, p.wc, abort_flag)) { ok = false; break; }
+                            v_waited = true;
+                        }
+                        tc_fence_after();
+                        const uint32_t vbase = sbase + C::kOffV + s * C::kKVBytes;
+                        const uint32_t tP = tmem + C::kColS + 128 * t;
+                        const uint32_t tO = tmem + C::kColO + 128 * t;
 #pragma unroll
-                for (int kk = 0; kk < BN / 16; ++kk) {
-                    const uint64_t a =
-                        smem_desc_sw128(sbase + C::kOffP + (kk >> 2) * (BM * 128) + (kk & 3) * 32, 16, 1024);
-                    // V tile: keys along K (128 B per key row), head dims along N in 64-wide
-                    // chunks that are BN*128 bytes apart.
-                    const uint64_t bd = smem_desc_sw128(vbase + kk * (16 * 128), BN * 128, 1024);
-                    tc_mma_ss(tO, a, bd, kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
+                        for (int kk = 0; kk < BN / 16; ++kk) {
+                            const uint64_t bd = smem_desc_sw128(vbase + kk * (16 * 128), BN * 128, 1024);
+                            tc_mma_ts(tO, tP + kk * 8, bd, kIdescPV, (jp > rng[t].jb || kk > 0) ? 1u : 0u);
+                        }
+                        it[t] += 1;
+                        used_v = true;
+                        if (jp == rng[t].je - 1) tc_commit(bar0 + 8 * (kBarOFull + t));
+                    }
+                    if (j < ntiles && j >= rng[t].jb && j < rng[t].je) {
+                        const int s = j % kStages;
+                        if (!k_waited) {
+                            if (!mbar_wait(bar0 + 8 * (kBarKFull + s), (uint32_t)(j / kStages) & 1, p.wc, abort_flag)) { ok = false; break; }
+                            k_waited = true;
+                            tc_fence_after();
+                        }
+                        const uint32_t kbase = sbase + C::kOffK + s * C::kKVBytes;
+                        const uint32_t qbase = sbase + C::kOffQ + t * C::kQBytes;
+                        const uint32_t tS = tmem + C::kColS + 128 * t;
+#pragma unroll
+                        for (int ks = 0; ks < D / 16; ++ks) {
+                            const uint32_t off = (ks >> 2) * (BM * 128) + (ks & 3) * 32;
+                            const uint64_t a = smem_desc_sw128(qbase + off, 16, 1024);
+                            const uint64_t bd = smem_desc_sw128(kbase + off, 16, 1024);
+                            tc_mma_ss(tS, a, bd, kIdescQK, ks > 0 ? 1u : 0u);
+                        }
+                        tc_commit(bar0 + 8 * (kBarSFull + t));
+                        used_k = true;
+                    }
                 }
-                tc_commit(bar0 + 8 * (kBarVEmpty + s));
-                tc_commit(bar0 + 8 * kBarPVDone);
+                if (!ok) break;
+                if (used_v) tc_commit(bar0 + 8 * (kBarVEmpty + (j - 1) % kStages));
+                if (used_k) tc_commit(bar0 + 8 * (kBarKEmpty + j % kStages));
             }
-            // Wait for every MMA issued so far before the block may release TMEM.
             tc_commit(bar0 + 8 * kBarMmaDone);
             drain_wait(bar0 + 8 * kBarMmaDone, 0, p.wc);
         }
-    } else {
+    } else if (warp >= 4) {
         // ------------------------------------------------------------ softmax + epilogue
-        const int wq = warp & 3;                 // TMEM lane quarter this warp may access
-        const int row = wq * 32 + lane;          // query row within the tile
-        const int qi = q0 + row;
+        const int t = (warp - 4) >> 2;           // query tile of this warpgroup
+        const int wq = warp & 3;                 // TMEM lane quarter
+        const int row = wq * 32 + lane;
+        const int qi = q0 + t * BM + row;
         const long long qpos = (long long)p.P + qi;
         long long rlo, rhi;
         key_interval(p.mode, p.window, klen, qpos, qpos, &rlo, &rhi);
         const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
-        const uint32_t tS = tmem + lane_off + C::kColS;
-        const uint32_t tO = tmem + lane_off + C::kColO;
+        const uint32_t tS = tmem + lane_off + C::kColS + 128 * t;
+        const uint32_t tO = tmem + lane_off + C::kColO + 128 * t;
         const float sl = p.scale_log2;
         float m_run = -INFINITY;
         float l_run = 0.f;
         bool ok = true;
-        uint8_t* prow = smem + C::kOffP + (row >> 3) * 1024 + (row & 7) * 128;
-        const int sw = row & 7;
+        const int jb = rng[t].jb, je = rng[t].je;
 
-        for (int j = 0; j < ntiles; ++j) {
-            if (!mbar_wait(bar0 + 8 * kBarSFull, (uint32_t)j & 1, p.wc, abort_flag)) { ok = false; break; }
+        for (int j = jb; j < je; ++j) {
+            const int i = j - jb;
+            if (!mbar_wait(bar0 + 8 * (kBarSFull + t), (uint32_t)i & 1, p.wc, abort_flag)) { ok = false; break; }
             tc_fence_after();
             float s[BN];
 #pragma unroll
             for (int c = 0; c < BN / 32; ++c) tmem_ld32(tS + 32 * c, s + 32 * c);
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar0 + 8 * kBarSFree);
 
-            const long long tb = (long long)kv0 + (long long)j * BN;
+            const long long tb = kv0 + (long long)j * BN;
             const int c_lo = (int)max(0LL, min((long long)BN, rlo - tb));
             const int c_hi = (int)max(0LL, min((long long)BN, rhi - tb));
             const bool full = (c_lo == 0 && c_hi == BN);
-
-            // Extreme of the raw scores over the visible columns: the max when the
-            // scale is non-negative, the min when it is negative.
             float ext;
             if (sl >= 0.f) {
                 ext = -INFINITY;
@@ -290,7 +331,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<D>::kMinBlocks)
             if (any) {
                 const float ms = ext * sl;
                 if (m_run == -INFINITY) {
-                    m_run = ms;  // O holds only zero contributions so far
+                    m_run = ms;
                 } else if (ms > m_run + kRescaleThreshold) {
                     alpha = ex2_approx(m_run - ms);
                     m_run = ms;
@@ -298,82 +339,79 @@ __global__ void __launch_bounds__(kThreads, Cfg<D>::kMinBlocks)
                 }
             }
             const float neg_m = (m_run == -INFINITY) ? 0.f : -m_run;
-            float sum = 0.f;
-            uint32_t pk[BN / 2];
-#pragma unroll
-            for (int c = 0; c < BN; c += 2) {
-                float p0 = ex2_approx(fmaf(s[c], sl, neg_m));
-                float p1 = ex2_approx(fmaf(s[c + 1], sl, neg_m));
-                if (!full) {
-                    p0 = (c >= c_lo && c < c_hi) ? p0 : 0.f;
-                    p1 = (c + 1 >= c_lo && c + 1 < c_hi) ? p1 : 0.f;
-                }
-                sum += p0 + p1;
-                pk[c / 2] = pack_bf16x2(p0, p1);
-            }
-            l_run = l_run * alpha + sum;
 
-            // P buffer and O are free once the previous P V product has completed.
-            if (j > 0) {
-                if (!mbar_wait(bar0 + 8 * kBarPVDone, (uint32_t)(j - 1) & 1, p.wc, abort_flag)) { ok = false; break; }
-                tc_fence_after();
+            // P (bf16 pairs) into the first 64 columns of S_t, 32 keys at a time: the A
+            // operand of P V.  S_t is already in registers, so overwriting it is safe.
+            // The row sum adds the bf16-rounded probabilities, the same numbers the
+            // tensor core multiplies into V, so numerator and denominator agree.
+            float2 sum2 = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int k = 0; k < BN / 32; ++k) {
+                uint32_t pk[16];
+#pragma unroll
+                for (int c2 = 0; c2 < 32; c2 += 2) {
+                    const int c = 32 * k + c2;
+                    float p0 = ex2_approx(fmaf(s[c], sl, neg_m));
+                    float p1 = ex2_approx(fmaf(s[c + 1], sl, neg_m));
+                    if (!full) {
+                        p0 = (c >= c_lo && c < c_hi) ? p0 : 0.f;
+                        p1 = (c + 1 >= c_lo && c + 1 < c_hi) ? p1 : 0.f;
+                    }
+                    const uint32_t w = pack_bf16x2(p0, p1);
+                    pk[c2 / 2] = w;
+                    sum2 = __fadd2_rn(sum2, make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u)));
+                }
+                tmem_st16(tS + 16 * k, pk);
             }
+            l_run = l_run * alpha + (sum2.x + sum2.y);
+            // O_t is stable here: the commit behind S_t(j) covers the earlier P V product.
             if (__any_sync(0xffffffffu, rescale)) {
 #pragma unroll
                 for (int c = 0; c < D / 32; ++c) {
                     float o[32];
                     tmem_ld32(tO + 32 * c, o);
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) o[i] *= alpha;
+                    for (int q = 0; q < 32; ++q) o[q] *= alpha;
                     tmem_st32(tO + 32 * c, o);
                 }
             }
-            // P row -> shared memory, K-major with the 128-byte swizzle: 16-byte chunk cc of
-            // the row goes to chunk position cc ^ (row % 8); keys 64..127 in the second atom.
-#pragma unroll
-            for (int q = 0; q < BN / 8; ++q) {
-                const int atom = q >> 3, cc = q & 7;
-                uint4 v4 = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
-                *reinterpret_cast<uint4*>(prow + atom * (BM * 128) + ((cc ^ sw) << 4)) = v4;
-            }
-            fence_proxy_async_smem();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar0 + 8 * kBarPFull);
+            if (lane == 0) mbar_arrive(bar0 + 8 * (kBarPFull + t));
         }
 
         // ------------------------------------------------------------ epilogue
-        if (ok && ntiles > 0) {
-            ok = mbar_wait(bar0 + 8 * kBarPVDone, (uint32_t)(ntiles - 1) & 1, p.wc, abort_flag);
+        const bool has = je > jb;
+        if (ok && has) {
+            ok = mbar_wait(bar0 + 8 * (kBarOFull + t), 0, p.wc, abort_flag);
             tc_fence_after();
         }
-        if (ok) {
+        if (ok && q0 + t * BM < p.Lq) {
             const float inv = (l_run > 0.f) ? 1.f / l_run : 0.f;
             __nv_bfloat16* orow = p.out + ((size_t)(b * p.Hq + hq) * p.Lq + qi) * D;
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
                 float o[32];
-                if (ntiles > 0) {
+                if (has) {
                     tmem_ld32(tO + 32 * c, o);
                 } else {
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) o[i] = 0.f;
+                    for (int q = 0; q < 32; ++q) o[q] = 0.f;
                 }
                 if (qi < p.Lq) {
 #pragma unroll
-                    for (int i = 0; i < 32; i += 8) {
-                        uint4 v4 = make_uint4(pack_bf16x2(o[i] * inv, o[i + 1] * inv),
-                                              pack_bf16x2(o[i + 2] * inv, o[i + 3] * inv),
-                                              pack_bf16x2(o[i + 4] * inv, o[i + 5] * inv),
-                                              pack_bf16x2(o[i + 6] * inv, o[i + 7] * inv));
-                        *reinterpret_cast<uint4*>(orow + 32 * c + i) = v4;
+                    for (int q = 0; q < 32; q += 8) {
+                        uint4 v4 = make_uint4(pack_bf16x2(o[q] * inv, o[q + 1] * inv),
+                                              pack_bf16x2(o[q + 2] * inv, o[q + 3] * inv),
+                                              pack_bf16x2(o[q + 4] * inv, o[q + 5] * inv),
+                                              pack_bf16x2(o[q + 6] * inv, o[q + 7] * inv));
+                        *reinterpret_cast<uint4*>(orow + 32 * c + q) = v4;
                     }
                 }
             }
         }
     }
 
-    // ---------------------------------------------------------------- teardown
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -449,7 +487,7 @@ cudaError_t launch_impl(const Problem& pr, const WaitCtl& wc, cudaStream_t strea
     p.P = pr.pos_offset;
     p.mode = pr.mode;
     p.window = pr.window;
-    p.num_m = (pr.Lq + BM - 1) / BM;
+    p.num_m = (pr.Lq + kTiles * BM - 1) / (kTiles * BM);
     p.scale_log2 = pr.scale * kLog2e;
     p.wc = wc;
     const long long grid = (long long)p.num_m * pr.B * pr.Hq;
