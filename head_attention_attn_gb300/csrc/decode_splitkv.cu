@@ -6,10 +6,13 @@
 // range of a decode query is one interval [lo, hi) (causal at pos_offset,
 // windows, key padding); a cluster of S CTAs splits it into S contiguous chunks.
 //
-// Inside a CTA (4 warps) each warp takes batches of keys in turn:
+// Inside a CTA one producer lane streams the CTA's keys in chunks of 32 rows of K
+// and of V with bulk asynchronous copies (cp.async.bulk, completing on an mbarrier)
+// into a 6-stage shared-memory ring, so about 100 KB per CTA is in flight; four
+// compute warps take 8 keys each of every chunk:
 //   - a key row (head_dim bf16) is spread over D/8 lanes, 16 bytes per lane, read
-//     with 128-bit non-caching loads, so a warp reads 2 (D=128) or 4 (D=64)
-//     whole rows per load instruction;
+//     from shared memory with 128-bit loads, 2 (D=128) or 4 (D=64) rows per
+//     instruction;
 //   - q (pre-scaled by scale*log2(e)) lives in registers; the per-lane partial
 //     dot products of all (head, key) pairs are summed across the lanes of a
 //     row with a shuffle reduce-scatter (each level halves the values a lane
@@ -32,9 +35,11 @@
 namespace attn {
 namespace {
 
-constexpr int kWarps = 4;
-constexpr int kThreads = kWarps * 32;
-constexpr int kMaxSplits = 8;   // portable cluster size
+constexpr int kWarps = 4;                  // compute warps
+constexpr int kThreads = (kWarps + 1) * 32;  // + one producer warp
+constexpr int kMaxSplits = 8;              // portable cluster size
+constexpr int kChunk = 32;                 // keys per pipeline stage (8 per compute warp)
+constexpr int kStages = 6;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f;
 
@@ -51,23 +56,18 @@ struct DecodeParams {
 
 template <int D, int G>
 struct DCfg {
-    static constexpr int LPK = D / 8;           // lanes per key row (16 bytes each)
-    static constexpr int KPP = 32 / LPK;        // key rows per warp load instruction
-    static constexpr int NP = (D == 128) ? 4 : 2;  // load instructions (passes) per batch
-    static constexpr int KB = NP * KPP;         // keys per warp batch (8)
-    static constexpr int NV = NP * G;           // partial dot products per lane per batch
+    static constexpr int LPK = D / 8;              // lanes per key row (16 bytes each)
+    static constexpr int KPP = 32 / LPK;           // key rows per warp load instruction
+    static constexpr int NP = kChunk / kWarps / KPP;  // passes per warp batch
+    static constexpr int KB = NP * KPP;            // keys per warp batch (8)
+    static constexpr int NV = NP * G;              // partial dot products per lane per batch
     static constexpr int LEVELS = (LPK == 16) ? 4 : 3;
+    static constexpr int kRowBytes = D * 2;
+    static constexpr int kStageBytes = 2 * kChunk * kRowBytes;  // K rows then V rows
+    static constexpr int kSmem = kStages * kStageBytes + 1024;  // ring + 1 KB alignment slack
 };
 
-__device__ __forceinline__ uint4 ldg_stream(const void* p) {
-    uint4 r;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-                 : "l"(p));
-    return r;
-}
-
-// 8 bf16 (one 16-byte load) -> 4 float2 pairs (element 2i in .x, 2i+1 in .y).
+// 8 bf16 (16 bytes) -> 4 float2 pairs (element 2i in .x, 2i+1 in .y).
 __device__ __forceinline__ void bf16x8_to_f2(const uint4& u, float2 (&f)[4]) {
     const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
@@ -82,53 +82,78 @@ __device__ __forceinline__ float safe_ex2_diff(float a, float m) {
     return (m == -INFINITY) ? 0.f : ex2_approx(a - m);
 }
 
+// Bulk copy of `bytes` contiguous bytes global -> shared, completing on an mbarrier.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+    uint4 r;
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "r"(addr));
+    return r;
+}
+
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, const WaitCtl& wc) {
+    const unsigned long long t0 = globaltimer_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (globaltimer_ns() - t0 > wc.limit_ns) {
+            record_status(wc.status, kStatusTimeout);
+            return;
+        }
+    }
+}
+
 template <int D, int G>
-__global__ void __launch_bounds__(kThreads, 3) decode_splitkv_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(kThreads, 2) decode_splitkv_kernel(const DecodeParams p) {
     using C = DCfg<D, G>;
     constexpr int LPK = C::LPK, KPP = C::KPP, NP = C::NP, KB = C::KB, NV = C::NV;
+    static_assert(KB * kWarps == kChunk, "a chunk is split evenly over the compute warps");
 
+    extern __shared__ uint8_t dsmem[];
+    __shared__ __align__(8) uint64_t s_full[kStages], s_empty[kStages];
+    __shared__ int s_abort;
     __shared__ float s_p[kWarps][KPP][NV];          // per-group probabilities of the current batch
     __shared__ float s_wm[kWarps][G], s_wl[kWarps][G];
     __shared__ __align__(16) float s_wacc[kWarps][G][D];
     __shared__ float s_cm[G], s_cl[G];
     __shared__ __align__(16) float s_cacc[G][D];
 
+    const uint32_t raw = smem_u32(dsmem);
+    const uint32_t ring = raw + ((1024u - (raw & 1023u)) & 1023u);
+    volatile int* abort_flag = &s_abort;
+
     const int split = blockIdx.x;          // == rank in the cluster
     const int nsplit = gridDim.x;
     const int hk = blockIdx.y;
     const int b = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int grp = lane / LPK;            // which key row of a load instruction this lane reads
-    const int gl = lane % LPK;             // position inside the row: dims [8*gl, 8*gl+8)
 
-    // Visible interval of the single query at position P, split over the cluster.
+    // Visible interval of the single query at position P, split over the cluster in
+    // whole chunks.
     const int klen = valid_keys(p.key_lens, b, p.Lk);
     long long lo, hi;
     key_interval(p.mode, p.window, klen, p.P, p.P, &lo, &hi);
     if (hi < lo) hi = lo;
     const long long span = hi - lo;
-    long long chunk = (span + nsplit - 1) / nsplit;
-    chunk = (chunk + KB - 1) / KB * KB;
-    const long long kbeg = lo + (long long)split * chunk;
-    const long long kend = min(hi, kbeg + chunk);
-
-    // q of the G heads, my 8 dims, pre-scaled by scale*log2(e).
-    float2 qf[G][4];
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-        const __nv_bfloat16* qp = p.q + ((size_t)b * p.Hq + (size_t)hk * G + g) * D + 8 * gl;
-        const uint4 u = *reinterpret_cast<const uint4*>(qp);
-        bf16x8_to_f2(u, qf[g]);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            qf[g][i].x *= p.scale_log2;
-            qf[g][i].y *= p.scale_log2;
-        }
-    }
-
+    long long per = (span + nsplit - 1) / nsplit;
+    per = (per + kChunk - 1) / kChunk * kChunk;
+    const long long kbeg = lo + (long long)split * per;
+    const long long kend = min(hi, kbeg + per);
+    const int nchunks = (kend > kbeg) ? (int)((kend - kbeg + kChunk - 1) / kChunk) : 0;
     const size_t head_off = ((size_t)b * p.Hkv + hk) * (size_t)p.Lk * D;
-    const __nv_bfloat16* kh = p.k + head_off + 8 * gl;
-    const __nv_bfloat16* vh = p.v + head_off + 8 * gl;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kStages; ++i) {
+            mbar_init(smem_u32(&s_full[i]), 1);
+            mbar_init(smem_u32(&s_empty[i]), kWarps);
+        }
+        s_abort = 0;
+        mbar_fence_init();
+    }
+    __syncthreads();
 
     float m_run[G], l_run[G];
     float2 acc[G][4];
@@ -140,172 +165,209 @@ __global__ void __launch_bounds__(kThreads, 3) decode_splitkv_kernel(const Decod
         for (int i = 0; i < 4; ++i) acc[g][i] = make_float2(0.f, 0.f);
     }
 
-    // Value index layout of a batch: i = g * NP + pass.  The reduce-scatter
-    // halves on the high index bit first (head bits, then pass bits), so after
-    // RS levels a lane keeps KEEP consecutive passes of a single head.  Levels
-    // beyond RS (when NV < LPK) become all-reduce levels and leave identical
-    // copies in the lanes that differ only in those bits.
-    constexpr int LOG_NV = (NV >= 32) ? 5 : (NV >= 16) ? 4 : (NV >= 8) ? 3 : (NV >= 4) ? 2 : 1;
-    constexpr int RS = (LOG_NV < C::LEVELS) ? LOG_NV : C::LEVELS;
-    constexpr int KEEP = NV >> RS;                                   // values per lane after RS
-    constexpr int LOG_G = (G >= 8) ? 3 : (G >= 4) ? 2 : (G >= 2) ? 1 : 0;
-    constexpr int HEAD_LEVELS = LOG_G;                               // first RS levels: head bits
-    static_assert(KEEP >= 1 && NP % KEEP == 0, "values of a lane stay within one head");
-    static_assert(HEAD_LEVELS <= RS, "head bits are spread by reduce-scatter levels");
+    if (warp == kWarps) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            int issued = 0;
+            for (int c = 0; c < nchunks; ++c) {
+                const int st = c % kStages;
+                if (c >= kStages &&
+                    !mbar_wait(smem_u32(&s_empty[st]), (uint32_t)(c / kStages - 1) & 1, p.wc, abort_flag))
+                    break;
+                const long long k0 = kbeg + (long long)c * kChunk;
+                const int rows = (int)min((long long)kChunk, kend - k0);
+                const uint32_t bytes = (uint32_t)rows * C::kRowBytes;
+                const uint32_t dst = ring + st * C::kStageBytes;
+                const uint32_t bar = smem_u32(&s_full[st]);
+                mbar_arrive_expect_tx(bar, 2 * bytes);
+                bulk_load(dst, p.k + head_off + k0 * D, bytes, bar);
+                bulk_load(dst + kChunk * C::kRowBytes, p.v + head_off + k0 * D, bytes, bar);
+                issued = c + 1;
+            }
+            // no copy may still be writing shared memory when the block moves on
+            for (int c = (issued > kStages ? issued - kStages : 0); c < issued; ++c)
+                drain_wait(smem_u32(&s_full[c % kStages]), (uint32_t)(c / kStages) & 1, p.wc);
+        }
+    } else {
+        // ------------------------------------------------------------ compute warps
+        const int grp = lane / LPK;            // which key row of a load instruction this lane reads
+        const int gl = lane % LPK;             // position inside the row: dims [8*gl, 8*gl+8)
 
-    for (long long kb = kbeg + (long long)warp * KB; kb < kend; kb += (long long)kWarps * KB) {
-        // ---- loads (keys past the chunk end are not read)
-        uint4 kr[NP], vr[NP];
-#pragma unroll
-        for (int ps = 0; ps < NP; ++ps) {
-            const long long key = kb + ps * KPP + grp;
-            if (key < kend) {
-                kr[ps] = ldg_stream(kh + key * D);
-                vr[ps] = ldg_stream(vh + key * D);
-            } else {
-                kr[ps] = make_uint4(0, 0, 0, 0);
-                vr[ps] = make_uint4(0, 0, 0, 0);
-            }
-        }
-        // ---- partial dots over my 8 dims
-        float val[NV];
-#pragma unroll
-        for (int ps = 0; ps < NP; ++ps) {
-            float2 kf[4];
-            bf16x8_to_f2(kr[ps], kf);
-#pragma unroll
-            for (int g = 0; g < G; ++g) {
-                float2 t = __fmul2_rn(qf[g][0], kf[0]);
-                t = __ffma2_rn(qf[g][1], kf[1], t);
-                t = __ffma2_rn(qf[g][2], kf[2], t);
-                t = __ffma2_rn(qf[g][3], kf[3], t);
-                val[g * NP + ps] = t.x + t.y;
-            }
-        }
-        // ---- reduce-scatter, then all-reduce, over the LPK lanes of the row
-        int base = 0;
-#pragma unroll
-        for (int lev = 0; lev < RS; ++lev) {
-            const int mask = LPK >> (lev + 1);
-            const int half = NV >> (lev + 1);
-            const bool upper = (gl & mask) != 0;
-#pragma unroll
-            for (int t = 0; t < half; ++t) {
-                const float send = upper ? val[t] : val[t + half];
-                const float keep = upper ? val[t + half] : val[t];
-                val[t] = keep + __shfl_xor_sync(0xffffffffu, send, mask);
-            }
-            if (upper) base += half;
-        }
-#pragma unroll
-        for (int lev = RS; lev < C::LEVELS; ++lev) {
-            const int mask = LPK >> (lev + 1);
-#pragma unroll
-            for (int t = 0; t < KEEP; ++t) val[t] += __shfl_xor_sync(0xffffffffu, val[t], mask);
-        }
-        // ---- this lane's values: head gh, passes p0 .. p0+KEEP-1; mask keys past the chunk
-        const int gh = base / NP;
-        const int p0 = base % NP;
-        float bm = -INFINITY;
-#pragma unroll
-        for (int t = 0; t < KEEP; ++t) {
-            const long long key = kb + (long long)(p0 + t) * KPP + grp;
-            if (key >= kend) val[t] = -INFINITY;
-            bm = fmaxf(bm, val[t]);
-        }
-        // batch max of my head: reduce over the pass-bit levels (RS levels after the head levels)
-#pragma unroll
-        for (int lev = HEAD_LEVELS; lev < RS; ++lev)
-            bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, LPK >> (lev + 1)));
-        // every lane gathers the batch max of every head and updates the running max
-        float alpha[G];
-        bool any_rescale = false;
+        // q of the G heads, my 8 dims, pre-scaled by scale*log2(e).
+        float2 qf[G][4];
 #pragma unroll
         for (int g = 0; g < G; ++g) {
-            int src_gl = 0;  // a lane whose head bits spell g
-#pragma unroll
-            for (int lev = 0; lev < HEAD_LEVELS; ++lev)
-                if ((g >> (HEAD_LEVELS - 1 - lev)) & 1) src_gl |= LPK >> (lev + 1);
-            const float bmg = (G > 1) ? __shfl_sync(0xffffffffu, bm, grp * LPK + src_gl) : bm;
-            alpha[g] = 1.f;
-            if (bmg != -INFINITY) {
-                if (m_run[g] == -INFINITY) {
-                    m_run[g] = bmg;
-                } else if (bmg > m_run[g] + kRescaleThreshold) {
-                    alpha[g] = ex2_approx(m_run[g] - bmg);
-                    m_run[g] = bmg;
-                    any_rescale = true;
-                }
-            }
-        }
-        // ---- probabilities of my values -> shared memory (copies write identical values)
-        {
-            float mh = m_run[0];
-#pragma unroll
-            for (int g = 1; g < G; ++g) mh = (gh == g) ? m_run[g] : mh;
-#pragma unroll
-            for (int t = 0; t < KEEP; ++t) s_p[warp][grp][base + t] = safe_ex2_diff(val[t], mh);
-        }
-        __syncwarp();
-        // ---- rescale + accumulate P V for my 8 dims, every probability read from shared memory
-        if (any_rescale) {
-#pragma unroll
-            for (int g = 0; g < G; ++g) {
-                l_run[g] *= alpha[g];
-                const float2 a2 = make_float2(alpha[g], alpha[g]);
-#pragma unroll
-                for (int i = 0; i < 4; ++i) acc[g][i] = __fmul2_rn(acc[g][i], a2);
-            }
-        }
-#pragma unroll
-        for (int ps = 0; ps < NP; ++ps) {
-            float2 vf[4];
-            bf16x8_to_f2(vr[ps], vf);
-#pragma unroll
-            for (int g = 0; g < G; ++g) {
-                const float pv = s_p[warp][grp][g * NP + ps];
-                l_run[g] += pv;
-                const float2 p2 = make_float2(pv, pv);
-#pragma unroll
-                for (int i = 0; i < 4; ++i) acc[g][i] = __ffma2_rn(p2, vf[i], acc[g][i]);
-            }
-        }
-        __syncwarp();  // s_p is rewritten by the next batch
-    }
-
-    // ---------------------------------------------------------------- combine
-    // (1) the KPP row groups of the warp (same dims, different keys)
-#pragma unroll
-    for (int off = LPK; off < 32; off <<= 1) {
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-            const float mo = __shfl_xor_sync(0xffffffffu, m_run[g], off);
-            const float lo_ = __shfl_xor_sync(0xffffffffu, l_run[g], off);
-            const float mc = fmaxf(m_run[g], mo);
-            const float fa = safe_ex2_diff(m_run[g], mc);
-            const float fb = safe_ex2_diff(mo, mc);
-            l_run[g] = l_run[g] * fa + lo_ * fb;
+            const __nv_bfloat16* qp = p.q + ((size_t)b * p.Hq + (size_t)hk * G + g) * D + 8 * gl;
+            const uint4 u = *reinterpret_cast<const uint4*>(qp);
+            bf16x8_to_f2(u, qf[g]);
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                float2 other;
-                other.x = __shfl_xor_sync(0xffffffffu, acc[g][i].x, off);
-                other.y = __shfl_xor_sync(0xffffffffu, acc[g][i].y, off);
-                acc[g][i].x = acc[g][i].x * fa + other.x * fb;
-                acc[g][i].y = acc[g][i].y * fa + other.y * fb;
+                qf[g][i].x *= p.scale_log2;
+                qf[g][i].y *= p.scale_log2;
             }
-            m_run[g] = mc;
         }
-    }
-    // (2) the warps of the CTA, through shared memory
-    if (lane < LPK) {
+
+        // Value index layout of a batch: i = g * NP + pass.  The reduce-scatter
+        // halves on the high index bit first (head bits, then pass bits), so after
+        // RS levels a lane keeps KEEP consecutive passes of a single head.  Levels
+        // beyond RS (when NV < LPK) become all-reduce levels and leave identical
+        // copies in the lanes that differ only in those bits.
+        constexpr int LOG_NV = (NV >= 32) ? 5 : (NV >= 16) ? 4 : (NV >= 8) ? 3 : (NV >= 4) ? 2 : 1;
+        constexpr int RS = (LOG_NV < C::LEVELS) ? LOG_NV : C::LEVELS;
+        constexpr int KEEP = NV >> RS;
+        constexpr int HEAD_LEVELS = (G >= 8) ? 3 : (G >= 4) ? 2 : (G >= 2) ? 1 : 0;
+        static_assert(KEEP >= 1 && NP % KEEP == 0, "values of a lane stay within one head");
+        static_assert(HEAD_LEVELS <= RS, "head bits are spread by reduce-scatter levels");
+
+        for (int c = 0; c < nchunks; ++c) {
+            const int st = c % kStages;
+            if (!mbar_wait(smem_u32(&s_full[st]), (uint32_t)(c / kStages) & 1, p.wc, abort_flag)) break;
+            const long long kb = kbeg + (long long)c * kChunk + warp * KB;   // this warp's 8 keys
+            const uint32_t kst = ring + st * C::kStageBytes + (warp * KB) * C::kRowBytes + 16 * gl;
+            const uint32_t vst = kst + kChunk * C::kRowBytes;
+
+            // ---- partial dots over my 8 dims (rows past the range are not read)
+            float val[NV];
 #pragma unroll
-        for (int g = 0; g < G; ++g) {
+            for (int ps = 0; ps < NP; ++ps) {
+                const int r = ps * KPP + grp;
+                const bool valid = kb + r < kend;
+                const uint4 u = valid ? lds128(kst + r * C::kRowBytes) : make_uint4(0, 0, 0, 0);
+                float2 kf[4];
+                bf16x8_to_f2(u, kf);
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
-                *reinterpret_cast<float2*>(&s_wacc[warp][g][8 * gl + 2 * i]) = acc[g][i];
-            if (lane == 0) {
-                s_wm[warp][g] = m_run[g];
-                s_wl[warp][g] = l_run[g];
+                for (int g = 0; g < G; ++g) {
+                    float2 t = __fmul2_rn(qf[g][0], kf[0]);
+                    t = __ffma2_rn(qf[g][1], kf[1], t);
+                    t = __ffma2_rn(qf[g][2], kf[2], t);
+                    t = __ffma2_rn(qf[g][3], kf[3], t);
+                    val[g * NP + ps] = t.x + t.y;
+                }
+            }
+            // ---- reduce-scatter, then all-reduce, over the LPK lanes of the row
+            int base = 0;
+#pragma unroll
+            for (int lev = 0; lev < RS; ++lev) {
+                const int mask = LPK >> (lev + 1);
+                const int half = NV >> (lev + 1);
+                const bool upper = (gl & mask) != 0;
+#pragma unroll
+                for (int t = 0; t < half; ++t) {
+                    const float send = upper ? val[t] : val[t + half];
+                    const float keep = upper ? val[t + half] : val[t];
+                    val[t] = keep + __shfl_xor_sync(0xffffffffu, send, mask);
+                }
+                if (upper) base += half;
+            }
+#pragma unroll
+            for (int lev = RS; lev < C::LEVELS; ++lev) {
+                const int mask = LPK >> (lev + 1);
+#pragma unroll
+                for (int t = 0; t < KEEP; ++t) val[t] += __shfl_xor_sync(0xffffffffu, val[t], mask);
+            }
+            // ---- this lane's values: head gh, passes p0 .. p0+KEEP-1; mask keys past the range
+            const int gh = base / NP;
+            const int p0 = base % NP;
+            float bm = -INFINITY;
+#pragma unroll
+            for (int t = 0; t < KEEP; ++t) {
+                if (kb + (p0 + t) * KPP + grp >= kend) val[t] = -INFINITY;
+                bm = fmaxf(bm, val[t]);
+            }
+#pragma unroll
+            for (int lev = HEAD_LEVELS; lev < RS; ++lev)
+                bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, LPK >> (lev + 1)));
+            float alpha[G];
+            bool any_rescale = false;
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                int src_gl = 0;  // a lane whose head bits spell g
+#pragma unroll
+                for (int lev = 0; lev < HEAD_LEVELS; ++lev)
+                    if ((g >> (HEAD_LEVELS - 1 - lev)) & 1) src_gl |= LPK >> (lev + 1);
+                const float bmg = (G > 1) ? __shfl_sync(0xffffffffu, bm, grp * LPK + src_gl) : bm;
+                alpha[g] = 1.f;
+                if (bmg != -INFINITY) {
+                    if (m_run[g] == -INFINITY) {
+                        m_run[g] = bmg;
+                    } else if (bmg > m_run[g] + kRescaleThreshold) {
+                        alpha[g] = ex2_approx(m_run[g] - bmg);
+                        m_run[g] = bmg;
+                        any_rescale = true;
+                    }
+                }
+            }
+            {
+                float mh = m_run[0];
+#pragma unroll
+                for (int g = 1; g < G; ++g) mh = (gh == g) ? m_run[g] : mh;
+#pragma unroll
+                for (int t = 0; t < KEEP; ++t) s_p[warp][grp][base + t] = safe_ex2_diff(val[t], mh);
+            }
+            __syncwarp();
+            if (any_rescale) {
+#pragma unroll
+                for (int g = 0; g < G; ++g) {
+                    l_run[g] *= alpha[g];
+                    const float2 a2 = make_float2(alpha[g], alpha[g]);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) acc[g][i] = __fmul2_rn(acc[g][i], a2);
+                }
+            }
+            // ---- accumulate P V for my 8 dims (value rows past the range read as zeros)
+#pragma unroll
+            for (int ps = 0; ps < NP; ++ps) {
+                const int r = ps * KPP + grp;
+                const uint4 u = (kb + r < kend) ? lds128(vst + r * C::kRowBytes) : make_uint4(0, 0, 0, 0);
+                float2 vf[4];
+                bf16x8_to_f2(u, vf);
+#pragma unroll
+                for (int g = 0; g < G; ++g) {
+                    const float pv = s_p[warp][grp][g * NP + ps];
+                    l_run[g] += pv;
+                    const float2 p2 = make_float2(pv, pv);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) acc[g][i] = __ffma2_rn(p2, vf[i], acc[g][i]);
+                }
+            }
+            __syncwarp();  // s_p is rewritten by the next batch; the stage may be refilled
+            if (lane == 0) mbar_arrive(smem_u32(&s_empty[st]));
+        }
+
+        // ---------------------------------------------------------------- combine
+        // (1) the KPP row groups of the warp (same dims, different keys)
+#pragma unroll
+        for (int off = LPK; off < 32; off <<= 1) {
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                const float mo = __shfl_xor_sync(0xffffffffu, m_run[g], off);
+                const float lo_ = __shfl_xor_sync(0xffffffffu, l_run[g], off);
+                const float mc = fmaxf(m_run[g], mo);
+                const float fa = safe_ex2_diff(m_run[g], mc);
+                const float fb = safe_ex2_diff(mo, mc);
+                l_run[g] = l_run[g] * fa + lo_ * fb;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    float2 other;
+                    other.x = __shfl_xor_sync(0xffffffffu, acc[g][i].x, off);
+                    other.y = __shfl_xor_sync(0xffffffffu, acc[g][i].y, off);
+                    acc[g][i].x = acc[g][i].x * fa + other.x * fb;
+                    acc[g][i].y = acc[g][i].y * fa + other.y * fb;
+                }
+                m_run[g] = mc;
+            }
+        }
+        // (2) the warps of the CTA, through shared memory
+        if (lane < LPK) {
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    *reinterpret_cast<float2*>(&s_wacc[warp][g][8 * gl + 2 * i]) = acc[g][i];
+                if (lane == 0) {
+                    s_wm[warp][g] = m_run[g];
+                    s_wl[warp][g] = l_run[g];
+                }
             }
         }
     }
@@ -361,10 +423,25 @@ __global__ void __launch_bounds__(kThreads, 3) decode_splitkv_kernel(const Decod
 
 template <int D, int G>
 cudaError_t launch_dg(const DecodeParams& p, int B, int nsplit, cudaStream_t stream) {
+    using C = DCfg<D, G>;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    static std::mutex mu;
+    static bool configured[64] = {};
+    {
+        std::lock_guard<std::mutex> g(mu);
+        if (dev < 64 && !configured[dev]) {
+            e = cudaFuncSetAttribute(decode_splitkv_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     C::kSmem);
+            if (e != cudaSuccess) return e;
+            configured[dev] = true;
+        }
+    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)nsplit, (unsigned)p.Hkv, (unsigned)B);
     cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = 0;
+    cfg.dynamicSmemBytes = C::kSmem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;

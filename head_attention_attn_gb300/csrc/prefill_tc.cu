@@ -38,6 +38,10 @@ constexpr int kThreads = 384;     // 12 warps
 constexpr int kStages = 2;        // K/V ring depth
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f;
+// Of every kPolyPeriod column pairs, kPolyPairs take 2^x from the FMA-pipe polynomial
+// and the rest from the special-function unit, so both units share the exponentials.
+constexpr int kPolyPeriod = 8;
+constexpr int kPolyPairs = 3;
 
 template <int D>
 struct Cfg {
@@ -302,30 +306,38 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int i = j - jb;
             if (!mbar_wait(bar0 + 8 * (kBarSFull + t), (uint32_t)i & 1, p.wc, abort_flag)) { ok = false; break; }
             tc_fence_after();
-            float s[BN];
-#pragma unroll
-            for (int c = 0; c < BN / 32; ++c) tmem_ld32(tS + 32 * c, s + 32 * c);
-
             const long long tb = kv0 + (long long)j * BN;
             const int c_lo = (int)max(0LL, min((long long)BN, rlo - tb));
             const int c_hi = (int)max(0LL, min((long long)BN, rhi - tb));
             const bool full = (c_lo == 0 && c_hi == BN);
-            float ext;
-            if (sl >= 0.f) {
-                ext = -INFINITY;
-                if (full) {
-#pragma unroll
-                    for (int c = 0; c < BN; ++c) ext = fmaxf(ext, s[c]);
-                } else {
-#pragma unroll
-                    for (int c = 0; c < BN; ++c) ext = (c >= c_lo && c < c_hi) ? fmaxf(ext, s[c]) : ext;
-                }
-            } else {
-                ext = INFINITY;
-#pragma unroll
-                for (int c = 0; c < BN; ++c) ext = (c >= c_lo && c < c_hi) ? fminf(ext, s[c]) : ext;
-            }
             const bool any = c_lo < c_hi;
+
+            // Pass 1: the extreme of the raw scores over the visible columns (the max when
+            // the scale is non-negative, the min otherwise), in 8 independent chains.
+            float ext;
+            {
+                float s[BN];
+                tmem_ld128(tS, s);
+                const float fill = (sl >= 0.f) ? -INFINITY : INFINITY;
+                if (!full) {
+#pragma unroll
+                    for (int c = 0; c < BN; ++c) s[c] = (c >= c_lo && c < c_hi) ? s[c] : fill;
+                }
+                if (sl < 0.f) {
+#pragma unroll
+                    for (int c = 0; c < BN; ++c) s[c] = -s[c];
+                }
+                float e8[8];
+#pragma unroll
+                for (int q = 0; q < 8; ++q) e8[q] = s[q];
+#pragma unroll
+                for (int c = 8; c < BN; c += 16) {
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) e8[q] = fmax3(e8[q], s[c + q], (c + 8 + q < BN) ? s[c + 8 + q] : -INFINITY);
+                }
+                ext = fmax3(fmax3(e8[0], e8[1], e8[2]), fmax3(e8[3], e8[4], e8[5]), fmaxf(e8[6], e8[7]));
+                if (sl < 0.f) ext = -ext;
+            }
             float alpha = 1.f;
             bool rescale = false;
             if (any) {
@@ -339,31 +351,51 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             const float neg_m = (m_run == -INFINITY) ? 0.f : -m_run;
+            const float2 sl2 = make_float2(sl, sl), negm2 = make_float2(neg_m, neg_m);
 
-            // P (bf16 pairs) into the first 64 columns of S_t, 32 keys at a time: the A
-            // operand of P V.  S_t is already in registers, so overwriting it is safe.
+            // Pass 2: S again, 32 columns at a time with the next chunk's load in flight;
+            // P chunk k (columns 16k..16k+15) only overwrites S columns already read.
             // The row sum adds the bf16-rounded probabilities, the same numbers the
             // tensor core multiplies into V, so numerator and denominator agree.
-            float2 sum2 = make_float2(0.f, 0.f);
+            float2 sum2[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) sum2[q] = make_float2(0.f, 0.f);
+            uint32_t buf[2][32];
+            tmem_ld32_async(tS, buf[0]);
 #pragma unroll
             for (int k = 0; k < BN / 32; ++k) {
+                uint32_t* sc = buf[k & 1];
+                tmem_ld_wait32(sc);
+                if (k + 1 < BN / 32) tmem_ld32_async(tS + 32 * (k + 1), buf[(k + 1) & 1]);
                 uint32_t pk[16];
 #pragma unroll
                 for (int c2 = 0; c2 < 32; c2 += 2) {
                     const int c = 32 * k + c2;
-                    float p0 = ex2_approx(fmaf(s[c], sl, neg_m));
-                    float p1 = ex2_approx(fmaf(s[c + 1], sl, neg_m));
+                    const float2 x2 = __ffma2_rn(make_float2(__uint_as_float(sc[c2]), __uint_as_float(sc[c2 + 1])),
+                                                 sl2, negm2);
+                    float p0, p1;
+                    if ((c2 / 2) % kPolyPeriod >= kPolyPeriod - kPolyPairs) {
+                        const float2 e2 = ex2_poly2(x2);  // on the FMA pipes
+                        p0 = e2.x;
+                        p1 = e2.y;
+                    } else {
+                        p0 = ex2_approx(x2.x);  // on the special-function unit
+                        p1 = ex2_approx(x2.y);
+                    }
                     if (!full) {
                         p0 = (c >= c_lo && c < c_hi) ? p0 : 0.f;
                         p1 = (c + 1 >= c_lo && c + 1 < c_hi) ? p1 : 0.f;
                     }
                     const uint32_t w = pack_bf16x2(p0, p1);
                     pk[c2 / 2] = w;
-                    sum2 = __fadd2_rn(sum2, make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u)));
+                    sum2[(c2 / 2) & 3] = __fadd2_rn(sum2[(c2 / 2) & 3],
+                                                    make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u)));
                 }
-                tmem_st16(tS + 16 * k, pk);
+                tmem_st16_async(tS + 16 * k, pk);
             }
-            l_run = l_run * alpha + (sum2.x + sum2.y);
+            tmem_st_wait();
+            sum2[0] = __fadd2_rn(__fadd2_rn(sum2[0], sum2[1]), __fadd2_rn(sum2[2], sum2[3]));
+            l_run = l_run * alpha + (sum2[0].x + sum2[0].y);
             // O_t is stable here: the commit behind S_t(j) covers the earlier P V product.
             if (__any_sync(0xffffffffu, rescale)) {
 #pragma unroll

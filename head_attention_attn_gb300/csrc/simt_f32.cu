@@ -109,21 +109,6 @@ __global__ void __launch_bounds__(kRowsPerBlock * 32) simt_f32_kernel(const Simt
     }
 }
 
-// One block waits on a shared-memory barrier that nothing arrives on; the bounded
-// wait gives up, records the time-out in the status word, and the block returns.
-__global__ void timeout_selftest_kernel(const WaitCtl wc) {
-    __shared__ __align__(8) uint64_t bar;
-    __shared__ int abort_flag;
-    if (threadIdx.x == 0) {
-        abort_flag = 0;
-        mbar_init(smem_u32(&bar), 1);
-        mbar_fence_init();
-    }
-    __syncthreads();
-    if (threadIdx.x == 0) (void)mbar_wait(smem_u32(&bar), 0, wc, &abort_flag);
-    __syncthreads();
-}
-
 }  // namespace
 
 cudaError_t launch_simt_f32(const Problem& pr, const WaitCtl& wc, cudaStream_t stream) {
@@ -146,11 +131,6 @@ cudaError_t launch_simt_f32(const Problem& pr, const WaitCtl& wc, cudaStream_t s
     if (pr.Hq > 65535 || pr.B > 65535) return cudaErrorInvalidConfiguration;
     dim3 grid((unsigned)((pr.Lq + kRowsPerBlock - 1) / kRowsPerBlock), (unsigned)pr.Hq, (unsigned)pr.B);
     simt_f32_kernel<<<grid, kRowsPerBlock * 32, 0, stream>>>(p);
-    return cudaGetLastError();
-}
-
-cudaError_t launch_timeout_selftest(const WaitCtl& wc, cudaStream_t stream) {
-    timeout_selftest_kernel<<<1, 32, 0, stream>>>(wc);
     return cudaGetLastError();
 }
 
