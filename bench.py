@@ -414,6 +414,23 @@ def run_reference(args, rank, world):
     }
 
 
+def run_profile_case(args):
+    """A few launches of one workload and nothing else: the command ncu captures."""
+    import head_attention_attn_gb300 as attn
+    from head_attention_attn_gb300.inputs import case
+    from head_attention_attn_gb300 import build
+    build.build_library()
+    attn.load()
+    c = WORKLOADS[args.profile] if args.batch is None else case(args.profile, B=args.batch)
+    q, k, v, kl = make_inputs(c, device="cuda:0")
+    out = torch.empty_like(q)
+    for _ in range(args.warmup + args.steps):
+        attn.attn_fwd(q, k, v, out, pos_offset=c.pos_offset, mask_mode=c.mask_mode, window=c.window, key_lens=kl)
+    torch.cuda.synchronize()
+    attn.check_device_status()
+    print(json.dumps({"profile": args.profile, "batch": c.B, "launches": args.warmup + args.steps}))
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -423,8 +440,15 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-rows", type=int, default=64)
+    ap.add_argument("--profile", choices=sorted(WORKLOADS), default=None,
+                    help="only run --warmup + --steps launches of one workload (for profilers)")
+    ap.add_argument("--batch", type=int, default=None, help="batch size override for --profile")
     args = ap.parse_args(argv)
-    args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps
+    if args.profile is None:
+        args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps
+    if args.profile is not None:
+        run_profile_case(args)
+        return
     rank, world, local = dist_setup()
     if args.impl == "reference":
         res = run_reference(args, rank, world)

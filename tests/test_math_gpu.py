@@ -19,7 +19,7 @@ def test_exp2_routines_meet_their_error_bounds():
     rel_unit = ((yu.double().cpu() - exact) / exact).abs().max().item()
     assert rel_poly < 1e-4, rel_poly
     assert rel_unit < 1e-6, rel_unit
-    # below the clamp the polynomial returns 2^-125 and the unit returns (flushed) zero
+    # below the clamp the polynomial returns 2^-125 (within its error bound) and the unit flushes to zero
     ninf = torch.tensor([-float("inf"), -200.0], device="cuda")
     yp, yu = attn.selftest_exp2(ninf)
-    assert torch.all(yp == 2.0 ** -125) and torch.all(yu == 0)
+    assert torch.all((yp.double() / 2.0 ** -125 - 1).abs() < 1e-4) and torch.all(yu == 0)
