@@ -8,8 +8,8 @@
 //
 // Inside a CTA one producer lane streams the CTA's keys in chunks of 32 rows of K
 // and of V with bulk asynchronous copies (cp.async.bulk, completing on an mbarrier)
-// into a 6-stage shared-memory ring, so about 100 KB per CTA is in flight; four
-// compute warps take 8 keys each of every chunk:
+// into a 4-stage shared-memory ring of 48-key stages, so about 100 KB per CTA is in
+// flight; six compute warps take 8 keys each of every chunk:
 //   - a key row (head_dim bf16) is spread over D/8 lanes, 16 bytes per lane, read
 //     from shared memory with 128-bit loads, 2 (D=128) or 4 (D=64) rows per
 //     instruction;
@@ -20,7 +20,7 @@
 //   - a lane-group running max and sum per head (base-2 exponent, O rescaled
 //     only when the max grows by more than 2^8) and fp32 accumulators of P V
 //     for the lane's 8 head dims, with packed f32x2 FMAs.
-// Combine: the two lane groups of a warp merge with shuffles, the 4 warps merge
+// Combine: the lane groups of a warp merge with shuffles, the 6 warps merge
 // through shared memory, and the S CTAs of the cluster merge through
 // distributed shared memory in CTA rank 0, which normalises and stores bf16.
 // No global scratch memory is used.
@@ -35,11 +35,11 @@
 namespace attn {
 namespace {
 
-constexpr int kWarps = 4;                  // compute warps
+constexpr int kWarps = 6;                  // compute warps
 constexpr int kThreads = (kWarps + 1) * 32;  // + one producer warp
 constexpr int kMaxSplits = 8;              // portable cluster size
-constexpr int kChunk = 32;                 // keys per pipeline stage (8 per compute warp)
-constexpr int kStages = 6;
+constexpr int kChunk = 8 * kWarps;         // keys per pipeline stage (8 per compute warp)
+constexpr int kStages = 4;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f;
 
@@ -115,7 +115,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_splitkv_kernel(const Decod
     extern __shared__ uint8_t dsmem[];
     __shared__ __align__(8) uint64_t s_full[kStages], s_empty[kStages];
     __shared__ int s_abort;
-    __shared__ float s_p[kWarps][KPP][NV];          // per-group probabilities of the current batch
+    __shared__ __align__(16) float s_p[kWarps][KPP][NP][G];  // probabilities of the current batch, [pass][head]
     __shared__ float s_wm[kWarps][G], s_wl[kWarps][G];
     __shared__ __align__(16) float s_wacc[kWarps][G][D];
     __shared__ float s_cm[G], s_cl[G];
@@ -219,6 +219,15 @@ __global__ void __launch_bounds__(kThreads, 2) decode_splitkv_kernel(const Decod
         static_assert(KEEP >= 1 && NP % KEEP == 0, "values of a lane stay within one head");
         static_assert(HEAD_LEVELS <= RS, "head bits are spread by reduce-scatter levels");
 
+        // Lanes that differ only in all-reduce bits hold copies of the same values; one
+        // of them (all-reduce bits zero) owns the row sums of its head.
+        int ar_mask = 0;
+#pragma unroll
+        for (int lev = RS; lev < C::LEVELS; ++lev) ar_mask |= LPK >> (lev + 1);
+        const bool owner = (gl & ar_mask) == 0;
+        float l_own = 0.f;
+        int gh_lane = 0;
+
         for (int c = 0; c < nchunks; ++c) {
             const int st = c % kStages;
             if (!mbar_wait(smem_u32(&s_full[st]), (uint32_t)(c / kStages) & 1, p.wc, abort_flag)) break;
@@ -268,6 +277,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_splitkv_kernel(const Decod
             // ---- this lane's values: head gh, passes p0 .. p0+KEEP-1; mask keys past the range
             const int gh = base / NP;
             const int p0 = base % NP;
+            gh_lane = gh;
             float bm = -INFINITY;
 #pragma unroll
             for (int t = 0; t < KEEP; ++t) {
@@ -298,17 +308,26 @@ __global__ void __launch_bounds__(kThreads, 2) decode_splitkv_kernel(const Decod
                 }
             }
             {
-                float mh = m_run[0];
+                float mh = m_run[0], ah = alpha[0];
 #pragma unroll
-                for (int g = 1; g < G; ++g) mh = (gh == g) ? m_run[g] : mh;
+                for (int g = 1; g < G; ++g) {
+                    mh = (gh == g) ? m_run[g] : mh;
+                    ah = (gh == g) ? alpha[g] : ah;
+                }
+                float ps_sum = 0.f;
 #pragma unroll
-                for (int t = 0; t < KEEP; ++t) s_p[warp][grp][base + t] = safe_ex2_diff(val[t], mh);
+                for (int t = 0; t < KEEP; ++t) {
+                    const float pt = safe_ex2_diff(val[t], mh);
+                    s_p[warp][grp][p0 + t][gh] = pt;
+                    ps_sum += pt;
+                }
+                // the lane owning these probabilities (not an all-reduce copy) keeps their sum
+                l_own = l_own * ah + (owner ? ps_sum : 0.f);
             }
             __syncwarp();
             if (any_rescale) {
 #pragma unroll
                 for (int g = 0; g < G; ++g) {
-                    l_run[g] *= alpha[g];
                     const float2 a2 = make_float2(alpha[g], alpha[g]);
 #pragma unroll
                     for (int i = 0; i < 4; ++i) acc[g][i] = __fmul2_rn(acc[g][i], a2);
@@ -321,11 +340,23 @@ __global__ void __launch_bounds__(kThreads, 2) decode_splitkv_kernel(const Decod
                 const uint4 u = (kb + r < kend) ? lds128(vst + r * C::kRowBytes) : make_uint4(0, 0, 0, 0);
                 float2 vf[4];
                 bf16x8_to_f2(u, vf);
+                float pv[G];
+                if constexpr (G % 4 == 0) {
+#pragma unroll
+                    for (int g = 0; g < G; g += 4) {
+                        const float4 p4 = *reinterpret_cast<const float4*>(&s_p[warp][grp][ps][g]);
+                        pv[g] = p4.x;
+                        pv[g + 1] = p4.y;
+                        pv[g + 2] = p4.z;
+                        pv[g + 3] = p4.w;
+                    }
+                } else {
+#pragma unroll
+                    for (int g = 0; g < G; ++g) pv[g] = s_p[warp][grp][ps][g];
+                }
 #pragma unroll
                 for (int g = 0; g < G; ++g) {
-                    const float pv = s_p[warp][grp][g * NP + ps];
-                    l_run[g] += pv;
-                    const float2 p2 = make_float2(pv, pv);
+                    const float2 p2 = make_float2(pv[g], pv[g]);
 #pragma unroll
                     for (int i = 0; i < 4; ++i) acc[g][i] = __ffma2_rn(p2, vf[i], acc[g][i]);
                 }
@@ -335,6 +366,23 @@ __global__ void __launch_bounds__(kThreads, 2) decode_splitkv_kernel(const Decod
         }
 
         // ---------------------------------------------------------------- combine
+        // (0) row sums: add the owners' partial sums over the pass-bit and all-reduce
+        // lanes of each head, then every lane gathers the sum of every head
+        {
+            float lsum = l_own;
+#pragma unroll
+            for (int lev = HEAD_LEVELS; lev < C::LEVELS; ++lev)
+                lsum += __shfl_xor_sync(0xffffffffu, lsum, LPK >> (lev + 1));
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                int src_gl = 0;
+#pragma unroll
+                for (int lev = 0; lev < HEAD_LEVELS; ++lev)
+                    if ((g >> (HEAD_LEVELS - 1 - lev)) & 1) src_gl |= LPK >> (lev + 1);
+                l_run[g] = (G > 1) ? __shfl_sync(0xffffffffu, lsum, grp * LPK + src_gl) : lsum;
+            }
+            (void)gh_lane;
+        }
         // (1) the KPP row groups of the warp (same dims, different keys)
 #pragma unroll
         for (int off = LPK; off < 32; off <<= 1) {
