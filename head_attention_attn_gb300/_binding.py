@@ -16,8 +16,8 @@ ATTN_OK, ATTN_ERR_INVALID_ARG, ATTN_ERR_UNSUPPORTED, ATTN_ERR_CUDA, ATTN_ERR_TIM
 MASK_NONE, MASK_CAUSAL, MASK_WINDOW, MASK_CAUSAL_WINDOW = 0, 1, 2, 3
 ATTN_BF16, ATTN_F32 = 0, 1
 
-EXPORTED = ("attn_fwd", "attn_last_error", "attn_sync_status", "attn_selftest_timeout", "attn_selftest_exp2",
-            "attn_version")
+EXPORTED = ("attn_fwd", "attn_decode_caches", "attn_last_error", "attn_sync_status", "attn_selftest_timeout",
+            "attn_selftest_exp2", "attn_version")
 
 _STATUS_NAMES = {0: "ATTN_OK", 1: "ATTN_ERR_INVALID_ARG", 2: "ATTN_ERR_UNSUPPORTED", 3: "ATTN_ERR_CUDA",
                  4: "ATTN_ERR_TIMEOUT"}
@@ -52,6 +52,8 @@ def load(path: str | None = None):
         vp, ci = ctypes.c_void_p, ctypes.c_int
         lib.attn_fwd.restype = ci
         lib.attn_fwd.argtypes = [vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, ci, ci, ci, vp, ctypes.c_float, ci, vp]
+        lib.attn_decode_caches.restype = ci
+        lib.attn_decode_caches.argtypes = [vp, vp, vp, vp, ci, ci, ci, ci, ci, vp, ci, ctypes.c_float, ci, vp]
         lib.attn_last_error.restype = ctypes.c_char_p
         lib.attn_last_error.argtypes = []
         lib.attn_sync_status.restype = ci
@@ -137,6 +139,52 @@ def attn_fwd(q, k, v, out=None, *, pos_offset: int = 0, mask_mode: int = MASK_NO
                           int(pos_offset), int(mask_mode), int(window), kl_ptr, float(scale), dtype,
                           _stream_handle(stream))
     _check(status)
+    return out
+
+
+def attn_decode_caches(q, k_caches, v_caches, kv_lens, out=None, *, sliding_window: int = 0,
+                       scale: float | None = None, stream=None):
+    """One decode step for m items against per-item caches (see attn_decode_caches in attn.h).
+
+    q: [m, Hq, D] bf16 CUDA tensor; k_caches, v_caches: sequences of m [Hkv, capacity, D]
+    bf16 CUDA tensors (or int64 CUDA tensors of m device addresses); kv_lens: int32 CUDA [m].
+    The pointer arrays are built here (device tensors kept alive until the call is enqueued
+    and the stream reaches it; this function synchronises nothing).
+    """
+    import torch
+    if not q.is_cuda or q.dtype != torch.bfloat16 or q.dim() != 3 or not q.is_contiguous():
+        raise ValueError("q must be a contiguous bf16 CUDA tensor [m, Hq, D]")
+    m, Hq, D = q.shape
+
+    def ptrs(caches):
+        if isinstance(caches, torch.Tensor) and caches.dtype == torch.int64:
+            return caches, None
+        caches = list(caches)
+        if len(caches) != m:
+            raise ValueError("one cache per item is required")
+        shape = caches[0].shape
+        for t in caches:
+            if not t.is_cuda or t.dtype != torch.bfloat16 or not t.is_contiguous() or t.shape != shape:
+                raise ValueError("caches must be contiguous bf16 CUDA tensors of one shape [Hkv, capacity, D]")
+        arr = torch.tensor([t.data_ptr() for t in caches], dtype=torch.int64, device=q.device)
+        return arr, shape
+
+    kp, kshape = ptrs(k_caches)
+    vp_, vshape = ptrs(v_caches)
+    if kshape is None or vshape is None or kshape != vshape or kshape[2] != D:
+        raise ValueError("k and v caches must share a shape [Hkv, capacity, D] matching q")
+    Hkv, capacity = int(kshape[0]), int(kshape[1])
+    if kv_lens.dtype != torch.int32 or not kv_lens.is_cuda or kv_lens.numel() != m:
+        raise ValueError("kv_lens must be an int32 CUDA tensor with m entries")
+    if out is None:
+        out = torch.empty_like(q)
+    if scale is None:
+        scale = float(torch.tensor(1.0 / math.sqrt(D), dtype=torch.float32).item())
+    status = load().attn_decode_caches(q.data_ptr(), kp.data_ptr(), vp_.data_ptr(), out.data_ptr(), m, Hq, Hkv,
+                                       capacity, D, kv_lens.data_ptr(), int(sliding_window), ctypes.c_float(scale),
+                                       ATTN_BF16, _stream_handle(stream))
+    _check(status)
+    out._attn_keepalive = (kp, vp_)  # the pointer arrays must outlive the queued launch
     return out
 
 

@@ -14,6 +14,7 @@ namespace attn {
 
 // Status codes written to the device status word (same numbers as attn_status).
 constexpr unsigned kStatusTimeout = 4u;
+constexpr unsigned kStatusBadPointer = 5u;  // a device-side pointer argument was null or misaligned
 
 // Arguments every kernel receives for its bounded waits.
 struct WaitCtl {

@@ -30,6 +30,7 @@
 // launch for all items, device-side lengths, sliding window = last w positions).
 #include "kernels.h"
 
+#include <algorithm>
 #include <mutex>
 
 namespace attn {
@@ -45,11 +46,14 @@ constexpr float kRescaleThreshold = 8.0f;
 
 struct DecodeParams {
     const __nv_bfloat16* q;
-    const __nv_bfloat16* k;
+    const __nv_bfloat16* k;           // contiguous caches [B, Hkv, Lk, D] (k/v), or
     const __nv_bfloat16* v;
+    const __nv_bfloat16* const* kc;   // per-item caches: device arrays of B pointers, each
+    const __nv_bfloat16* const* vc;   // [Hkv, Lk, D] with Lk the capacity (null: contiguous)
     __nv_bfloat16* out;
-    const int32_t* key_lens;
+    const int32_t* key_lens;          // per-item valid lengths (required with per-item caches)
     int Hq, Hkv, Lk, P, mode, window;
+    int sliding;                      // per-item caches: attend to the last `sliding` keys (0: all)
     float scale_log2;
     WaitCtl wc;
 };
@@ -131,11 +135,33 @@ __global__ void __launch_bounds__(kThreads, 2) decode_splitkv_kernel(const Decod
     const int b = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-    // Visible interval of the single query at position P, split over the cluster in
-    // whole chunks.
+    // Visible interval of the single query, split over the cluster in whole chunks.
+    // Contiguous caches: the query sits at position P and the mask mode applies.
+    // Per-item caches: the query is the newest of the item's kv_lens[b] positions and
+    // sees them all, or the last `sliding` of them.
     const int klen = valid_keys(p.key_lens, b, p.Lk);
     long long lo, hi;
-    key_interval(p.mode, p.window, klen, p.P, p.P, &lo, &hi);
+    const __nv_bfloat16* kbase;
+    const __nv_bfloat16* vbase;
+    if (p.kc != nullptr) {
+        kbase = p.kc[b];
+        vbase = p.vc[b];
+        lo = (p.sliding > 0 && klen > p.sliding) ? (long long)(klen - p.sliding) : 0;
+        hi = klen;
+        const bool bad = kbase == nullptr || vbase == nullptr ||
+                         ((reinterpret_cast<uintptr_t>(kbase) | reinterpret_cast<uintptr_t>(vbase)) & 15u) != 0;
+        if (bad) {
+            if (threadIdx.x == 0) record_status(p.wc.status, kStatusBadPointer);
+            lo = hi = 0;  // nothing is read; the item's output is written as zeros
+        }
+        kbase += (size_t)hk * (size_t)p.Lk * D;
+        vbase += (size_t)hk * (size_t)p.Lk * D;
+    } else {
+        key_interval(p.mode, p.window, klen, p.P, p.P, &lo, &hi);
+        const size_t head_off = ((size_t)b * p.Hkv + hk) * (size_t)p.Lk * D;
+        kbase = p.k + head_off;
+        vbase = p.v + head_off;
+    }
     if (hi < lo) hi = lo;
     const long long span = hi - lo;
     long long per = (span + nsplit - 1) / nsplit;
@@ -143,7 +169,6 @@ __global__ void __launch_bounds__(kThreads, 2) decode_splitkv_kernel(const Decod
     const long long kbeg = lo + (long long)split * per;
     const long long kend = min(hi, kbeg + per);
     const int nchunks = (kend > kbeg) ? (int)((kend - kbeg + kChunk - 1) / kChunk) : 0;
-    const size_t head_off = ((size_t)b * p.Hkv + hk) * (size_t)p.Lk * D;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kStages; ++i) {
@@ -180,8 +205,8 @@ __global__ void __launch_bounds__(kThreads, 2) decode_splitkv_kernel(const Decod
                 const uint32_t dst = ring + st * C::kStageBytes;
                 const uint32_t bar = smem_u32(&s_full[st]);
                 mbar_arrive_expect_tx(bar, 2 * bytes);
-                bulk_load(dst, p.k + head_off + k0 * D, bytes, bar);
-                bulk_load(dst + kChunk * C::kRowBytes, p.v + head_off + k0 * D, bytes, bar);
+                bulk_load(dst, kbase + k0 * D, bytes, bar);
+                bulk_load(dst + kChunk * C::kRowBytes, vbase + k0 * D, bytes, bar);
                 issued = c + 1;
             }
             // no copy may still be writing shared memory when the block moves on
@@ -525,6 +550,9 @@ cudaError_t launch_decode_splitkv(const Problem& pr, const WaitCtl& wc, cudaStre
     p.q = reinterpret_cast<const __nv_bfloat16*>(pr.q);
     p.k = reinterpret_cast<const __nv_bfloat16*>(pr.k);
     p.v = reinterpret_cast<const __nv_bfloat16*>(pr.v);
+    p.kc = nullptr;
+    p.vc = nullptr;
+    p.sliding = 0;
     p.out = reinterpret_cast<__nv_bfloat16*>(pr.out);
     p.key_lens = pr.key_lens;
     p.Hq = pr.Hq;
@@ -544,6 +572,35 @@ cudaError_t launch_decode_splitkv(const Problem& pr, const WaitCtl& wc, cudaStre
     const int G = pr.Hq / pr.Hkv;
     if (pr.D == 64) return launch_d<64>(p, G, pr.B, nsplit, stream);
     return launch_d<128>(p, G, pr.B, nsplit, stream);
+}
+
+cudaError_t launch_decode_caches(const CachesProblem& cp, const WaitCtl& wc, cudaStream_t stream, int num_sms) {
+    DecodeParams p;
+    p.q = reinterpret_cast<const __nv_bfloat16*>(cp.q);
+    p.k = nullptr;
+    p.v = nullptr;
+    p.kc = reinterpret_cast<const __nv_bfloat16* const*>(cp.k_caches);
+    p.vc = reinterpret_cast<const __nv_bfloat16* const*>(cp.v_caches);
+    p.out = reinterpret_cast<__nv_bfloat16*>(cp.out);
+    p.key_lens = cp.kv_lens;
+    p.Hq = cp.Hq;
+    p.Hkv = cp.Hkv;
+    p.Lk = cp.capacity;
+    p.P = 0;
+    p.mode = 0;
+    p.window = 0;
+    p.sliding = cp.sliding;
+    p.scale_log2 = cp.scale * kLog2e;
+    p.wc = wc;
+    if (cp.Hkv > 65535 || cp.m > 65535) return cudaErrorInvalidConfiguration;
+    const long long units = (long long)cp.m * cp.Hkv;
+    long long want = (8LL * (num_sms > 0 ? num_sms : 148) + units - 1) / units;
+    long long span = cp.sliding > 0 ? std::min(cp.sliding, cp.capacity) : cp.capacity;
+    long long by_len = (span + 255) / 256;
+    int nsplit = (int)std::max(1LL, std::min<long long>(kMaxSplits, std::min(want, by_len)));
+    const int G = cp.Hq / cp.Hkv;
+    if (cp.D == 64) return launch_d<64>(p, G, cp.m, nsplit, stream);
+    return launch_d<128>(p, G, cp.m, nsplit, stream);
 }
 
 }  // namespace attn

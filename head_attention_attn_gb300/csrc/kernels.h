@@ -58,6 +58,20 @@ cudaError_t launch_prefill_tc(const Problem& p, const WaitCtl& wc, cudaStream_t 
 bool decode_supported(const Problem& p);
 cudaError_t launch_decode_splitkv(const Problem& p, const WaitCtl& wc, cudaStream_t stream, int num_sms);
 
+// K2 over per-item caches: one single-query decode step for m items, item i reading its
+// own [Hkv, capacity, D] K and V caches through device pointer arrays.
+struct CachesProblem {
+    const void* q;
+    const void* const* k_caches;
+    const void* const* v_caches;
+    void* out;
+    int m, Hq, Hkv, capacity, D;
+    const int32_t* kv_lens;
+    int sliding;
+    float scale;
+};
+cudaError_t launch_decode_caches(const CachesProblem& p, const WaitCtl& wc, cudaStream_t stream, int num_sms);
+
 // K3: fp32 SIMT attention, any head_dim in [1, 256].
 cudaError_t launch_simt_f32(const Problem& p, const WaitCtl& wc, cudaStream_t stream);
 

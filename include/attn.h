@@ -130,6 +130,45 @@ ATTN_API attn_status attn_fwd(const void* q, const void* k, const void* v, void*
                      float scale, int dtype, void* cuda_stream);
 
 /*
+ * attn_decode_caches -- one decode step for m items, each against its own KV cache, in
+ * one launch.
+ *
+ * Source: ferrum-kernels Backend::flash_attention_batched_per_cache, the batched decode
+ * across M per-request caches that replaces the per-item flash_attention(q_len=1) loop.
+ *
+ * Arguments:
+ *   q, out     [m, q_heads, head_dim] bf16, item-major, contiguous, 16-byte aligned.
+ *   k_caches, v_caches
+ *              Device arrays of m device pointers.  Item i's K (and V) cache is
+ *              [kv_heads, capacity, head_dim] bf16, head-major and contiguous; each
+ *              pointer must be 16-byte aligned.
+ *   kv_lens    Device int32 [m]: the valid cached positions of item i.  The value is
+ *              clamped to [0, capacity].  It is read on the device, so a captured launch
+ *              replays with new lengths written between launches.
+ *   sliding_window
+ *              0: item i's query, the newest position kv_lens[i]-1, sees positions
+ *              0 .. kv_lens[i]-1.  w > 0: it sees only the last w of them.
+ *   scale      Finite multiplier of the raw dot products.
+ *   dtype      Must be ATTN_BF16.
+ *
+ * Query head h reads kv head h / (q_heads / kv_heads).
+ *
+ * Supported: head_dim 64 or 128, and q_heads / kv_heads in {1, 2, 4, 8}; otherwise
+ * ATTN_ERR_UNSUPPORTED.  An item with kv_lens[i] == 0 gets zeros.  capacity 0 zero-fills
+ * out.
+ *
+ * Errors: host-visible arguments are checked as for attn_fwd.  A null or misaligned
+ * pointer inside the device arrays is found on the device: that item is not read,
+ * its output is zeros, and attn_sync_status() reports ATTN_ERR_INVALID_ARG.
+ *
+ * The library allocates nothing and keeps no pointer after the call.
+ */
+ATTN_API attn_status attn_decode_caches(const void* q, const void* const* k_caches, const void* const* v_caches,
+                                        void* out, int m, int q_heads, int kv_heads, int capacity, int head_dim,
+                                        const int32_t* kv_lens, int sliding_window, float scale, int dtype,
+                                        void* cuda_stream);
+
+/*
  * attn_last_error -- message for the last non-OK status returned on this host thread.
  * The string belongs to the library and stays valid until the next call on this
  * thread.  The result is "" when there has been no error.
@@ -144,6 +183,8 @@ ATTN_API const char* attn_last_error(void);
  * records a code in this word, releases what it holds, and exits its block.
  * Returns:
  *   - ATTN_ERR_TIMEOUT when a wait gave up;
+ *   - ATTN_ERR_INVALID_ARG when a kernel found a bad device-side pointer
+ *     (attn_decode_caches);
  *   - ATTN_ERR_CUDA when the stream reported an error;
  *   - ATTN_OK otherwise.
  * Source: ferrum-kernels Backend::sync, where sync is separate from the launch.

@@ -114,3 +114,31 @@ def test_library_has_no_host_fallback_symbols(lib):
     out = os.popen(f"nm -D {attn.library_path()}").read()
     assert "oracle" not in out
     assert isinstance(ctypes.CDLL(attn.library_path()), ctypes.CDLL)
+
+
+def _caches_call(lib, **kw):
+    args = dict(q=16, kc=16, vc=16, out=16, m=2, hq=8, hkv=2, cap=64, d=128, lens=16, win=0, scale=0.1,
+                dtype=attn.ATTN_BF16, stream=None)
+    args.update(kw)
+    return lib.attn_decode_caches(args["q"], args["kc"], args["vc"], args["out"], args["m"], args["hq"], args["hkv"],
+                                  args["cap"], args["d"], args["lens"], args["win"], ctypes.c_float(args["scale"]),
+                                  args["dtype"], args["stream"])
+
+
+@pytest.mark.parametrize("change,status", [
+    (dict(m=-1), attn.ATTN_ERR_INVALID_ARG),
+    (dict(cap=-1), attn.ATTN_ERR_INVALID_ARG),
+    (dict(hq=6, hkv=4), attn.ATTN_ERR_INVALID_ARG),
+    (dict(win=-2), attn.ATTN_ERR_INVALID_ARG),
+    (dict(scale=float("nan")), attn.ATTN_ERR_INVALID_ARG),
+    (dict(lens=None), attn.ATTN_ERR_INVALID_ARG),
+    (dict(kc=None), attn.ATTN_ERR_INVALID_ARG),
+    (dict(q=24), attn.ATTN_ERR_INVALID_ARG),
+    (dict(kc=12), attn.ATTN_ERR_INVALID_ARG),
+    (dict(dtype=attn.ATTN_F32), attn.ATTN_ERR_UNSUPPORTED),
+    (dict(d=96), attn.ATTN_ERR_UNSUPPORTED),
+    (dict(hq=6, hkv=2), attn.ATTN_ERR_UNSUPPORTED),
+    (dict(m=0), attn.ATTN_OK),
+])
+def test_decode_caches_arguments(lib, change, status):
+    assert _caches_call(lib, **change) == status
