@@ -304,7 +304,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
         for (int j = jb; j < je; ++j) {
             const int i = j - jb;
-            if (!mbar_wait(bar0 + 8 * (kBarSFull + t), (uint32_t)i & 1, p.wc, abort_flag)) { ok = false; break; }
+            // every lane waits; the warp continues only if all lanes saw the phase, so the
+            // warp-collective tcgen05 operations below never run with a partial warp
+            if (!__all_sync(0xffffffffu, mbar_wait(bar0 + 8 * (kBarSFull + t), (uint32_t)i & 1, p.wc, abort_flag))) {
+                ok = false;
+                break;
+            }
             tc_fence_after();
             const long long tb = kv0 + (long long)j * BN;
             const int c_lo = (int)max(0LL, min((long long)BN, rlo - tb));
@@ -415,7 +420,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------------------ epilogue
         const bool has = je > jb;
         if (ok && has) {
-            ok = mbar_wait(bar0 + 8 * (kBarOFull + t), 0, p.wc, abort_flag);
+            ok = __all_sync(0xffffffffu, mbar_wait(bar0 + 8 * (kBarOFull + t), 0, p.wc, abort_flag));
             tc_fence_after();
         }
         if (ok && q0 + t * BM < p.Lq) {
