@@ -5,13 +5,15 @@
 //   warp 0       TMA producer: both Q tiles once, then 128-key K and V tiles
 //                through 2-stage shared-memory rings (128-byte swizzle).
 //   warp 1       TMEM owner (all 512 columns) and single-thread MMA issuer.
-//   warps 4-7    softmax of query tile 0, warps 8-11 softmax of query tile 1:
-//                one thread per row reads its S row from TMEM, masks, keeps the
-//                running max and sum (2^x with scale*log2(e) folded in), and
-//                writes P as packed bf16 back into the same TMEM columns.
-//   warps 2-3    idle.
-// TMEM: S0 | S1 | O0 | O1, 128 columns each; P_t aliases the first 64 columns
-// of S_t.  The MMA order is the ping-pong
+//   warps 2-17   softmax, 8 warps per query tile: a row of S is split between two
+//                threads, one per half of the 128 key columns.  Each thread reads its 64
+//                scores from TMEM, the two halves exchange their row maxima through
+//                shared memory, and each writes its 64 probabilities (2^x on the
+//                special-function unit, scale*log2(e) folded in) back into TMEM as
+//                packed bf16.  After the tile's last key block each half normalises
+//                and stores its half of the head dims of the row.
+// TMEM: S0 | S1 | O0 | O1, 128 columns each; P_t aliases the first 64 columns of S_t.
+// The MMA order is the ping-pong
 //   PV0(j-1), QK0(j), PV1(j-1), QK1(j)
 // so the tensor core works on one tile while the other tile's softmax runs:
 //   QK_t(j):  S_t  = Q_t K_j^T   (A, B from shared memory, K-major)
@@ -34,14 +36,10 @@ namespace {
 constexpr int BM = 128;           // query rows per tile
 constexpr int BN = 128;           // keys per tile
 constexpr int kTiles = 2;         // query tiles per CTA
-constexpr int kThreads = 384;     // 12 warps
+constexpr int kThreads = 576;     // 18 warps: producer, MMA, 16 softmax warps
 constexpr int kStages = 2;        // K/V ring depth
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f;
-// Of every kPolyPeriod column pairs, kPolyPairs take 2^x from the FMA-pipe polynomial
-// and the rest from the special-function unit, so both units share the exponentials.
-constexpr int kPolyPeriod = 8;
-constexpr int kPolyPairs = 3;
 
 template <int D>
 struct Cfg {
@@ -51,7 +49,9 @@ struct Cfg {
     static constexpr int kOffQ = 0;
     static constexpr int kOffK = kOffQ + kTiles * kQBytes;
     static constexpr int kOffV = kOffK + kStages * kKVBytes;
-    static constexpr int kOffBar = kOffV + kStages * kKVBytes;
+    static constexpr int kOffX = kOffV + kStages * kKVBytes;          // row-extreme exchange
+    static constexpr int kOffL = kOffX + kTiles * 2 * BM * 4;         // row-sum exchange
+    static constexpr int kOffBar = kOffL + kTiles * 2 * BM * 4;
     static constexpr int kSmem = kOffBar + 256 + 1024;
     static constexpr uint32_t kTmemCols = 512;
     static constexpr uint32_t kColS = 0;    // + 128 * tile
@@ -68,9 +68,10 @@ enum : int {
     kBarPFull = kBarSFull + kTiles,    // + tile
     kBarOFull = kBarPFull + kTiles,    // + tile: the tile's last P V product completed
     kBarMmaDone = kBarOFull + kTiles,
-    kNumBars = kBarMmaDone + 1,
+    kBarXch = kBarMmaDone + 1,          // + tile: both halves of the tile posted their row values
+    kNumBars = kBarXch + kTiles,
 };
-static_assert(kNumBars * 8 <= 128, "barrier area");
+static_assert(kNumBars * 8 <= 240, "barrier area");
 
 struct PrefillParams {
     __nv_bfloat16* out;
@@ -102,6 +103,35 @@ __device__ __forceinline__ void tc_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint
         : "memory");
 }
 
+
+// Load 64 consecutive fp32 columns (two 32-column loads, one wait).
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, float* r) {
+    uint32_t* u = reinterpret_cast<uint32_t*>(r);
+    tmem_ld32_async(taddr, u);
+    tmem_ld32_async(taddr + 32, u + 32);
+    tmem_ld_wait32(u);
+    tmem_ld_wait32(u + 32);
+}
+
+__device__ __forceinline__ float row_max64(const float* s) {
+    float e8[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) e8[q] = fmaxf(s[q], s[8 + q]);
+#pragma unroll
+    for (int c = 16; c < 64; c += 16) {
+#pragma unroll
+        for (int q = 0; q < 8; ++q) e8[q] = fmax3(e8[q], s[c + q], s[c + 8 + q]);
+    }
+    return fmax3(fmax3(e8[0], e8[1], e8[2]), fmax3(e8[3], e8[4], e8[5]), fmaxf(e8[6], e8[7]));
+}
+
+__device__ __forceinline__ float row_min64(const float* s) {
+    float m = s[0];
+#pragma unroll
+    for (int c = 1; c < 64; ++c) m = fminf(m, s[c]);
+    return m;
+}
+
 // Key tiles of one query tile: [jb, je) in units of BN keys from kv0.
 struct TileRange {
     int jb, je;
@@ -117,8 +147,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* smem = smem_raw + ((1024u - (raw_s & 1023u)) & 1023u);
     const uint32_t sbase = smem_u32(smem);
     const uint32_t bar0 = sbase + C::kOffBar;
-    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::kOffBar + 128);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffBar + 136);
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::kOffBar + 240);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffBar + 248);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -165,7 +195,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         for (int i = 0; i < kNumBars; ++i) {
             uint32_t count = 1;
-            if (i >= kBarPFull && i < kBarPFull + kTiles) count = 4;  // one arrival per softmax warp
+            if ((i >= kBarPFull && i < kBarPFull + kTiles) || (i >= kBarXch && i < kBarXch + kTiles))
+                count = 8;  // one arrival per softmax warp of the tile
             mbar_init(bar0 + 8 * i, count);
         }
         *abort_flag = 0;
@@ -284,9 +315,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_commit(bar0 + 8 * kBarMmaDone);
             drain_wait(bar0 + 8 * kBarMmaDone, 0, p.wc);
         }
-    } else if (warp >= 4) {
+    } else {
         // ------------------------------------------------------------ softmax + epilogue
-        const int t = (warp - 4) >> 2;           // query tile of this warpgroup
+        // 16 warps: tile t = sw / 8; half h = (sw / 4) % 2 takes key columns [64h, 64h + 64)
+        // of every S row and the head dims [h D/2, (h+1) D/2) of O.
+        const int sw = warp - 2;
+        const int t = sw >> 3;
+        const int h = (sw >> 2) & 1;
         const int wq = warp & 3;                 // TMEM lane quarter
         const int row = wq * 32 + lane;
         const int qi = q0 + t * BM + row;
@@ -298,9 +333,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t tO = tmem + lane_off + C::kColO + 128 * t;
         const float sl = p.scale_log2;
         float m_run = -INFINITY;
-        float l_run = 0.f;
+        float l_run = 0.f;  // this half's share of the row sum
         bool ok = true;
         const int jb = rng[t].jb, je = rng[t].je;
+        float* xch = reinterpret_cast<float*>(smem + C::kOffX) + (t * 2) * BM;  // [2 halves][128 rows]
+        uint32_t x_it = 0;  // phases of the tile's exchange barrier
 
         for (int j = jb; j < je; ++j) {
             const int i = j - jb;
@@ -311,38 +348,43 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             }
             tc_fence_after();
-            const long long tb = kv0 + (long long)j * BN;
-            const int c_lo = (int)max(0LL, min((long long)BN, rlo - tb));
-            const int c_hi = (int)max(0LL, min((long long)BN, rhi - tb));
-            const bool full = (c_lo == 0 && c_hi == BN);
-            const bool any = c_lo < c_hi;
+            const long long tb = kv0 + (long long)j * BN + 64 * h;  // first key of my 64 columns
+            const int c_lo = (int)max(0LL, min(64LL, rlo - tb));
+            const int c_hi = (int)max(0LL, min(64LL, rhi - tb));
+            const bool full = (c_lo == 0 && c_hi == 64);
 
-            // Pass 1: the extreme of the raw scores over the visible columns (the max when
-            // the scale is non-negative, the min otherwise), in 8 independent chains.
-            float ext;
-            {
-                float s[BN];
-                tmem_ld128(tS, s);
-                const float fill = (sl >= 0.f) ? -INFINITY : INFINITY;
+            // My 64 scores stay in registers for both passes: the other half writes P into
+            // columns 32..63 after the exchange below, so nothing is read back from TMEM.
+            float s[64];
+            tmem_ld64(tS + 64 * h, s);
+            float hext;
+            if (sl >= 0.f) {
                 if (!full) {
 #pragma unroll
-                    for (int c = 0; c < BN; ++c) s[c] = (c >= c_lo && c < c_hi) ? s[c] : fill;
+                    for (int c = 0; c < 64; ++c) s[c] = (c >= c_lo && c < c_hi) ? s[c] : -INFINITY;
                 }
-                if (sl < 0.f) {
+                hext = row_max64(s);
+            } else {
+                if (!full) {
 #pragma unroll
-                    for (int c = 0; c < BN; ++c) s[c] = -s[c];
+                    for (int c = 0; c < 64; ++c) s[c] = (c >= c_lo && c < c_hi) ? s[c] : INFINITY;
                 }
-                float e8[8];
-#pragma unroll
-                for (int q = 0; q < 8; ++q) e8[q] = s[q];
-#pragma unroll
-                for (int c = 8; c < BN; c += 16) {
-#pragma unroll
-                    for (int q = 0; q < 8; ++q) e8[q] = fmax3(e8[q], s[c + q], (c + 8 + q < BN) ? s[c + 8 + q] : -INFINITY);
-                }
-                ext = fmax3(fmax3(e8[0], e8[1], e8[2]), fmax3(e8[3], e8[4], e8[5]), fmaxf(e8[6], e8[7]));
-                if (sl < 0.f) ext = -ext;
+                hext = row_min64(s);
             }
+            // exchange the half extremes of each row between the two halves of the tile
+            // (a bounded barrier wait: a partner that gave up cannot hang this warp)
+            xch[h * BM + row] = hext;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar0 + 8 * (kBarXch + t));
+            if (!__all_sync(0xffffffffu, mbar_wait(bar0 + 8 * (kBarXch + t), x_it & 1, p.wc, abort_flag))) {
+                ok = false;
+                break;
+            }
+            ++x_it;
+            const float oext = xch[(1 - h) * BM + row];
+            const float ext = (sl >= 0.f) ? fmaxf(hext, oext) : fminf(hext, oext);
+            const bool any = (sl >= 0.f) ? (ext != -INFINITY) : (ext != INFINITY);
+
             float alpha = 1.f;
             bool rescale = false;
             if (any) {
@@ -358,58 +400,41 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float neg_m = (m_run == -INFINITY) ? 0.f : -m_run;
             const float2 sl2 = make_float2(sl, sl), negm2 = make_float2(neg_m, neg_m);
 
-            // Pass 2: S again, 32 columns at a time with the next chunk's load in flight;
-            // P chunk k (columns 16k..16k+15) only overwrites S columns already read.
-            // The row sum adds the bf16-rounded probabilities, the same numbers the
-            // tensor core multiplies into V, so numerator and denominator agree.
-            float2 sum2[4];
+            // P for my 64 keys -> TMEM columns [32h, 32h + 32) of S_t, as bf16 pairs; the row
+            // sum adds the rounded values the tensor core will multiply into V.
+            float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
 #pragma unroll
-            for (int q = 0; q < 4; ++q) sum2[q] = make_float2(0.f, 0.f);
-            uint32_t buf[2][32];
-            tmem_ld32_async(tS, buf[0]);
-#pragma unroll
-            for (int k = 0; k < BN / 32; ++k) {
-                uint32_t* sc = buf[k & 1];
-                tmem_ld_wait32(sc);
-                if (k + 1 < BN / 32) tmem_ld32_async(tS + 32 * (k + 1), buf[(k + 1) & 1]);
+            for (int k = 0; k < 2; ++k) {
                 uint32_t pk[16];
 #pragma unroll
                 for (int c2 = 0; c2 < 32; c2 += 2) {
                     const int c = 32 * k + c2;
-                    const float2 x2 = __ffma2_rn(make_float2(__uint_as_float(sc[c2]), __uint_as_float(sc[c2 + 1])),
-                                                 sl2, negm2);
-                    float p0, p1;
-                    if ((c2 / 2) % kPolyPeriod >= kPolyPeriod - kPolyPairs) {
-                        const float2 e2 = ex2_poly2(x2);  // on the FMA pipes
-                        p0 = e2.x;
-                        p1 = e2.y;
-                    } else {
-                        p0 = ex2_approx(x2.x);  // on the special-function unit
-                        p1 = ex2_approx(x2.y);
-                    }
-                    if (!full) {
+                    const float2 x2 = __ffma2_rn(make_float2(s[c], s[c + 1]), sl2, negm2);
+                    float p0 = ex2_approx(x2.x);  // special-function unit; 2^-inf = 0
+                    float p1 = ex2_approx(x2.y);
+                    if (!full) {  // masked columns get exactly 0 (also when scale is 0 or negative)
                         p0 = (c >= c_lo && c < c_hi) ? p0 : 0.f;
                         p1 = (c + 1 >= c_lo && c + 1 < c_hi) ? p1 : 0.f;
                     }
-                    const uint32_t w = pack_bf16x2(p0, p1);
-                    pk[c2 / 2] = w;
-                    sum2[(c2 / 2) & 3] = __fadd2_rn(sum2[(c2 / 2) & 3],
-                                                    make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u)));
+                    const uint32_t wv = pack_bf16x2(p0, p1);
+                    pk[c2 / 2] = wv;
+                    const float2 r2 = make_float2(__uint_as_float(wv << 16), __uint_as_float(wv & 0xffff0000u));
+                    if ((c2 / 2) & 1) acc1 = __fadd2_rn(acc1, r2); else acc0 = __fadd2_rn(acc0, r2);
                 }
-                tmem_st16_async(tS + 16 * k, pk);
+                tmem_st16_async(tS + 32 * h + 16 * k, pk);
             }
             tmem_st_wait();
-            sum2[0] = __fadd2_rn(__fadd2_rn(sum2[0], sum2[1]), __fadd2_rn(sum2[2], sum2[3]));
-            l_run = l_run * alpha + (sum2[0].x + sum2[0].y);
+            acc0 = __fadd2_rn(acc0, acc1);
+            l_run = l_run * alpha + (acc0.x + acc0.y);
             // O_t is stable here: the commit behind S_t(j) covers the earlier P V product.
             if (__any_sync(0xffffffffu, rescale)) {
 #pragma unroll
-                for (int c = 0; c < D / 32; ++c) {
+                for (int c = 0; c < D / 64; ++c) {
                     float o[32];
-                    tmem_ld32(tO + 32 * c, o);
+                    tmem_ld32(tO + (D / 2) * h + 32 * c, o);
 #pragma unroll
                     for (int q = 0; q < 32; ++q) o[q] *= alpha;
-                    tmem_st32(tO + 32 * c, o);
+                    tmem_st32(tO + (D / 2) * h + 32 * c, o);
                 }
             }
             tc_fence_before();
@@ -418,19 +443,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
 
         // ------------------------------------------------------------ epilogue
+        // row sum = both halves' shares; each half stores its D/2 head dims of the row
+        float* lch = reinterpret_cast<float*>(smem + C::kOffL) + (t * 2) * BM;
+        float l_tot = l_run;
+        if (ok) {
+            lch[h * BM + row] = l_run;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar0 + 8 * (kBarXch + t));
+            ok = __all_sync(0xffffffffu, mbar_wait(bar0 + 8 * (kBarXch + t), x_it & 1, p.wc, abort_flag));
+            if (ok) l_tot += lch[(1 - h) * BM + row];
+        }
         const bool has = je > jb;
         if (ok && has) {
             ok = __all_sync(0xffffffffu, mbar_wait(bar0 + 8 * (kBarOFull + t), 0, p.wc, abort_flag));
             tc_fence_after();
         }
         if (ok && q0 + t * BM < p.Lq) {
-            const float inv = (l_run > 0.f) ? 1.f / l_run : 0.f;
-            __nv_bfloat16* orow = p.out + ((size_t)(b * p.Hq + hq) * p.Lq + qi) * D;
+            const float inv = (l_tot > 0.f) ? 1.f / l_tot : 0.f;
+            __nv_bfloat16* orow = p.out + ((size_t)(b * p.Hq + hq) * p.Lq + qi) * D + (D / 2) * h;
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
+            for (int c = 0; c < D / 64; ++c) {
                 float o[32];
                 if (has) {
-                    tmem_ld32(tO + 32 * c, o);
+                    tmem_ld32(tO + (D / 2) * h + 32 * c, o);
                 } else {
 #pragma unroll
                     for (int q = 0; q < 32; ++q) o[q] = 0.f;
