@@ -17,7 +17,7 @@ MASK_NONE, MASK_CAUSAL, MASK_WINDOW, MASK_CAUSAL_WINDOW = 0, 1, 2, 3
 ATTN_BF16, ATTN_F32 = 0, 1
 
 EXPORTED = ("attn_fwd", "attn_decode_caches", "attn_last_error", "attn_sync_status", "attn_selftest_timeout",
-            "attn_selftest_exp2", "attn_version")
+            "attn_version")
 
 _STATUS_NAMES = {0: "ATTN_OK", 1: "ATTN_ERR_INVALID_ARG", 2: "ATTN_ERR_UNSUPPORTED", 3: "ATTN_ERR_CUDA",
                  4: "ATTN_ERR_TIMEOUT"}
@@ -60,8 +60,6 @@ def load(path: str | None = None):
         lib.attn_sync_status.argtypes = [vp]
         lib.attn_selftest_timeout.restype = ci
         lib.attn_selftest_timeout.argtypes = [ci, vp]
-        lib.attn_selftest_exp2.restype = ci
-        lib.attn_selftest_exp2.argtypes = [vp, vp, vp, ci, vp]
         lib.attn_version.restype = ci
         lib.attn_version.argtypes = []
         if path is None:
@@ -201,17 +199,6 @@ def check_device_status(stream=None):
 def selftest_timeout(limit_us: int, stream=None) -> int:
     """Enqueue the bounded-wait self test (see attn_selftest_timeout); returns the launch status."""
     return load().attn_selftest_timeout(int(limit_us), _stream_handle(stream))
-
-
-def selftest_exp2(x):
-    """(poly, unit) = the two 2^x routines of the kernels applied to a float32 CUDA tensor."""
-    import torch
-    if not x.is_cuda or x.dtype != torch.float32 or not x.is_contiguous():
-        raise ValueError("x must be a contiguous float32 CUDA tensor")
-    yp, yu = torch.empty_like(x), torch.empty_like(x)
-    _check(load().attn_selftest_exp2(x.data_ptr(), yp.data_ptr(), yu.data_ptr(), x.numel(),
-                                     _stream_handle(None)))
-    return yp, yu
 
 
 def version() -> int:

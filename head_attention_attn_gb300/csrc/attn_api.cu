@@ -217,16 +217,6 @@ attn_status attn_selftest_timeout(int limit_us, void* cuda_stream) {
     return ATTN_OK;
 }
 
-attn_status attn_selftest_exp2(const float* x, float* y_poly, float* y_unit, int n, void* cuda_stream) {
-    t_last_error.clear();
-    if (n < 0) return fail(ATTN_ERR_INVALID_ARG, "negative n");
-    if (n == 0) return ATTN_OK;
-    if (!x || !y_poly || !y_unit) return fail(ATTN_ERR_INVALID_ARG, "null pointer");
-    cudaError_t e = attn::launch_exp2_selftest(x, y_poly, y_unit, n, static_cast<cudaStream_t>(cuda_stream));
-    if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "exp2 selftest launch: %s", cudaGetErrorString(e));
-    return ATTN_OK;
-}
-
 int attn_version(void) { return 100; }
 
 }  // extern "C"

@@ -274,29 +274,6 @@ __device__ __forceinline__ float ex2_approx(float x) {
     return y;
 }
 
-// 2^x for a pair of floats on the FMA pipes (the special-function unit stays free).
-// Method: Cody-Waite style range reduction x = n + f with n = round(x) and
-// |f| <= 1/2 (adding 1.5*2^23 leaves round(x) in the low mantissa bits), a
-// degree-3 polynomial for 2^f whose coefficients come from a Remez exchange
-// minimising the relative error on [-1/2, 1/2] (max relative error 7.5e-5),
-// and n added to the exponent field of the result.  x is clamped to >= -125 so
-// the exponent stays normal; callers zero masked entries themselves.
-__device__ __forceinline__ float2 ex2_poly2(float2 x) {
-    constexpr float kShift = 12582912.0f;  // 1.5 * 2^23
-    constexpr float c0 = 0.9999280571937561f, c1 = 0.6932609677314758f;
-    constexpr float c2 = 0.2426111251115799f, c3 = 0.0551716685295105f;
-    x.x = fmaxf(x.x, -125.0f);
-    x.y = fmaxf(x.y, -125.0f);
-    const float2 t = __fadd2_rn(x, make_float2(kShift, kShift));
-    const float2 n = __fadd2_rn(t, make_float2(-kShift, -kShift));
-    const float2 f = __ffma2_rn(n, make_float2(-1.0f, -1.0f), x);
-    float2 p = __ffma2_rn(f, make_float2(c3, c3), make_float2(c2, c2));
-    p = __ffma2_rn(p, f, make_float2(c1, c1));
-    p = __ffma2_rn(p, f, make_float2(c0, c0));
-    return make_float2(__uint_as_float(__float_as_uint(p.x) + (__float_as_uint(t.x) << 23)),
-                       __uint_as_float(__float_as_uint(p.y) + (__float_as_uint(t.y) << 23)));
-}
-
 // Maximum of three floats (PTX three-input max).
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
     float r;

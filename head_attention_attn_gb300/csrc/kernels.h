@@ -78,7 +78,4 @@ cudaError_t launch_simt_f32(const Problem& p, const WaitCtl& wc, cudaStream_t st
 // Bounded-wait self test: one block waits on an mbarrier nobody signals.
 cudaError_t launch_timeout_selftest(const WaitCtl& wc, cudaStream_t stream);
 
-// 2^x self test: the FMA-pipe polynomial and the special-function unit, element-wise.
-cudaError_t launch_exp2_selftest(const float* x, float* y_poly, float* y_unit, int n, cudaStream_t stream);
-
 }  // namespace attn

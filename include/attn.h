@@ -205,21 +205,6 @@ ATTN_API attn_status attn_sync_status(void* cuda_stream);
 ATTN_API attn_status attn_selftest_timeout(int limit_us, void* cuda_stream);
 
 /*
- * attn_selftest_exp2 -- evaluate the two 2^x routines of the softmax, element-wise.
- *
- * x, y_poly, y_unit: caller-owned device arrays of n floats.
- *   y_poly[i]  2^x[i] by the FMA-pipe routine: range reduction to round(x) plus a
- *              fraction in [-1/2, 1/2], a degree-3 minimax polynomial (relative
- *              error below 1e-4 for x in [-125, 64]), exponent added in the
- *              integer field.  Inputs below -125 give 2^-125.
- *   y_unit[i]  2^x[i] by the special-function unit (PTX ex2.approx).
- * A test hook for the kernels' exponent; the pages have no counterpart.
- * Returns ATTN_ERR_INVALID_ARG for n < 0 or null pointers, ATTN_ERR_CUDA on a
- * launch failure, ATTN_OK once enqueued on cuda_stream.
- */
-ATTN_API attn_status attn_selftest_exp2(const float* x, float* y_poly, float* y_unit, int n, void* cuda_stream);
-
-/*
  * attn_version -- library version as major*10000 + minor*100 + patch.
  */
 ATTN_API int attn_version(void);
