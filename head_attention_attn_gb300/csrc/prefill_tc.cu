@@ -1,21 +1,22 @@
 // prefill_tc.cu -- K1: fused attention prefill on the 5th-generation tensor cores (sm_103a).
 //
-// One CTA computes two 128-row query tiles (256 consecutive rows) of one
-// (batch, query head), sharing every K and V tile between them:
-//   warp 0       TMA producer: both Q tiles once, then 128-key K and V tiles
+// One CTA computes NT 128-row query tiles (NT = 2 for head_dim 128, NT = 1 for
+// head_dim 64) of one (batch, query head), sharing every K and V tile between them:
+//   warp 0       TMA producer: the Q tiles once, then 128-key K and V tiles
 //                through 2-stage shared-memory rings (128-byte swizzle).
-//   warp 1       TMEM owner (all 512 columns) and single-thread MMA issuer.
-//   warps 2-17   softmax, 8 warps per query tile: a row of S is split between two
+//   warp 1       TMEM owner and single-thread MMA issuer.
+//   warps 2..    softmax, 8 warps per query tile: a row of S is split between two
 //                threads, one per half of the 128 key columns.  Each thread reads its 64
 //                scores from TMEM, the two halves exchange their row maxima through
 //                shared memory, and each writes its 64 probabilities (2^x on the
 //                special-function unit, scale*log2(e) folded in) back into TMEM as
 //                packed bf16.  After the tile's last key block each half normalises
 //                and stores its half of the head dims of the row.
-// TMEM: S0 | S1 | O0 | O1, 128 columns each; P_t aliases the first 64 columns of S_t.
-// The MMA order is the ping-pong
+// TMEM: S_0 .. S_{NT-1} | O_0 .. O_{NT-1}, 128 columns each; P_t aliases the first 64
+// columns of S_t.  With two tiles the MMA order is the ping-pong
 //   PV0(j-1), QK0(j), PV1(j-1), QK1(j)
-// so the tensor core works on one tile while the other tile's softmax runs:
+// so the tensor core works on one tile while the other tile's softmax runs; with one
+// tile per CTA the two CTAs resident on an SM take turns in the same way.
 //   QK_t(j):  S_t  = Q_t K_j^T   (A, B from shared memory, K-major)
 //   PV_t(j):  O_t += P_t V_j     (A = P from TMEM, B = V from shared memory, MN-major)
 // A commit after QK_t(j) completes only after every earlier MMA, PV_t(j-1)
@@ -35,14 +36,16 @@ namespace {
 
 constexpr int BM = 128;           // query rows per tile
 constexpr int BN = 128;           // keys per tile
-constexpr int kTiles = 2;         // query tiles per CTA
-constexpr int kThreads = 576;     // 18 warps: producer, MMA, 16 softmax warps
+// NT query tiles per CTA (1 or 2); 2 + 8 NT warps: producer, MMA, 8 softmax warps per tile
+template <int NT>
+constexpr int threads_for() { return 64 + 256 * NT; }
 constexpr int kStages = 2;        // K/V ring depth
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f;
 
-template <int D>
+template <int D, int NT>
 struct Cfg {
+    static constexpr int kTiles = NT;
     static constexpr int kChunks = D / 64;
     static constexpr int kQBytes = BM * D * 2;   // one query tile
     static constexpr int kKVBytes = BN * D * 2;  // one K or V tile
@@ -53,11 +56,12 @@ struct Cfg {
     static constexpr int kOffL = kOffX + kTiles * 2 * BM * 4;         // row-sum exchange
     static constexpr int kOffBar = kOffL + kTiles * 2 * BM * 4;
     static constexpr int kSmem = kOffBar + 256 + 1024;
-    static constexpr uint32_t kTmemCols = 512;
+    static constexpr uint32_t kTmemCols = NT == 2 ? 512 : 256;
     static constexpr uint32_t kColS = 0;    // + 128 * tile
-    static constexpr uint32_t kColO = 256;  // + 128 * tile
+    static constexpr uint32_t kColO = 128 * NT;  // + 128 * tile
 };
 
+constexpr int kTiles = 2;  // barrier slots are laid out for the larger configuration
 enum : int {
     kBarQFull = 0,
     kBarKFull = 1,
@@ -137,11 +141,12 @@ struct TileRange {
     int jb, je;
 };
 
-template <int D>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int D, int NT>
+__global__ void __launch_bounds__(threads_for<NT>(), 3 - NT)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV, const PrefillParams p) {
-    using C = Cfg<D>;
+    using C = Cfg<D, NT>;
+    constexpr int kTiles = NT;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_s = smem_u32(smem_raw);
     uint8_t* smem = smem_raw + ((1024u - (raw_s & 1023u)) & 1023u);
@@ -259,7 +264,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             constexpr uint32_t kIdescQK = idesc_bf16_f32(BM, BN, 0, 0);
             constexpr uint32_t kIdescPV = idesc_bf16_f32(BM, D, 0, 1);
             bool ok = mbar_wait(bar0 + 8 * kBarQFull, 0, p.wc, abort_flag);
-            int it[kTiles] = {0, 0};  // local iteration (P phases consumed) per tile
+            int it[kTiles] = {};  // local iteration (P phases consumed) per tile
             for (int j = 0; ok && j <= ntiles; ++j) {
                 // PV_t(j-1) then QK_t(j), tile by tile
                 bool v_waited = false, k_waited = false;
@@ -528,9 +533,10 @@ bool encode_bf16_3d(CUtensorMap* map, const void* base, int D, int L, int outer)
     return r == CUDA_SUCCESS;
 }
 
-template <int D>
+template <int D, int NT>
 cudaError_t launch_impl(const Problem& pr, const WaitCtl& wc, cudaStream_t stream) {
-    using C = Cfg<D>;
+    using C = Cfg<D, NT>;
+    constexpr int kTiles = NT;
     CUtensorMap tq, tk, tv;
     if (!encode_bf16_3d(&tq, pr.q, D, pr.Lq, pr.B * pr.Hq) || !encode_bf16_3d(&tk, pr.k, D, pr.Lk, pr.B * pr.Hkv) ||
         !encode_bf16_3d(&tv, pr.v, D, pr.Lk, pr.B * pr.Hkv))
@@ -543,7 +549,7 @@ cudaError_t launch_impl(const Problem& pr, const WaitCtl& wc, cudaStream_t strea
     {
         std::lock_guard<std::mutex> g(mu);
         if (dev < 64 && !configured[dev]) {
-            e = cudaFuncSetAttribute(prefill_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+            e = cudaFuncSetAttribute(prefill_tc_kernel<D, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
             if (e != cudaSuccess) return e;
             configured[dev] = true;
         }
@@ -564,15 +570,18 @@ cudaError_t launch_impl(const Problem& pr, const WaitCtl& wc, cudaStream_t strea
     p.wc = wc;
     const long long grid = (long long)p.num_m * pr.B * pr.Hq;
     if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    prefill_tc_kernel<D><<<(unsigned)grid, kThreads, C::kSmem, stream>>>(tq, tk, tv, p);
+    prefill_tc_kernel<D, NT><<<(unsigned)grid, threads_for<NT>(), C::kSmem, stream>>>(tq, tk, tv, p);
     return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_prefill_tc(const Problem& p, const WaitCtl& wc, cudaStream_t stream) {
-    if (p.D == 64) return launch_impl<64>(p, wc, stream);
-    if (p.D == 128) return launch_impl<128>(p, wc, stream);
+    // head_dim 64: one query tile per CTA, so two CTAs share an SM (256 TMEM columns and
+    // about 83 KB of shared memory each) and hide each other's set-up and epilogue.
+    // head_dim 128: two tiles per CTA (512 TMEM columns, one CTA per SM), ping-pong inside.
+    if (p.D == 64) return launch_impl<64, 1>(p, wc, stream);
+    if (p.D == 128) return launch_impl<128, 2>(p, wc, stream);
     return cudaErrorInvalidValue;
 }
 
