@@ -140,7 +140,10 @@ def read_peaks():
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled every 200 ms while running."""
+    """nvidia-smi clocks and throttle reasons sampled every 20 ms while running.
+
+    Entering waits (up to 5 s) for the first sample, so the samples cover the timed
+    region that follows rather than nvidia-smi's own start-up."""
 
     QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -158,9 +161,18 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+                 "-lms", "20"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
+        if self.proc is not None:
+            t0 = time.time()
+            while time.time() - t0 < 5.0 and self.proc.poll() is None:
+                try:
+                    if os.path.getsize(self.path) > 0:
+                        break
+                except OSError:
+                    pass
+                time.sleep(0.01)
         return self
 
     def __exit__(self, *exc):
@@ -260,7 +272,7 @@ def run_ours(args, rank, world, local):
     value = tflops * world  # replicas: every rank processes one full workload per step
     roof = {"bound": "tensor", "achieved": round(tflops, 2), "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
             "frac": round(tflops / peaks["bf16_tflops"], 4), "peak_source": f"{peak_src} bf16 dense (burst)",
-            "traffic": NCU_TRAFFIC.get(kernel_source_hash()), "kernel": "prefill_tc_kernel<128>",
+            "traffic": NCU_TRAFFIC.get(kernel_source_hash()), "kernel": "prefill_tc_kernel<128, 2 tiles, bf16>",
             "algorithmic_flops_per_launch": flops}
 
     # ---- end to end through the public call with pinned host buffers: every step copies its
@@ -338,7 +350,7 @@ def run_ours(args, rank, world, local):
               "ms_per_step": round(dsec * 1e3, 4),
               "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                            "frac": round(gbs / peaks["hbm_gbs"], 4), "peak_source": f"{peak_src} HBM copy",
-                           "traffic": None, "kernel": "decode_splitkv_kernel<128,4>",
+                           "traffic": None, "kernel": "decode_splitkv_kernel<128, G4, bf16>",
                            "algorithmic_bytes_per_launch": dec_bytes},
               "l2": f"inputs {dec_bytes / 1e6:.0f} MB > {L2_BYTES / 1e6:.0f} MB L2, no flush"}
     del host_d, devt_d

@@ -14,7 +14,7 @@ from .build import LIB_PATH
 
 ATTN_OK, ATTN_ERR_INVALID_ARG, ATTN_ERR_UNSUPPORTED, ATTN_ERR_CUDA, ATTN_ERR_TIMEOUT = range(5)
 MASK_NONE, MASK_CAUSAL, MASK_WINDOW, MASK_CAUSAL_WINDOW = 0, 1, 2, 3
-ATTN_BF16, ATTN_F32 = 0, 1
+ATTN_BF16, ATTN_F32, ATTN_F16 = 0, 1, 2
 
 EXPORTED = ("attn_fwd", "attn_decode_caches", "attn_last_error", "attn_sync_status", "attn_selftest_timeout",
             "attn_version")
@@ -97,7 +97,7 @@ def attn_fwd(q, k, v, out=None, *, pos_offset: int = 0, mask_mode: int = MASK_NO
              key_lens=None, scale: float | None = None, stream=None):
     """Attention forward on CUDA tensors (head-major, contiguous).
 
-    q [B, Hq, Lq, D], k and v [B, Hkv, Lk, D] (bf16 or fp32, same dtype),
+    q [B, Hq, Lq, D], k and v [B, Hkv, Lk, D] (bf16, fp16 or fp32, same dtype),
     key_lens: int32 CUDA tensor [B] or None; out: preallocated [B, Hq, Lq, D] or None.
     scale None means 1/sqrt(D) rounded to fp32.  Enqueues on `stream`
     (default: torch's current stream) and returns out without synchronising.
@@ -114,6 +114,8 @@ def attn_fwd(q, k, v, out=None, *, pos_offset: int = 0, mask_mode: int = MASK_NO
         raise ValueError("q, k, v must share a dtype")
     if q.dtype == torch.bfloat16:
         dtype = ATTN_BF16
+    elif q.dtype == torch.float16:
+        dtype = ATTN_F16
     elif q.dtype == torch.float32:
         dtype = ATTN_F32
     else:
@@ -141,37 +143,49 @@ def attn_fwd(q, k, v, out=None, *, pos_offset: int = 0, mask_mode: int = MASK_NO
 
 
 def attn_decode_caches(q, k_caches, v_caches, kv_lens, out=None, *, sliding_window: int = 0,
-                       scale: float | None = None, stream=None):
+                       scale: float | None = None, stream=None, kv_heads: int | None = None,
+                       capacity: int | None = None):
     """One decode step for m items against per-item caches (see attn_decode_caches in attn.h).
 
-    q: [m, Hq, D] bf16 CUDA tensor; k_caches, v_caches: sequences of m [Hkv, capacity, D]
-    bf16 CUDA tensors (or int64 CUDA tensors of m device addresses); kv_lens: int32 CUDA [m].
+    q: [m, Hq, D] bf16 or fp16 CUDA tensor; k_caches, v_caches: sequences of m
+    [Hkv, capacity, D] CUDA tensors of q's dtype, or int64 CUDA tensors of m device
+    addresses (then kv_heads and capacity must be given); kv_lens: int32 CUDA [m].
     The pointer arrays are built here (device tensors kept alive until the call is enqueued
     and the stream reaches it; this function synchronises nothing).
     """
     import torch
-    if not q.is_cuda or q.dtype != torch.bfloat16 or q.dim() != 3 or not q.is_contiguous():
-        raise ValueError("q must be a contiguous bf16 CUDA tensor [m, Hq, D]")
+    if q.dtype == torch.bfloat16:
+        dtype = ATTN_BF16
+    elif q.dtype == torch.float16:
+        dtype = ATTN_F16
+    else:
+        raise ValueError("q must be bf16 or fp16")
+    if not q.is_cuda or q.dim() != 3 or not q.is_contiguous():
+        raise ValueError("q must be a contiguous CUDA tensor [m, Hq, D]")
     m, Hq, D = q.shape
 
     def ptrs(caches):
         if isinstance(caches, torch.Tensor) and caches.dtype == torch.int64:
-            return caches, None
+            if not caches.is_cuda or caches.numel() != m:
+                raise ValueError("an address array must be an int64 CUDA tensor with m entries")
+            if kv_heads is None or capacity is None:
+                raise ValueError("kv_heads and capacity are required with address arrays")
+            return caches.contiguous(), (int(kv_heads), int(capacity), D)
         caches = list(caches)
         if len(caches) != m:
             raise ValueError("one cache per item is required")
-        shape = caches[0].shape
+        shape = tuple(caches[0].shape)
         for t in caches:
-            if not t.is_cuda or t.dtype != torch.bfloat16 or not t.is_contiguous() or t.shape != shape:
-                raise ValueError("caches must be contiguous bf16 CUDA tensors of one shape [Hkv, capacity, D]")
+            if not t.is_cuda or t.dtype != q.dtype or not t.is_contiguous() or tuple(t.shape) != shape:
+                raise ValueError("caches must be contiguous CUDA tensors of q's dtype and one shape [Hkv, capacity, D]")
         arr = torch.tensor([t.data_ptr() for t in caches], dtype=torch.int64, device=q.device)
         return arr, shape
 
     kp, kshape = ptrs(k_caches)
     vp_, vshape = ptrs(v_caches)
-    if kshape is None or vshape is None or kshape != vshape or kshape[2] != D:
+    if len(kshape) != 3 or kshape != vshape or kshape[2] != D:
         raise ValueError("k and v caches must share a shape [Hkv, capacity, D] matching q")
-    Hkv, capacity = int(kshape[0]), int(kshape[1])
+    Hkv, cap = int(kshape[0]), int(kshape[1])
     if kv_lens.dtype != torch.int32 or not kv_lens.is_cuda or kv_lens.numel() != m:
         raise ValueError("kv_lens must be an int32 CUDA tensor with m entries")
     if out is None:
@@ -179,8 +193,8 @@ def attn_decode_caches(q, k_caches, v_caches, kv_lens, out=None, *, sliding_wind
     if scale is None:
         scale = float(torch.tensor(1.0 / math.sqrt(D), dtype=torch.float32).item())
     status = load().attn_decode_caches(q.data_ptr(), kp.data_ptr(), vp_.data_ptr(), out.data_ptr(), m, Hq, Hkv,
-                                       capacity, D, kv_lens.data_ptr(), int(sliding_window), ctypes.c_float(scale),
-                                       ATTN_BF16, _stream_handle(stream))
+                                       cap, D, kv_lens.data_ptr(), int(sliding_window), ctypes.c_float(scale),
+                                       dtype, _stream_handle(stream))
     _check(status)
     out._attn_keepalive = (kp, vp_)  # the pointer arrays must outlive the queued launch
     return out

@@ -3,8 +3,8 @@
 //
 // Kernel choice:
 //   f32                          -> K3 (SIMT fp32, any head_dim 1..256)
-//   bf16, q_len == 1, group 1/2/4/8 -> K2 (split-KV decode)
-//   bf16 otherwise               -> K1 (tcgen05 + TMA fused prefill)
+//   bf16/fp16, q_len == 1, group 1/2/4/8 -> K2 (split-KV decode)
+//   bf16/fp16 otherwise          -> K1 (tcgen05 + TMA fused prefill)
 // There is no host fallback: an unsupported shape is refused (ferrum-kernels:
 // CUDA ops fail rather than copy data through host memory).
 #include <math.h>
@@ -86,12 +86,13 @@ attn_status attn_fwd(const void* q, const void* k, const void* v, void* out, int
         return fail(ATTN_ERR_INVALID_ARG, "q_heads (%d) is not a multiple of kv_heads (%d)", q_heads, kv_heads);
     if (mask_mode < ATTN_MASK_NONE || mask_mode > ATTN_MASK_CAUSAL_WINDOW)
         return fail(ATTN_ERR_INVALID_ARG, "mask_mode %d out of range", mask_mode);
-    if (dtype != ATTN_BF16 && dtype != ATTN_F32) return fail(ATTN_ERR_INVALID_ARG, "dtype %d out of range", dtype);
+    if (dtype != ATTN_BF16 && dtype != ATTN_F32 && dtype != ATTN_F16)
+        return fail(ATTN_ERR_INVALID_ARG, "dtype %d out of range", dtype);
     if (window < 0) return fail(ATTN_ERR_INVALID_ARG, "negative window %d", window);
     if (pos_offset < 0) return fail(ATTN_ERR_INVALID_ARG, "negative pos_offset %d", pos_offset);
     if (!isfinite(scale)) return fail(ATTN_ERR_INVALID_ARG, "scale is not finite");
-    if (dtype == ATTN_BF16 && head_dim != 64 && head_dim != 128)
-        return fail(ATTN_ERR_UNSUPPORTED, "bf16 supports head_dim 64 and 128, not %d", head_dim);
+    if (dtype != ATTN_F32 && head_dim != 64 && head_dim != 128)
+        return fail(ATTN_ERR_UNSUPPORTED, "bf16 and fp16 support head_dim 64 and 128, not %d", head_dim);
     if (dtype == ATTN_F32 && head_dim > 256)
         return fail(ATTN_ERR_UNSUPPORTED, "f32 supports head_dim up to 256, not %d", head_dim);
     if ((long long)batch * q_heads > 0x7fffffffLL || (long long)batch * kv_heads > 0x7fffffffLL)
@@ -99,7 +100,7 @@ attn_status attn_fwd(const void* q, const void* k, const void* v, void* out, int
     if (batch == 0 || q_len == 0) return ATTN_OK;  // nothing to compute
 
     if (!q || !out) return fail(ATTN_ERR_INVALID_ARG, "null q or out pointer");
-    const size_t esize = (dtype == ATTN_BF16) ? 2 : 4;
+    const size_t esize = (dtype == ATTN_F32) ? 4 : 2;
     cudaStream_t stream = static_cast<cudaStream_t>(cuda_stream);
     if (kv_len == 0) {
         // Every row sees no key: the defined result is all zeros.
@@ -109,7 +110,7 @@ attn_status attn_fwd(const void* q, const void* k, const void* v, void* out, int
         return ATTN_OK;
     }
     if (!k || !v) return fail(ATTN_ERR_INVALID_ARG, "null k or v pointer");
-    const uintptr_t align = (dtype == ATTN_BF16) ? 16 : 4;
+    const uintptr_t align = (dtype == ATTN_F32) ? 4 : 16;
     if (!aligned(q, align) || !aligned(k, align) || !aligned(v, align) || !aligned(out, align))
         return fail(ATTN_ERR_INVALID_ARG, "q, k, v and out must be %u-byte aligned", (unsigned)align);
     if (key_lens && !aligned(key_lens, 4)) return fail(ATTN_ERR_INVALID_ARG, "key_lens must be 4-byte aligned");
@@ -119,7 +120,7 @@ attn_status attn_fwd(const void* q, const void* k, const void* v, void* out, int
     if (s != ATTN_OK) return s;
     attn::WaitCtl wc{st->status, kWaitLimitNs};
     attn::Problem p{q, k, v, out, batch, q_heads, kv_heads, q_len, kv_len, head_dim,
-                    pos_offset, mask_mode, window, key_lens, scale};
+                    pos_offset, mask_mode, window, key_lens, scale, dtype == ATTN_F16};
 
     cudaError_t e;
     const char* which;
@@ -151,9 +152,10 @@ attn_status attn_decode_caches(const void* q, const void* const* k_caches, const
         return fail(ATTN_ERR_INVALID_ARG, "q_heads (%d) is not a multiple of kv_heads (%d)", q_heads, kv_heads);
     if (sliding_window < 0) return fail(ATTN_ERR_INVALID_ARG, "negative sliding_window %d", sliding_window);
     if (!isfinite(scale)) return fail(ATTN_ERR_INVALID_ARG, "scale is not finite");
-    if (dtype != ATTN_BF16) return fail(ATTN_ERR_UNSUPPORTED, "per-item caches support bf16 only");
+    if (dtype != ATTN_BF16 && dtype != ATTN_F16)
+        return fail(ATTN_ERR_UNSUPPORTED, "per-item caches support bf16 and fp16 only");
     if (head_dim != 64 && head_dim != 128)
-        return fail(ATTN_ERR_UNSUPPORTED, "bf16 supports head_dim 64 and 128, not %d", head_dim);
+        return fail(ATTN_ERR_UNSUPPORTED, "bf16 and fp16 support head_dim 64 and 128, not %d", head_dim);
     const int G = q_heads / kv_heads;
     if (G != 1 && G != 2 && G != 4 && G != 8)
         return fail(ATTN_ERR_UNSUPPORTED, "per-item caches support 1, 2, 4 or 8 query heads per kv head, not %d", G);
@@ -174,7 +176,7 @@ attn_status attn_decode_caches(const void* q, const void* const* k_caches, const
     if (s != ATTN_OK) return s;
     attn::WaitCtl wc{st->status, kWaitLimitNs};
     attn::CachesProblem p{q, k_caches, v_caches, out, m, q_heads, kv_heads, capacity, head_dim,
-                          kv_lens, sliding_window, scale};
+                          kv_lens, sliding_window, scale, dtype == ATTN_F16};
     cudaError_t e = attn::launch_decode_caches(p, wc, stream, st->num_sms);
     if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "decode_caches launch: %s", cudaGetErrorString(e));
     return ATTN_OK;

@@ -7,6 +7,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -170,6 +171,14 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
     return d;
 }
 
+// Instruction descriptor for kind::f16 with fp16 or bf16 A/B (both the same type) and fp32 D.
+//   A and B format: 0 = f16, 1 = bf16.
+__host__ __device__ constexpr uint32_t idesc_f16kind_f32(int M, int N, int a_mn_major, int b_mn_major, bool f16) {
+    return (1u << 4) | ((f16 ? 0u : 1u) << 7) | ((f16 ? 0u : 1u) << 10) |
+           (static_cast<uint32_t>(a_mn_major) << 15) | (static_cast<uint32_t>(b_mn_major) << 16) |
+           (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
 // Instruction descriptor for kind::f16 with bf16 A/B and fp32 D.
 //   D format bits 4-5 (1 = f32), A format bits 7-9 (1 = bf16), B format bits 10-12,
 //   A major bit 15 and B major bit 16 (0 = K-major, 1 = MN-major),
@@ -286,6 +295,34 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     uint32_t r;
     asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
     return r;
+}
+
+// Round two floats to a packed fp16 pair (lo in the low half), round-to-nearest-even.
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// A packed pair of the 16-bit element type: fp16 (F16) or bf16, round-to-nearest-even.
+template <bool F16>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+    if constexpr (F16) return pack_f16x2(lo, hi);
+    else return pack_bf16x2(lo, hi);
+}
+
+// The exact float values of a packed pair (low half in .x).
+template <bool F16>
+__device__ __forceinline__ float2 unpack2(uint32_t w) {
+    if constexpr (F16) {
+        float2 f;
+        asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\tcvt.f32.f16 %0, lo;\n\tcvt.f32.f16 %1, hi;\n\t}"
+            : "=f"(f.x), "=f"(f.y)
+            : "r"(w));
+        return f;
+    } else {
+        return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+    }
 }
 
 }  // namespace attn

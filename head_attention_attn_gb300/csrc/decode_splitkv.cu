@@ -1,4 +1,4 @@
-// decode_splitkv.cu -- K2: single-query (q_len == 1) attention against a KV cache, bf16,
+// decode_splitkv.cu -- K2: single-query (q_len == 1) attention against a KV cache, bf16 or fp16,
 // head_dim 64 or 128, bound by HBM bandwidth.
 //
 // Work unit: (batch b, kv head hk).  Its G = q_heads/kv_heads query heads are
@@ -10,7 +10,7 @@
 // and of V with bulk asynchronous copies (cp.async.bulk, completing on an mbarrier)
 // into a 4-stage shared-memory ring of 48-key stages, so about 100 KB per CTA is in
 // flight; six compute warps take 8 keys each of every chunk:
-//   - a key row (head_dim bf16) is spread over D/8 lanes, 16 bytes per lane, read
+//   - a key row (head_dim 16-bit values) is spread over D/8 lanes, 16 bytes per lane, read
 //     from shared memory with 128-bit loads, 2 (D=128) or 4 (D=64) rows per
 //     instruction;
 //   - q (pre-scaled by scale*log2(e)) lives in registers; the per-lane partial
@@ -22,7 +22,7 @@
 //     for the lane's 8 head dims, with packed f32x2 FMAs.
 // Combine: the lane groups of a warp merge with shuffles, the 6 warps merge
 // through shared memory, and the S CTAs of the cluster merge through
-// distributed shared memory in CTA rank 0, which normalises and stores bf16.
+// distributed shared memory in CTA rank 0, which normalises and stores the input type.
 // No global scratch memory is used.
 //
 // The operation is the q_len = 1 case of ferrum-kernels Backend::flash_attention
@@ -71,14 +71,12 @@ struct DCfg {
     static constexpr int kSmem = kStages * kStageBytes + 1024;  // ring + 1 KB alignment slack
 };
 
-// 8 bf16 (16 bytes) -> 4 float2 pairs (element 2i in .x, 2i+1 in .y).
-__device__ __forceinline__ void bf16x8_to_f2(const uint4& u, float2 (&f)[4]) {
+// 8 bf16 or fp16 values (16 bytes) -> 4 float2 pairs (element 2i in .x, 2i+1 in .y).
+template <bool F16>
+__device__ __forceinline__ void elem8_to_f2(const uint4& u, float2 (&f)[4]) {
     const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        f[i].x = __uint_as_float(w[i] << 16);
-        f[i].y = __uint_as_float(w[i] & 0xffff0000u);
-    }
+    for (int i = 0; i < 4; ++i) f[i] = unpack2<F16>(w[i]);
 }
 
 __device__ __forceinline__ float safe_ex2_diff(float a, float m) {
@@ -110,7 +108,7 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, const 
     }
 }
 
-template <int D, int G>
+template <int D, int G, bool F16>
 __global__ void __launch_bounds__(kThreads, 2) decode_splitkv_kernel(const DecodeParams p) {
     using C = DCfg<D, G>;
     constexpr int LPK = C::LPK, KPP = C::KPP, NP = C::NP, KB = C::KB, NV = C::NV;
@@ -224,7 +222,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_splitkv_kernel(const Decod
         for (int g = 0; g < G; ++g) {
             const __nv_bfloat16* qp = p.q + ((size_t)b * p.Hq + (size_t)hk * G + g) * D + 8 * gl;
             const uint4 u = *reinterpret_cast<const uint4*>(qp);
-            bf16x8_to_f2(u, qf[g]);
+            elem8_to_f2<F16>(u, qf[g]);
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 qf[g][i].x *= p.scale_log2;
@@ -268,7 +266,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_splitkv_kernel(const Decod
                 const bool valid = kb + r < kend;
                 const uint4 u = valid ? lds128(kst + r * C::kRowBytes) : make_uint4(0, 0, 0, 0);
                 float2 kf[4];
-                bf16x8_to_f2(u, kf);
+                elem8_to_f2<F16>(u, kf);
 #pragma unroll
                 for (int g = 0; g < G; ++g) {
                     float2 t = __fmul2_rn(qf[g][0], kf[0]);
@@ -364,7 +362,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_splitkv_kernel(const Decod
                 const int r = ps * KPP + grp;
                 const uint4 u = (kb + r < kend) ? lds128(vst + r * C::kRowBytes) : make_uint4(0, 0, 0, 0);
                 float2 vf[4];
-                bf16x8_to_f2(u, vf);
+                elem8_to_f2<F16>(u, vf);
                 float pv[G];
                 if constexpr (G % 4 == 0) {
 #pragma unroll
@@ -487,14 +485,16 @@ __global__ void __launch_bounds__(kThreads, 2) decode_splitkv_kernel(const Decod
                 l += f * ls[r];
             }
             const float res = (l > 0.f) ? o / l : 0.f;
-            p.out[((size_t)b * p.Hq + (size_t)hk * G + g) * D + d] = __float2bfloat16_rn(res);
+            const size_t oi = ((size_t)b * p.Hq + (size_t)hk * G + g) * D + d;
+            if constexpr (F16) reinterpret_cast<__half*>(p.out)[oi] = __float2half_rn(res);
+            else p.out[oi] = __float2bfloat16_rn(res);
         }
     }
     // keep every CTA's shared memory alive until rank 0 has read it
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
-template <int D, int G>
+template <int D, int G, bool F16>
 cudaError_t launch_dg(const DecodeParams& p, int B, int nsplit, cudaStream_t stream) {
     using C = DCfg<D, G>;
     int dev = 0;
@@ -505,7 +505,7 @@ cudaError_t launch_dg(const DecodeParams& p, int B, int nsplit, cudaStream_t str
     {
         std::lock_guard<std::mutex> g(mu);
         if (dev < 64 && !configured[dev]) {
-            e = cudaFuncSetAttribute(decode_splitkv_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+            e = cudaFuncSetAttribute(decode_splitkv_kernel<D, G, F16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      C::kSmem);
             if (e != cudaSuccess) return e;
             configured[dev] = true;
@@ -523,18 +523,23 @@ cudaError_t launch_dg(const DecodeParams& p, int B, int nsplit, cudaStream_t str
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, decode_splitkv_kernel<D, G>, p);
+    return cudaLaunchKernelEx(&cfg, decode_splitkv_kernel<D, G, F16>, p);
 }
 
-template <int D>
-cudaError_t launch_d(const DecodeParams& p, int G, int B, int nsplit, cudaStream_t s) {
+template <int D, bool F16>
+cudaError_t launch_dt(const DecodeParams& p, int G, int B, int nsplit, cudaStream_t s) {
     switch (G) {
-        case 1: return launch_dg<D, 1>(p, B, nsplit, s);
-        case 2: return launch_dg<D, 2>(p, B, nsplit, s);
-        case 4: return launch_dg<D, 4>(p, B, nsplit, s);
-        case 8: return launch_dg<D, 8>(p, B, nsplit, s);
+        case 1: return launch_dg<D, 1, F16>(p, B, nsplit, s);
+        case 2: return launch_dg<D, 2, F16>(p, B, nsplit, s);
+        case 4: return launch_dg<D, 4, F16>(p, B, nsplit, s);
+        case 8: return launch_dg<D, 8, F16>(p, B, nsplit, s);
         default: return cudaErrorInvalidValue;
     }
+}
+
+cudaError_t launch_any(const DecodeParams& p, int D, bool f16, int G, int B, int nsplit, cudaStream_t s) {
+    if (D == 64) return f16 ? launch_dt<64, true>(p, G, B, nsplit, s) : launch_dt<64, false>(p, G, B, nsplit, s);
+    return f16 ? launch_dt<128, true>(p, G, B, nsplit, s) : launch_dt<128, false>(p, G, B, nsplit, s);
 }
 
 }  // namespace
@@ -570,8 +575,7 @@ cudaError_t launch_decode_splitkv(const Problem& pr, const WaitCtl& wc, cudaStre
     long long by_len = (pr.Lk + 255) / 256;
     int nsplit = (int)std::max(1LL, std::min<long long>(kMaxSplits, std::min(want, by_len)));
     const int G = pr.Hq / pr.Hkv;
-    if (pr.D == 64) return launch_d<64>(p, G, pr.B, nsplit, stream);
-    return launch_d<128>(p, G, pr.B, nsplit, stream);
+    return launch_any(p, pr.D, pr.f16, G, pr.B, nsplit, stream);
 }
 
 cudaError_t launch_decode_caches(const CachesProblem& cp, const WaitCtl& wc, cudaStream_t stream, int num_sms) {
@@ -599,8 +603,7 @@ cudaError_t launch_decode_caches(const CachesProblem& cp, const WaitCtl& wc, cud
     long long by_len = (span + 255) / 256;
     int nsplit = (int)std::max(1LL, std::min<long long>(kMaxSplits, std::min(want, by_len)));
     const int G = cp.Hq / cp.Hkv;
-    if (cp.D == 64) return launch_d<64>(p, G, cp.m, nsplit, stream);
-    return launch_d<128>(p, G, cp.m, nsplit, stream);
+    return launch_any(p, cp.D, cp.f16, G, cp.m, nsplit, stream);
 }
 
 }  // namespace attn

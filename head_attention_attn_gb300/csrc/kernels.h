@@ -19,6 +19,7 @@ struct Problem {
     int pos_offset, mode, window;
     const int32_t* key_lens;
     float scale;
+    bool f16;  // 16-bit element type: fp16 (true) or bf16 (false); unused by the fp32 path
 };
 
 // Visible key interval [lo, hi) for queries at positions [qpos_lo, qpos_hi]
@@ -51,10 +52,10 @@ __device__ __forceinline__ int valid_keys(const int32_t* key_lens, int b, int Lk
     return n < 0 ? 0 : (n > Lk ? Lk : n);
 }
 
-// K1: tcgen05 + TMA fused prefill, bf16, head_dim 64 or 128.
+// K1: tcgen05 + TMA fused prefill, bf16 or fp16, head_dim 64 or 128.
 cudaError_t launch_prefill_tc(const Problem& p, const WaitCtl& wc, cudaStream_t stream);
 
-// K2: split-KV decode for q_len == 1, bf16, head_dim 64 or 128, group size 1/2/4/8.
+// K2: split-KV decode for q_len == 1, bf16 or fp16, head_dim 64 or 128, group size 1/2/4/8.
 bool decode_supported(const Problem& p);
 cudaError_t launch_decode_splitkv(const Problem& p, const WaitCtl& wc, cudaStream_t stream, int num_sms);
 
@@ -69,6 +70,7 @@ struct CachesProblem {
     const int32_t* kv_lens;
     int sliding;
     float scale;
+    bool f16;  // fp16 (true) or bf16 (false)
 };
 cudaError_t launch_decode_caches(const CachesProblem& p, const WaitCtl& wc, cudaStream_t stream, int num_sms);
 

@@ -1,4 +1,5 @@
-// prefill_tc.cu -- K1: fused attention prefill on the 5th-generation tensor cores (sm_103a).
+// prefill_tc.cu -- K1: fused attention prefill on the 5th-generation tensor cores (sm_103a),
+// bf16 or fp16 inputs and outputs, fp32 accumulation.
 //
 // One CTA computes NT 128-row query tiles (NT = 2 for head_dim 128, NT = 1 for
 // head_dim 64) of one (batch, query head), sharing every K and V tile between them:
@@ -10,7 +11,7 @@
 //                scores from TMEM, the two halves exchange their row maxima through
 //                shared memory, and each writes its 64 probabilities (2^x on the
 //                special-function unit, scale*log2(e) folded in) back into TMEM as
-//                packed bf16.  After the tile's last key block each half normalises
+//                packed 16-bit pairs (the input type: bf16 or fp16).  After the tile's last key block each half normalises
 //                and stores its half of the head dims of the row.
 // TMEM: S_0 .. S_{NT-1} | O_0 .. O_{NT-1}, 128 columns each; P_t aliases the first 64
 // columns of S_t.  With two tiles the MMA order is the ping-pong
@@ -141,7 +142,7 @@ struct TileRange {
     int jb, je;
 };
 
-template <int D, int NT>
+template <int D, int NT, bool F16>
 __global__ void __launch_bounds__(threads_for<NT>(), 3 - NT)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV, const PrefillParams p) {
@@ -261,8 +262,8 @@ __global__ void __launch_bounds__(threads_for<NT>(), 3 - NT)
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0 && ntiles > 0) {
-            constexpr uint32_t kIdescQK = idesc_bf16_f32(BM, BN, 0, 0);
-            constexpr uint32_t kIdescPV = idesc_bf16_f32(BM, D, 0, 1);
+            constexpr uint32_t kIdescQK = idesc_f16kind_f32(BM, BN, 0, 0, F16);
+            constexpr uint32_t kIdescPV = idesc_f16kind_f32(BM, D, 0, 1, F16);
             bool ok = mbar_wait(bar0 + 8 * kBarQFull, 0, p.wc, abort_flag);
             int it[kTiles] = {};  // local iteration (P phases consumed) per tile
             for (int j = 0; ok && j <= ntiles; ++j) {
@@ -405,7 +406,7 @@ __global__ void __launch_bounds__(threads_for<NT>(), 3 - NT)
             const float neg_m = (m_run == -INFINITY) ? 0.f : -m_run;
             const float2 sl2 = make_float2(sl, sl), negm2 = make_float2(neg_m, neg_m);
 
-            // P for my 64 keys -> TMEM columns [32h, 32h + 32) of S_t, as bf16 pairs; the row
+            // P for my 64 keys -> TMEM columns [32h, 32h + 32) of S_t, as bf16 or fp16 pairs; the row
             // sum adds the rounded values the tensor core will multiply into V.
             float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
 #pragma unroll
@@ -421,9 +422,9 @@ __global__ void __launch_bounds__(threads_for<NT>(), 3 - NT)
                         p0 = (c >= c_lo && c < c_hi) ? p0 : 0.f;
                         p1 = (c + 1 >= c_lo && c + 1 < c_hi) ? p1 : 0.f;
                     }
-                    const uint32_t wv = pack_bf16x2(p0, p1);
+                    const uint32_t wv = pack2<F16>(p0, p1);
                     pk[c2 / 2] = wv;
-                    const float2 r2 = make_float2(__uint_as_float(wv << 16), __uint_as_float(wv & 0xffff0000u));
+                    const float2 r2 = unpack2<F16>(wv);
                     if ((c2 / 2) & 1) acc1 = __fadd2_rn(acc1, r2); else acc0 = __fadd2_rn(acc0, r2);
                 }
                 tmem_st16_async(tS + 32 * h + 16 * k, pk);
@@ -478,10 +479,10 @@ __global__ void __launch_bounds__(threads_for<NT>(), 3 - NT)
                 if (qi < p.Lq) {
 #pragma unroll
                     for (int q = 0; q < 32; q += 8) {
-                        uint4 v4 = make_uint4(pack_bf16x2(o[q] * inv, o[q + 1] * inv),
-                                              pack_bf16x2(o[q + 2] * inv, o[q + 3] * inv),
-                                              pack_bf16x2(o[q + 4] * inv, o[q + 5] * inv),
-                                              pack_bf16x2(o[q + 6] * inv, o[q + 7] * inv));
+                        uint4 v4 = make_uint4(pack2<F16>(o[q] * inv, o[q + 1] * inv),
+                                              pack2<F16>(o[q + 2] * inv, o[q + 3] * inv),
+                                              pack2<F16>(o[q + 4] * inv, o[q + 5] * inv),
+                                              pack2<F16>(o[q + 6] * inv, o[q + 7] * inv));
                         *reinterpret_cast<uint4*>(orow + 32 * c + q) = v4;
                     }
                 }
@@ -518,28 +519,29 @@ EncodeTiledFn get_encode_fn() {
     return fn;
 }
 
-// [rows_outer, L, D] bf16 tensor viewed as 3-D (D, L, rows_outer); box 64 x 128 x 1, 128-byte swizzle,
-// out-of-range rows read as zeros.
-bool encode_bf16_3d(CUtensorMap* map, const void* base, int D, int L, int outer) {
+// [rows_outer, L, D] 16-bit tensor (bf16 or fp16) viewed as 3-D (D, L, rows_outer); box 64 x 128 x 1,
+// 128-byte swizzle, out-of-range rows read as zeros.
+bool encode_16bit_3d(CUtensorMap* map, const void* base, int D, int L, int outer, bool f16) {
     EncodeTiledFn fn = get_encode_fn();
     if (!fn) return false;
     cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)L, (cuuint64_t)outer};
     cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)L * D * 2};
     cuuint32_t box[3] = {64, 128, 1};
     cuuint32_t estr[3] = {1, 1, 1};
-    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+    CUresult r = fn(map, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
 
-template <int D, int NT>
+template <int D, int NT, bool F16>
 cudaError_t launch_impl(const Problem& pr, const WaitCtl& wc, cudaStream_t stream) {
     using C = Cfg<D, NT>;
     constexpr int kTiles = NT;
     CUtensorMap tq, tk, tv;
-    if (!encode_bf16_3d(&tq, pr.q, D, pr.Lq, pr.B * pr.Hq) || !encode_bf16_3d(&tk, pr.k, D, pr.Lk, pr.B * pr.Hkv) ||
-        !encode_bf16_3d(&tv, pr.v, D, pr.Lk, pr.B * pr.Hkv))
+    if (!encode_16bit_3d(&tq, pr.q, D, pr.Lq, pr.B * pr.Hq, F16) ||
+        !encode_16bit_3d(&tk, pr.k, D, pr.Lk, pr.B * pr.Hkv, F16) ||
+        !encode_16bit_3d(&tv, pr.v, D, pr.Lk, pr.B * pr.Hkv, F16))
         return cudaErrorInvalidValue;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -549,7 +551,7 @@ cudaError_t launch_impl(const Problem& pr, const WaitCtl& wc, cudaStream_t strea
     {
         std::lock_guard<std::mutex> g(mu);
         if (dev < 64 && !configured[dev]) {
-            e = cudaFuncSetAttribute(prefill_tc_kernel<D, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+            e = cudaFuncSetAttribute(prefill_tc_kernel<D, NT, F16>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
             if (e != cudaSuccess) return e;
             configured[dev] = true;
         }
@@ -570,7 +572,7 @@ cudaError_t launch_impl(const Problem& pr, const WaitCtl& wc, cudaStream_t strea
     p.wc = wc;
     const long long grid = (long long)p.num_m * pr.B * pr.Hq;
     if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    prefill_tc_kernel<D, NT><<<(unsigned)grid, threads_for<NT>(), C::kSmem, stream>>>(tq, tk, tv, p);
+    prefill_tc_kernel<D, NT, F16><<<(unsigned)grid, threads_for<NT>(), C::kSmem, stream>>>(tq, tk, tv, p);
     return cudaGetLastError();
 }
 
@@ -580,8 +582,8 @@ cudaError_t launch_prefill_tc(const Problem& p, const WaitCtl& wc, cudaStream_t 
     // head_dim 64: one query tile per CTA, so two CTAs share an SM (256 TMEM columns and
     // about 83 KB of shared memory each) and hide each other's set-up and epilogue.
     // head_dim 128: two tiles per CTA (512 TMEM columns, one CTA per SM), ping-pong inside.
-    if (p.D == 64) return launch_impl<64, 1>(p, wc, stream);
-    if (p.D == 128) return launch_impl<128, 2>(p, wc, stream);
+    if (p.D == 64) return p.f16 ? launch_impl<64, 1, true>(p, wc, stream) : launch_impl<64, 1, false>(p, wc, stream);
+    if (p.D == 128) return p.f16 ? launch_impl<128, 2, true>(p, wc, stream) : launch_impl<128, 2, false>(p, wc, stream);
     return cudaErrorInvalidValue;
 }
 

@@ -4,8 +4,8 @@ This module holds shapes, seeds and random draws only: no attention arithmetic.
 It imports neither the oracle nor the CUDA library.
 
 Draw order for every case: Q, K, V as float32 N(0, 1) from one CPU generator,
-then a cast to the case's dtype (bf16 rounding happens once, and both the
-oracle and the kernels read the rounded values), then the per-sequence valid
+then a cast to the case's dtype (bf16 or fp16 rounding happens once, and both
+the oracle and the kernels read the rounded values), then the per-sequence valid
 key lengths when the case has key padding.
 """
 from __future__ import annotations
@@ -21,7 +21,7 @@ MASK_NONE, MASK_CAUSAL, MASK_WINDOW, MASK_CAUSAL_WINDOW = 0, 1, 2, 3
 @dataclass(frozen=True)
 class Case:
     name: str
-    dtype: str            # "bf16" or "f32"
+    dtype: str            # "bf16", "f16" or "f32"
     B: int
     Hq: int
     Hkv: int
@@ -36,7 +36,7 @@ class Case:
 
     @property
     def torch_dtype(self):
-        return torch.bfloat16 if self.dtype == "bf16" else torch.float32
+        return {"bf16": torch.bfloat16, "f16": torch.float16, "f32": torch.float32}[self.dtype]
 
 
 # The five workloads the pages' encoder, prefill and decode paths are measured on.

@@ -74,8 +74,11 @@ typedef enum {
     ATTN_MASK_CAUSAL_WINDOW = 3
 } attn_mask_mode;
 
-/* Element type of q, k, v and out.  Accumulation is always fp32. */
-typedef enum { ATTN_BF16 = 0, ATTN_F32 = 1 } attn_dtype;
+/* Element type of q, k, v and out.  Accumulation is always fp32.
+ * ATTN_F16 follows the pages' CUDA activation type (ferrum-kernels
+ * activation_elem_size_bytes: fp16 on CUDA; ripvec-core's _f16 kernels with fp32
+ * reductions).  bf16 and fp16 take the same kernels and the same shape rules. */
+typedef enum { ATTN_BF16 = 0, ATTN_F32 = 1, ATTN_F16 = 2 } attn_dtype;
 
 /*
  * attn_fwd -- enqueue one attention forward pass on cuda_stream and return.
@@ -99,7 +102,7 @@ typedef enum { ATTN_BF16 = 0, ATTN_F32 = 1 } attn_dtype;
  *   cuda_stream A cudaStream_t.  NULL means the legacy default stream.
  *
  * Supported shapes:
- *   - bf16 needs head_dim 64 or 128, and the base addresses of q, k, v and out
+ *   - bf16 and fp16 need head_dim 64 or 128, and the base addresses of q, k, v and out
  *     aligned to 16 bytes.
  *   - f32 accepts any head_dim from 1 to 256, with 4-byte alignment.
  *   - batch or q_len 0: nothing is launched and ATTN_OK is returned.
@@ -137,10 +140,10 @@ ATTN_API attn_status attn_fwd(const void* q, const void* k, const void* v, void*
  * across M per-request caches that replaces the per-item flash_attention(q_len=1) loop.
  *
  * Arguments:
- *   q, out     [m, q_heads, head_dim] bf16, item-major, contiguous, 16-byte aligned.
+ *   q, out     [m, q_heads, head_dim] bf16 or fp16, item-major, contiguous, 16-byte aligned.
  *   k_caches, v_caches
  *              Device arrays of m device pointers.  Item i's K (and V) cache is
- *              [kv_heads, capacity, head_dim] bf16, head-major and contiguous; each
+ *              [kv_heads, capacity, head_dim] of the same type, head-major and contiguous; each
  *              pointer must be 16-byte aligned.
  *   kv_lens    Device int32 [m]: the valid cached positions of item i.  The value is
  *              clamped to [0, capacity].  It is read on the device, so a captured launch
@@ -149,7 +152,7 @@ ATTN_API attn_status attn_fwd(const void* q, const void* k, const void* v, void*
  *              0: item i's query, the newest position kv_lens[i]-1, sees positions
  *              0 .. kv_lens[i]-1.  w > 0: it sees only the last w of them.
  *   scale      Finite multiplier of the raw dot products.
- *   dtype      Must be ATTN_BF16.
+ *   dtype      ATTN_BF16 or ATTN_F16.
  *
  * Query head h reads kv head h / (q_heads / kv_heads).
  *

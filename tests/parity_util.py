@@ -10,6 +10,14 @@ import oracle
 BF16_MAX_ABS = 1e-2
 BF16_REL_L2 = 5e-3
 F32_MAX_ABS = 1e-4
+# fp16 (no stated target; derived from the arithmetic): P and the output are rounded to
+# fp16 (11 significant bits, half-ulp 2^-11 relative).  Output rounding is at most
+# |o| * 2^-11 <= 5 * 2^-11 ~ 2.4e-3 for N(0, 1) values, and the rounded-P weights move
+# an output by at most 2^-11 * max|v - o| ~ 4.4e-3 if every rounding error aligned, so
+# max-abs <= 5e-3 covers the sum with margin for fp32 accumulation; the relative L2 of
+# random rounding is ~2^-11 / sqrt(3) ~ 3e-4 per term, bounded here by 1e-3.
+F16_MAX_ABS = 5e-3
+F16_REL_L2 = 1e-3
 
 
 def errors(got: np.ndarray, ref: np.ndarray):
@@ -27,6 +35,9 @@ def assert_close(got, ref, dtype: str, what: str = ""):
     max_abs, rel_l2 = errors(got, ref)
     if dtype == "f32":
         assert max_abs <= F32_MAX_ABS, f"{what}: max-abs {max_abs:.3e} > {F32_MAX_ABS}"
+    elif dtype == "f16":
+        assert max_abs <= F16_MAX_ABS, f"{what}: max-abs {max_abs:.3e} > {F16_MAX_ABS}"
+        assert rel_l2 <= F16_REL_L2, f"{what}: rel-L2 {rel_l2:.3e} > {F16_REL_L2}"
     else:
         assert max_abs <= BF16_MAX_ABS, f"{what}: max-abs {max_abs:.3e} > {BF16_MAX_ABS}"
         assert rel_l2 <= BF16_REL_L2, f"{what}: rel-L2 {rel_l2:.3e} > {BF16_REL_L2}"

@@ -61,7 +61,7 @@ def _call(**kw):
     (dict(q_heads=3, kv_heads=2), "not a multiple"),
     (dict(mask_mode=4), "mask_mode"),
     (dict(mask_mode=-1), "mask_mode"),
-    (dict(dtype=2), "dtype"),
+    (dict(dtype=3), "dtype"),
     (dict(window=-1), "negative window"),
     (dict(pos_offset=-1), "negative pos_offset"),
     (dict(scale=float("nan")), "not finite"),
@@ -72,6 +72,7 @@ def _call(**kw):
     (dict(q_ptr=18), "aligned"),
     (dict(out_ptr=24), "aligned"),
     (dict(dtype=attn.ATTN_F32, k_ptr=18), "aligned"),
+    (dict(dtype=attn.ATTN_F16, v_ptr=24), "aligned"),
 ])
 def test_invalid_arguments_are_refused_before_launch(lib, change, fragment):
     assert _call(**change) == attn.ATTN_ERR_INVALID_ARG
@@ -79,6 +80,7 @@ def test_invalid_arguments_are_refused_before_launch(lib, change, fragment):
 
 
 @pytest.mark.parametrize("change", [dict(head_dim=32), dict(head_dim=96), dict(head_dim=256),
+                                    dict(dtype=attn.ATTN_F16, head_dim=96),
                                     dict(dtype=attn.ATTN_F32, head_dim=257)])
 def test_unsupported_head_dims(lib, change):
     assert _call(**change) == attn.ATTN_ERR_UNSUPPORTED
@@ -136,6 +138,8 @@ def _caches_call(lib, **kw):
     (dict(q=24), attn.ATTN_ERR_INVALID_ARG),
     (dict(kc=12), attn.ATTN_ERR_INVALID_ARG),
     (dict(dtype=attn.ATTN_F32), attn.ATTN_ERR_UNSUPPORTED),
+    (dict(dtype=3), attn.ATTN_ERR_UNSUPPORTED),
+    (dict(dtype=attn.ATTN_F16, d=96), attn.ATTN_ERR_UNSUPPORTED),
     (dict(d=96), attn.ATTN_ERR_UNSUPPORTED),
     (dict(hq=6, hkv=2), attn.ATTN_ERR_UNSUPPORTED),
     (dict(m=0), attn.ATTN_OK),
