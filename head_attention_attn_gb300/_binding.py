@@ -16,7 +16,7 @@ ATTN_OK, ATTN_ERR_INVALID_ARG, ATTN_ERR_UNSUPPORTED, ATTN_ERR_CUDA, ATTN_ERR_TIM
 MASK_NONE, MASK_CAUSAL, MASK_WINDOW, MASK_CAUSAL_WINDOW = 0, 1, 2, 3
 ATTN_BF16, ATTN_F32, ATTN_F16 = 0, 1, 2
 
-EXPORTED = ("attn_fwd", "attn_decode_caches", "attn_last_error", "attn_sync_status", "attn_selftest_timeout",
+EXPORTED = ("attn_fwd", "attn_fwd_varlen", "attn_decode_caches", "attn_last_error", "attn_sync_status", "attn_selftest_timeout",
             "attn_version")
 
 _STATUS_NAMES = {0: "ATTN_OK", 1: "ATTN_ERR_INVALID_ARG", 2: "ATTN_ERR_UNSUPPORTED", 3: "ATTN_ERR_CUDA",
@@ -52,6 +52,8 @@ def load(path: str | None = None):
         vp, ci = ctypes.c_void_p, ctypes.c_int
         lib.attn_fwd.restype = ci
         lib.attn_fwd.argtypes = [vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, ci, ci, ci, vp, ctypes.c_float, ci, vp]
+        lib.attn_fwd_varlen.restype = ci
+        lib.attn_fwd_varlen.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, ci, ci, ctypes.c_float, ci, vp]
         lib.attn_decode_caches.restype = ci
         lib.attn_decode_caches.argtypes = [vp, vp, vp, vp, ci, ci, ci, ci, ci, vp, ci, ctypes.c_float, ci, vp]
         lib.attn_last_error.restype = ctypes.c_char_p
@@ -138,6 +140,47 @@ def attn_fwd(q, k, v, out=None, *, pos_offset: int = 0, mask_mode: int = MASK_NO
     status = attn_fwd_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), B, Hq, Hkv, Lq, Lk, D,
                           int(pos_offset), int(mask_mode), int(window), kl_ptr, float(scale), dtype,
                           _stream_handle(stream))
+    _check(status)
+    return out
+
+
+def attn_fwd_varlen(q, k, v, cu_seqlens, max_seqlen: int, out=None, *, mask_mode: int = MASK_NONE,
+                    window: int = 0, scale: float | None = None, stream=None):
+    """Attention over packed sequences (see attn_fwd_varlen in attn.h).
+
+    q [total, Hq, D], k and v [total, Hkv, D]: contiguous bf16 or fp16 CUDA tensors,
+    token-major; cu_seqlens: int32 CUDA tensor [batch + 1]; max_seqlen: an upper bound
+    on every sequence length.  Returns out [total, Hq, D] without synchronising.
+    """
+    import torch
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not t.is_cuda or not t.is_contiguous() or t.dim() != 3:
+            raise ValueError(f"{name} must be a contiguous 3-D CUDA tensor [total, heads, D]")
+    if q.dtype != k.dtype or q.dtype != v.dtype:
+        raise ValueError("q, k, v must share a dtype")
+    if q.dtype == torch.bfloat16:
+        dtype = ATTN_BF16
+    elif q.dtype == torch.float16:
+        dtype = ATTN_F16
+    else:
+        raise ValueError(f"unsupported dtype {q.dtype} (bf16 or fp16)")
+    total, Hq, D = q.shape
+    if tuple(k.shape) != tuple(v.shape) or k.shape[0] != total or k.shape[2] != D:
+        raise ValueError("k and v must be [total, Hkv, D] matching q")
+    Hkv = k.shape[1]
+    if cu_seqlens.dtype != torch.int32 or not cu_seqlens.is_cuda or cu_seqlens.dim() != 1 or cu_seqlens.numel() < 1:
+        raise ValueError("cu_seqlens must be a 1-D int32 CUDA tensor [batch + 1]")
+    batch = cu_seqlens.numel() - 1
+    if out is None:
+        out = torch.empty_like(q)
+    elif out.shape != q.shape or out.dtype != q.dtype or not out.is_contiguous() or not out.is_cuda:
+        raise ValueError("out must be a contiguous CUDA tensor shaped and typed like q")
+    if scale is None:
+        scale = float(torch.tensor(1.0 / math.sqrt(D), dtype=torch.float32).item())
+    status = load().attn_fwd_varlen(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                    cu_seqlens.contiguous().data_ptr(), batch, total, int(max_seqlen), Hq, Hkv, D,
+                                    int(mask_mode), int(window), ctypes.c_float(scale), dtype,
+                                    _stream_handle(stream))
     _check(status)
     return out
 

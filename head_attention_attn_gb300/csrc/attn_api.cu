@@ -140,6 +140,48 @@ attn_status attn_fwd(const void* q, const void* k, const void* v, void* out, int
     return ATTN_OK;
 }
 
+attn_status attn_fwd_varlen(const void* q, const void* k, const void* v, void* out, const int32_t* cu_seqlens,
+                            int batch, int total, int max_seqlen, int q_heads, int kv_heads, int head_dim,
+                            int mask_mode, int window, float scale, int dtype, void* cuda_stream) {
+    t_last_error.clear();
+    if (batch < 0 || total < 0 || max_seqlen < 0)
+        return fail(ATTN_ERR_INVALID_ARG, "negative size (batch=%d, total=%d, max_seqlen=%d)", batch, total,
+                    max_seqlen);
+    if (q_heads <= 0 || kv_heads <= 0 || head_dim <= 0)
+        return fail(ATTN_ERR_INVALID_ARG, "q_heads, kv_heads and head_dim must be positive (%d, %d, %d)", q_heads,
+                    kv_heads, head_dim);
+    if (q_heads % kv_heads != 0)
+        return fail(ATTN_ERR_INVALID_ARG, "q_heads (%d) is not a multiple of kv_heads (%d)", q_heads, kv_heads);
+    if (mask_mode < ATTN_MASK_NONE || mask_mode > ATTN_MASK_CAUSAL_WINDOW)
+        return fail(ATTN_ERR_INVALID_ARG, "mask_mode %d out of range", mask_mode);
+    if (dtype != ATTN_BF16 && dtype != ATTN_F32 && dtype != ATTN_F16)
+        return fail(ATTN_ERR_INVALID_ARG, "dtype %d out of range", dtype);
+    if (window < 0) return fail(ATTN_ERR_INVALID_ARG, "negative window %d", window);
+    if (!isfinite(scale)) return fail(ATTN_ERR_INVALID_ARG, "scale is not finite");
+    if (dtype == ATTN_F32) return fail(ATTN_ERR_UNSUPPORTED, "packed sequences support bf16 and fp16");
+    if (head_dim != 64 && head_dim != 128)
+        return fail(ATTN_ERR_UNSUPPORTED, "bf16 and fp16 support head_dim 64 and 128, not %d", head_dim);
+    if (max_seqlen > total) return fail(ATTN_ERR_INVALID_ARG, "max_seqlen %d exceeds total %d", max_seqlen, total);
+    if (batch == 0 || max_seqlen == 0) return ATTN_OK;  // nothing to compute
+    const long long blocks = ((long long)max_seqlen + 255) / 128;  // upper bound on query blocks per head
+    if (blocks * batch * q_heads > 0x7fffffffLL)
+        return fail(ATTN_ERR_UNSUPPORTED, "max_seqlen * batch * q_heads is too large for one launch");
+    if (!q || !k || !v || !out) return fail(ATTN_ERR_INVALID_ARG, "null q, k, v or out pointer");
+    if (!cu_seqlens) return fail(ATTN_ERR_INVALID_ARG, "null cu_seqlens pointer");
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) || !aligned(cu_seqlens, 4))
+        return fail(ATTN_ERR_INVALID_ARG, "q, k, v and out must be 16-byte aligned, cu_seqlens 4-byte aligned");
+
+    DeviceState* st = nullptr;
+    attn_status s = device_state(&st);
+    if (s != ATTN_OK) return s;
+    attn::WaitCtl wc{st->status, kWaitLimitNs};
+    attn::Problem p{q, k, v, out, batch, q_heads, kv_heads, max_seqlen, max_seqlen, head_dim,
+                    0, mask_mode, window, nullptr, scale, dtype == ATTN_F16, cu_seqlens, total};
+    cudaError_t e = attn::launch_prefill_tc(p, wc, static_cast<cudaStream_t>(cuda_stream));
+    if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "prefill_tc launch: %s", cudaGetErrorString(e));
+    return ATTN_OK;
+}
+
 attn_status attn_decode_caches(const void* q, const void* const* k_caches, const void* const* v_caches, void* out,
                                int m, int q_heads, int kv_heads, int capacity, int head_dim, const int32_t* kv_lens,
                                int sliding_window, float scale, int dtype, void* cuda_stream) {
@@ -201,6 +243,9 @@ attn_status attn_sync_status(void* cuda_stream) {
         if (word == attn::kStatusTimeout) return fail(ATTN_ERR_TIMEOUT, "a device-side wait timed out");
         if (word == attn::kStatusBadPointer)
             return fail(ATTN_ERR_INVALID_ARG, "a per-item cache pointer is null or not 16-byte aligned");
+        if (word == attn::kStatusBadSeqlens)
+            return fail(ATTN_ERR_INVALID_ARG,
+                        "cu_seqlens is not non-decreasing from >= 0 to <= total with lengths <= max_seqlen");
         return fail(ATTN_ERR_CUDA, "device status word %u", word);
     }
     return ATTN_OK;

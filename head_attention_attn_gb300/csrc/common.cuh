@@ -16,6 +16,7 @@ namespace attn {
 // Status codes written to the device status word (same numbers as attn_status).
 constexpr unsigned kStatusTimeout = 4u;
 constexpr unsigned kStatusBadPointer = 5u;  // a device-side pointer argument was null or misaligned
+constexpr unsigned kStatusBadSeqlens = 6u;  // cu_seqlens is not a prefix sum within total and max_seqlen
 
 // Arguments every kernel receives for its bounded waits.
 struct WaitCtl {

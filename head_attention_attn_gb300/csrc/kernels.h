@@ -20,6 +20,11 @@ struct Problem {
     const int32_t* key_lens;
     float scale;
     bool f16;  // 16-bit element type: fp16 (true) or bf16 (false); unused by the fp32 path
+    // Packed sequences (K1 only): q/out [total, Hq, D] and k/v [total, Hkv, D] token-major,
+    // sequence b is rows [cu_seqlens[b], cu_seqlens[b+1]); Lq = Lk = the longest sequence.
+    // Null for the head-major batch layout.
+    const int32_t* cu_seqlens;
+    int total;
 };
 
 // Visible key interval [lo, hi) for queries at positions [qpos_lo, qpos_hi]

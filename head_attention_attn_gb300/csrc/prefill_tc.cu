@@ -82,7 +82,9 @@ struct PrefillParams {
     __nv_bfloat16* out;
     const int32_t* key_lens;
     int B, Hq, Hkv, Lq, Lk, P, mode, window;
-    int num_m;          // 256-row query blocks per head
+    int num_m;          // query blocks (NT tiles each) per head
+    const int32_t* cu_seqlens;  // packed token-major sequences [B + 1], or null (head-major batch)
+    int total;          // packed rows (token-major)
     float scale_log2;
     WaitCtl wc;
 };
@@ -142,7 +144,7 @@ struct TileRange {
     int jb, je;
 };
 
-template <int D, int NT, bool F16>
+template <int D, int NT, bool F16, bool TOK>
 __global__ void __launch_bounds__(threads_for<NT>(), 3 - NT)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV, const PrefillParams p) {
@@ -167,7 +169,22 @@ __global__ void __launch_bounds__(threads_for<NT>(), 3 - NT)
     const int mblk = p.num_m - 1 - idx;  // heaviest blocks first
     const int hk = hq / (p.Hq / p.Hkv);
     const int q0 = mblk * (kTiles * BM);
-    const int klen = valid_keys(p.key_lens, b, p.Lk);
+    // Rows of this item: the batch entry's Lq queries / Lk keys (head-major), or (TOK) packed
+    // sequence b, rows [row0, row0 + len) of the token-major tensors (self-attention).
+    constexpr bool tok = TOK;
+    int Lq = p.Lq, Lk = p.Lk, row0 = 0;
+    if constexpr (TOK) {
+        const int s0 = __ldg(p.cu_seqlens + b), s1 = __ldg(p.cu_seqlens + b + 1);
+        if (s0 < 0 || s1 < s0 || s1 > p.total || s1 - s0 > p.Lq) {
+            // not a prefix sum inside [0, total] with lengths <= max_seqlen: read nothing
+            if (threadIdx.x == 0 && mblk == 0) record_status(p.wc.status, kStatusBadSeqlens);
+            return;
+        }
+        row0 = s0;
+        Lq = Lk = s1 - s0;
+    }
+    if (q0 >= Lq) return;  // a packed sequence shorter than this query block (uniform exit)
+    const int klen = valid_keys(p.key_lens, b, Lk);
 
     // Visible key interval of each query tile, and the shared key-tile grid.
     long long tlo[kTiles], thi[kTiles];
@@ -175,12 +192,12 @@ __global__ void __launch_bounds__(threads_for<NT>(), 3 - NT)
 #pragma unroll
     for (int t = 0; t < kTiles; ++t) {
         const int qa = q0 + t * BM;
-        if (qa >= p.Lq) {
+        if (qa >= Lq) {
             tlo[t] = 0;
             thi[t] = 0;
             continue;
         }
-        const int qb = min(qa + BM, p.Lq) - 1;
+        const int qb = min(qa + BM, Lq) - 1;
         key_interval(p.mode, p.window, klen, (long long)p.P + qa, (long long)p.P + qb, &tlo[t], &thi[t]);
         if (thi[t] > tlo[t] && (kv0 < 0 || tlo[t] < kv0)) kv0 = tlo[t];
     }
@@ -230,8 +247,12 @@ __global__ void __launch_bounds__(threads_for<NT>(), 3 - NT)
             mbar_arrive_expect_tx(bar0 + 8 * kBarQFull, kTiles * C::kQBytes);
             for (int t = 0; t < kTiles; ++t)
                 for (int c = 0; c < C::kChunks; ++c)
-                    tma_load_3d(sbase + C::kOffQ + t * C::kQBytes + c * (BM * 128), &tmQ, bar0 + 8 * kBarQFull,
-                                c * 64, q0 + t * BM, qbh);
+                    if constexpr (TOK)
+                        tma_load_3d(sbase + C::kOffQ + t * C::kQBytes + c * (BM * 128), &tmQ, bar0 + 8 * kBarQFull,
+                                    c * 64, hq, row0 + q0 + t * BM);
+                    else
+                        tma_load_3d(sbase + C::kOffQ + t * C::kQBytes + c * (BM * 128), &tmQ, bar0 + 8 * kBarQFull,
+                                    c * 64, q0 + t * BM, qbh);
             int issued = 0;
             for (int j = 0; j < ntiles; ++j) {
                 const int s = j % kStages;
@@ -241,7 +262,7 @@ __global__ void __launch_bounds__(threads_for<NT>(), 3 - NT)
                 mbar_arrive_expect_tx(bar0 + 8 * (kBarKFull + s), C::kKVBytes);
                 for (int c = 0; c < C::kChunks; ++c)
                     tma_load_3d(sbase + C::kOffK + s * C::kKVBytes + c * (BN * 128), &tmK,
-                                bar0 + 8 * (kBarKFull + s), c * 64, krow, kbh);
+                                bar0 + 8 * (kBarKFull + s), c * 64, tok ? hk : krow, tok ? row0 + krow : kbh);
                 if (j >= kStages && !mbar_wait(bar0 + 8 * (kBarVEmpty + s), (n - 1) & 1, p.wc, abort_flag)) {
                     issued = 2 * j + 1;
                     break;
@@ -249,7 +270,7 @@ __global__ void __launch_bounds__(threads_for<NT>(), 3 - NT)
                 mbar_arrive_expect_tx(bar0 + 8 * (kBarVFull + s), C::kKVBytes);
                 for (int c = 0; c < C::kChunks; ++c)
                     tma_load_3d(sbase + C::kOffV + s * C::kKVBytes + c * (BN * 128), &tmV,
-                                bar0 + 8 * (kBarVFull + s), c * 64, krow, kbh);
+                                bar0 + 8 * (kBarVFull + s), c * 64, tok ? hk : krow, tok ? row0 + krow : kbh);
                 issued = 2 * j + 2;
             }
             drain_wait(bar0 + 8 * kBarQFull, 0, p.wc);
@@ -464,9 +485,11 @@ __global__ void __launch_bounds__(threads_for<NT>(), 3 - NT)
             ok = __all_sync(0xffffffffu, mbar_wait(bar0 + 8 * (kBarOFull + t), 0, p.wc, abort_flag));
             tc_fence_after();
         }
-        if (ok && q0 + t * BM < p.Lq) {
+        if (ok && q0 + t * BM < Lq) {
             const float inv = (l_tot > 0.f) ? 1.f / l_tot : 0.f;
-            __nv_bfloat16* orow = p.out + ((size_t)(b * p.Hq + hq) * p.Lq + qi) * D + (D / 2) * h;
+            __nv_bfloat16* orow =
+                p.out + (tok ? ((size_t)(row0 + qi) * p.Hq + hq) * D : ((size_t)(b * p.Hq + hq) * Lq + qi) * D) +
+                (D / 2) * h;
 #pragma unroll
             for (int c = 0; c < D / 64; ++c) {
                 float o[32];
@@ -476,7 +499,7 @@ __global__ void __launch_bounds__(threads_for<NT>(), 3 - NT)
 #pragma unroll
                     for (int q = 0; q < 32; ++q) o[q] = 0.f;
                 }
-                if (qi < p.Lq) {
+                if (qi < Lq) {
 #pragma unroll
                     for (int q = 0; q < 32; q += 8) {
                         uint4 v4 = make_uint4(pack2<F16>(o[q] * inv, o[q + 1] * inv),
@@ -534,15 +557,37 @@ bool encode_16bit_3d(CUtensorMap* map, const void* base, int D, int L, int outer
     return r == CUDA_SUCCESS;
 }
 
-template <int D, int NT, bool F16>
+// [total, H, D] 16-bit tensor (packed token-major rows) viewed as 3-D (D, H, total); box 64 x 1 x 128,
+// so one box is 128 consecutive rows of one head, laid out in shared memory exactly like the
+// head-major box above.  Rows past total read as zeros.
+bool encode_16bit_3d_tok(CUtensorMap* map, const void* base, int D, int H, int total, bool f16) {
+    EncodeTiledFn fn = get_encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)total};
+    cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2};
+    cuuint32_t box[3] = {64, 1, 128};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(map, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                    const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+template <int D, int NT, bool F16, bool TOK>
 cudaError_t launch_impl(const Problem& pr, const WaitCtl& wc, cudaStream_t stream) {
     using C = Cfg<D, NT>;
     constexpr int kTiles = NT;
     CUtensorMap tq, tk, tv;
-    if (!encode_16bit_3d(&tq, pr.q, D, pr.Lq, pr.B * pr.Hq, F16) ||
-        !encode_16bit_3d(&tk, pr.k, D, pr.Lk, pr.B * pr.Hkv, F16) ||
-        !encode_16bit_3d(&tv, pr.v, D, pr.Lk, pr.B * pr.Hkv, F16))
+    if (TOK) {
+        if (!encode_16bit_3d_tok(&tq, pr.q, D, pr.Hq, pr.total, F16) ||
+            !encode_16bit_3d_tok(&tk, pr.k, D, pr.Hkv, pr.total, F16) ||
+            !encode_16bit_3d_tok(&tv, pr.v, D, pr.Hkv, pr.total, F16))
+            return cudaErrorInvalidValue;
+    } else if (!encode_16bit_3d(&tq, pr.q, D, pr.Lq, pr.B * pr.Hq, F16) ||
+               !encode_16bit_3d(&tk, pr.k, D, pr.Lk, pr.B * pr.Hkv, F16) ||
+               !encode_16bit_3d(&tv, pr.v, D, pr.Lk, pr.B * pr.Hkv, F16)) {
         return cudaErrorInvalidValue;
+    }
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
@@ -551,7 +596,7 @@ cudaError_t launch_impl(const Problem& pr, const WaitCtl& wc, cudaStream_t strea
     {
         std::lock_guard<std::mutex> g(mu);
         if (dev < 64 && !configured[dev]) {
-            e = cudaFuncSetAttribute(prefill_tc_kernel<D, NT, F16>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+            e = cudaFuncSetAttribute(prefill_tc_kernel<D, NT, F16, TOK>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
             if (e != cudaSuccess) return e;
             configured[dev] = true;
         }
@@ -567,12 +612,14 @@ cudaError_t launch_impl(const Problem& pr, const WaitCtl& wc, cudaStream_t strea
     p.P = pr.pos_offset;
     p.mode = pr.mode;
     p.window = pr.window;
-    p.num_m = (pr.Lq + kTiles * BM - 1) / (kTiles * BM);
+    p.num_m = (pr.Lq + kTiles * BM - 1) / (kTiles * BM);  // pr.Lq is max_seqlen for packed sequences
+    p.cu_seqlens = pr.cu_seqlens;
+    p.total = pr.total;
     p.scale_log2 = pr.scale * kLog2e;
     p.wc = wc;
     const long long grid = (long long)p.num_m * pr.B * pr.Hq;
     if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    prefill_tc_kernel<D, NT, F16><<<(unsigned)grid, threads_for<NT>(), C::kSmem, stream>>>(tq, tk, tv, p);
+    prefill_tc_kernel<D, NT, F16, TOK><<<(unsigned)grid, threads_for<NT>(), C::kSmem, stream>>>(tq, tk, tv, p);
     return cudaGetLastError();
 }
 
@@ -582,8 +629,15 @@ cudaError_t launch_prefill_tc(const Problem& p, const WaitCtl& wc, cudaStream_t 
     // head_dim 64: one query tile per CTA, so two CTAs share an SM (256 TMEM columns and
     // about 83 KB of shared memory each) and hide each other's set-up and epilogue.
     // head_dim 128: two tiles per CTA (512 TMEM columns, one CTA per SM), ping-pong inside.
-    if (p.D == 64) return p.f16 ? launch_impl<64, 1, true>(p, wc, stream) : launch_impl<64, 1, false>(p, wc, stream);
-    if (p.D == 128) return p.f16 ? launch_impl<128, 2, true>(p, wc, stream) : launch_impl<128, 2, false>(p, wc, stream);
+    const bool tok = p.cu_seqlens != nullptr;
+    if (p.D == 64) {
+        if (tok) return p.f16 ? launch_impl<64, 1, true, true>(p, wc, stream) : launch_impl<64, 1, false, true>(p, wc, stream);
+        return p.f16 ? launch_impl<64, 1, true, false>(p, wc, stream) : launch_impl<64, 1, false, false>(p, wc, stream);
+    }
+    if (p.D == 128) {
+        if (tok) return p.f16 ? launch_impl<128, 2, true, true>(p, wc, stream) : launch_impl<128, 2, false, true>(p, wc, stream);
+        return p.f16 ? launch_impl<128, 2, true, false>(p, wc, stream) : launch_impl<128, 2, false, false>(p, wc, stream);
+    }
     return cudaErrorInvalidValue;
 }
 

@@ -133,6 +133,50 @@ ATTN_API attn_status attn_fwd(const void* q, const void* k, const void* v, void*
                      float scale, int dtype, void* cuda_stream);
 
 /*
+ * attn_fwd_varlen -- attention over a batch of packed (unpadded) sequences.
+ *
+ * Source: ripvec-core Driver::prepare_batch_unpadded, which concatenates all tokens flat
+ * and returns cu_seqlens for the attention boundaries; there attention pads around the
+ * per-head operations (fused_pad_qkv_split_f16: [total_tokens, 3*hidden] to
+ * [batch*heads, max_seq, head_dim]) and unpads afterwards (fused_reshape_unpad_f16).
+ * Here attention works on the flat layout directly, so neither copy exists and no
+ * padded query row is computed.
+ *
+ * Layout (caller-owned device memory, contiguous, token-major):
+ *   q, out      [total, q_heads, head_dim]   (hidden = q_heads * head_dim per token)
+ *   k, v        [total, kv_heads, head_dim]
+ *   cu_seqlens  [batch + 1] int32 in device memory: sequence b is rows
+ *               [cu_seqlens[b], cu_seqlens[b+1]) of every tensor.
+ *
+ * Each sequence attends to itself: query row i of sequence b sees key rows of the same
+ * sequence by mask_mode and window exactly as attn_fwd does with pos_offset 0 and no
+ * key padding (causal: j <= i; window modes as in attn_mask_mode).  Query head h reads
+ * kv head h / (q_heads / kv_heads).  Rows of out outside every sequence are not written.
+ *
+ * Arguments:
+ *   batch       number of sequences.
+ *   total       rows of q, k, v and out.
+ *   max_seqlen  an upper bound on every sequence length; it sizes the launch.
+ *   scale, dtype, cuda_stream: as for attn_fwd.  dtype must be ATTN_BF16 or ATTN_F16.
+ *
+ * Supported: head_dim 64 or 128, 16-byte aligned q, k, v, out, 4-byte aligned
+ * cu_seqlens; otherwise ATTN_ERR_UNSUPPORTED (fp32, other head_dim) or
+ * ATTN_ERR_INVALID_ARG.  batch 0 or max_seqlen 0 launches nothing.
+ *
+ * Errors: host-visible arguments are checked before the launch (max_seqlen > total is
+ * ATTN_ERR_INVALID_ARG).  cu_seqlens lives on the device and is checked there: a
+ * sequence with cu_seqlens[b] < 0, cu_seqlens[b+1] < cu_seqlens[b], cu_seqlens[b+1] >
+ * total or a length above max_seqlen is not read and its rows are not written, and
+ * attn_sync_status() reports ATTN_ERR_INVALID_ARG.
+ *
+ * The library allocates nothing and keeps no pointer after the call.
+ */
+ATTN_API attn_status attn_fwd_varlen(const void* q, const void* k, const void* v, void* out,
+                                     const int32_t* cu_seqlens, int batch, int total, int max_seqlen,
+                                     int q_heads, int kv_heads, int head_dim, int mask_mode, int window,
+                                     float scale, int dtype, void* cuda_stream);
+
+/*
  * attn_decode_caches -- one decode step for m items, each against its own KV cache, in
  * one launch.
  *

@@ -146,3 +146,35 @@ def _caches_call(lib, **kw):
 ])
 def test_decode_caches_arguments(lib, change, status):
     assert _caches_call(lib, **change) == status
+
+
+def _varlen_call(lib, **kw):
+    args = dict(q=16, k=16, v=16, out=16, cu=16, batch=2, total=64, maxlen=40, hq=4, hkv=2, d=64, mode=0, win=0,
+                scale=0.125, dtype=attn.ATTN_BF16, stream=None)
+    args.update(kw)
+    return lib.attn_fwd_varlen(args["q"], args["k"], args["v"], args["out"], args["cu"], args["batch"],
+                               args["total"], args["maxlen"], args["hq"], args["hkv"], args["d"], args["mode"],
+                               args["win"], ctypes.c_float(args["scale"]), args["dtype"], args["stream"])
+
+
+@pytest.mark.parametrize("change,status", [
+    (dict(batch=-1), attn.ATTN_ERR_INVALID_ARG),
+    (dict(total=-1), attn.ATTN_ERR_INVALID_ARG),
+    (dict(maxlen=65), attn.ATTN_ERR_INVALID_ARG),
+    (dict(hq=3), attn.ATTN_ERR_INVALID_ARG),
+    (dict(mode=5), attn.ATTN_ERR_INVALID_ARG),
+    (dict(win=-1), attn.ATTN_ERR_INVALID_ARG),
+    (dict(scale=float("inf")), attn.ATTN_ERR_INVALID_ARG),
+    (dict(cu=None), attn.ATTN_ERR_INVALID_ARG),
+    (dict(cu=18), attn.ATTN_ERR_INVALID_ARG),
+    (dict(q=None), attn.ATTN_ERR_INVALID_ARG),
+    (dict(out=40), attn.ATTN_ERR_INVALID_ARG),
+    (dict(dtype=attn.ATTN_F32), attn.ATTN_ERR_UNSUPPORTED),
+    (dict(d=96), attn.ATTN_ERR_UNSUPPORTED),
+    (dict(batch=0), attn.ATTN_OK),
+    (dict(maxlen=0), attn.ATTN_OK),
+])
+def test_varlen_arguments(lib, change, status):
+    assert _varlen_call(lib, **change) == status
+    if status != attn.ATTN_OK:
+        assert attn.last_error() != ""
