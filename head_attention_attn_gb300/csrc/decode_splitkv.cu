@@ -542,6 +542,20 @@ cudaError_t launch_any(const DecodeParams& p, int D, bool f16, int G, int B, int
     return f16 ? launch_dt<128, true>(p, G, B, nsplit, s) : launch_dt<128, false>(p, G, B, nsplit, s);
 }
 
+// Split count (cluster size) for `units` (item, kv head) pairs of up to `span` keys each.
+// Measured on GB300 over batch 1-64, 512-32768 keys: fewer, longer CTAs win as long as
+// there are about 256 of them (their pipeline fill and the cluster combine cost more than
+// a partly filled last wave), a split should cover at least 1024 keys, and with 256 or
+// more units two splits beat one.
+int choose_splits(long long units, long long span, int num_sms) {
+    const long long target = num_sms > 0 ? (27LL * num_sms) / 16 : 256;  // about 1.7 CTAs per SM (256 on 152 SMs)
+    int n = 1;
+    while (n < kMaxSplits && units * n < target) n *= 2;
+    if (units >= 256) n = std::max(n, 2);
+    const long long by_len = std::max(1LL, span / 1024);
+    return (int)std::max(1LL, std::min<long long>(n, by_len));
+}
+
 }  // namespace
 
 bool decode_supported(const Problem& p) {
@@ -569,11 +583,7 @@ cudaError_t launch_decode_splitkv(const Problem& pr, const WaitCtl& wc, cudaStre
     p.scale_log2 = pr.scale * kLog2e;
     p.wc = wc;
     if (pr.Hkv > 65535 || pr.B > 65535) return cudaErrorInvalidConfiguration;
-    // Splits: enough CTAs for several waves over the SMs, at least 256 keys per split.
-    const long long units = (long long)pr.B * pr.Hkv;
-    long long want = (8LL * (num_sms > 0 ? num_sms : 148) + units - 1) / units;
-    long long by_len = (pr.Lk + 255) / 256;
-    int nsplit = (int)std::max(1LL, std::min<long long>(kMaxSplits, std::min(want, by_len)));
+    const int nsplit = choose_splits((long long)pr.B * pr.Hkv, pr.Lk, num_sms);
     const int G = pr.Hq / pr.Hkv;
     return launch_any(p, pr.D, pr.f16, G, pr.B, nsplit, stream);
 }
@@ -597,11 +607,8 @@ cudaError_t launch_decode_caches(const CachesProblem& cp, const WaitCtl& wc, cud
     p.scale_log2 = cp.scale * kLog2e;
     p.wc = wc;
     if (cp.Hkv > 65535 || cp.m > 65535) return cudaErrorInvalidConfiguration;
-    const long long units = (long long)cp.m * cp.Hkv;
-    long long want = (8LL * (num_sms > 0 ? num_sms : 148) + units - 1) / units;
-    long long span = cp.sliding > 0 ? std::min(cp.sliding, cp.capacity) : cp.capacity;
-    long long by_len = (span + 255) / 256;
-    int nsplit = (int)std::max(1LL, std::min<long long>(kMaxSplits, std::min(want, by_len)));
+    const long long span = cp.sliding > 0 ? std::min(cp.sliding, cp.capacity) : cp.capacity;
+    const int nsplit = choose_splits((long long)cp.m * cp.Hkv, span, num_sms);
     const int G = cp.Hq / cp.Hkv;
     return launch_any(p, cp.D, cp.f16, G, cp.m, nsplit, stream);
 }
