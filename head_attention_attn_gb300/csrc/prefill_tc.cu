@@ -439,7 +439,10 @@ __global__ void __launch_bounds__(threads_for<NT>(), 3 - NT)
                     const float2 x2 = __ffma2_rn(make_float2(s[c], s[c + 1]), sl2, negm2);
                     float p0 = ex2_approx(x2.x);  // special-function unit; 2^-inf = 0
                     float p1 = ex2_approx(x2.y);
-                    if (!full) {  // masked columns get exactly 0 (also when scale is 0 or negative)
+                    // Masked scores hold -inf (or +inf with a negative scale), so their
+                    // 2^(s*scale*log2e - m) is already exactly 0; only scale 0 turns them
+                    // into NaN (inf * 0) and needs the explicit zero.
+                    if (!full && sl == 0.f) {
                         p0 = (c >= c_lo && c < c_hi) ? p0 : 0.f;
                         p1 = (c + 1 >= c_lo && c + 1 < c_hi) ? p1 : 0.f;
                     }
