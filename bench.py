@@ -4,7 +4,8 @@
 One step is one attn_fwd call on the headline workload: causal GQA prefill,
 bf16, batch 4, 32 query / 8 kv heads, 4096 tokens, head_dim 128.  The same run
 also times the KV-cache decode workload (batch 64, 32/8 heads, 8192 cached
-keys, head_dim 128) and the two smaller prefill workloads, and reports each
+keys, head_dim 128), the attention prelude (split QKV + QK norm + RoPE for the
+headline's 16384 tokens) and the two smaller prefill workloads, and reports each
 against its roofline.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
@@ -208,6 +209,35 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(rows)}
 
 
+def prelude_leg(args, world, dev, peaks, peak_src):
+    """GB/s of attn_qkv_prelude on 16384 tokens of a 32q/8kv, head_dim 128 layer (qk_mode 1)."""
+    import head_attention_attn_gb300 as attn
+    T, Hq, Hkv, hd = 16384, 32, 8, 128
+    g = torch.Generator().manual_seed(1005)
+    qkv = torch.randn(T, (Hq + 2 * Hkv) * hd, generator=g).to(torch.bfloat16).to(dev)
+    w = (torch.rand(hd, generator=g) + 0.5).to(dev)
+    j = torch.arange(hd // 2, dtype=torch.float64)
+    ang = torch.arange(T, dtype=torch.float64)[:, None] * 1.0e6 ** (-2.0 * j / hd)[None, :]
+    cos, sin = torch.cos(ang).float().to(dev), torch.sin(ang).float().to(dev)
+    q = torch.empty(Hq, T, hd, dtype=torch.bfloat16, device=dev)
+
+    def call():
+        attn.attn_qkv_prelude(qkv, Hq, Hkv, hd, qk_mode=attn.QK_NORM_ROPE, cos=cos, sin=sin, q_norm_w=w, k_norm_w=w,
+                              q_out=q)
+    steps = max(3, min(args.steps, 500))
+    sec = time_device(call, steps, args.warmup, world, dev)
+    if attn.sync_status() != attn.ATTN_OK:
+        raise RuntimeError("device status after the prelude: " + attn.last_error())
+    nbytes = 2.0 * qkv.numel() * 2 + cos.numel() * 4 * 2 + 2 * hd * 4  # qkv in, q/k/v out, tables, weights
+    gbs = nbytes / sec / 1e9
+    return {"workload": "qkv_prelude_bf16_16384x32q8kv_128_normrope", "value": round(gbs * world, 1), "unit": "GB/s",
+            "steps": steps, "ms_per_step": round(sec * 1e3, 4),
+            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": round(gbs / peaks["hbm_gbs"], 4), "peak_source": f"{peak_src} HBM copy",
+                         "traffic": None, "kernel": "prelude_kernel<128, bf16>", "algorithmic_bytes_per_launch": nbytes},
+            "l2": f"inputs {qkv.numel() * 2 / 1e6:.0f} MB > {L2_BYTES / 1e6:.0f} MB L2, no flush"}
+
+
 def kernel_source_hash() -> str:
     h = hashlib.sha1()
     for rel in ("head_attention_attn_gb300/csrc/prefill_tc.cu", "head_attention_attn_gb300/csrc/common.cuh"):
@@ -356,6 +386,10 @@ def run_ours(args, rank, world, local):
     del host_d, devt_d
     torch.cuda.empty_cache()
 
+    # ---- attention prelude leg: split fused QKV + QK RMS norm + RoPE + head-major transpose for
+    # the headline workload's 4 x 4096 tokens (32 q / 8 kv heads, head_dim 128, bf16)
+    prelude = prelude_leg(args, world, dev, peaks, peak_src)
+
     # ---- the other prefill workloads (smaller; context)
     per_config = []
     for name in EXTRA_PREFILL:
@@ -395,7 +429,7 @@ def run_ours(args, rank, world, local):
                    "l2": f"inputs {bytes_of(c) / 1e6:.0f} MB > {L2_BYTES / 1e6:.0f} MB L2, no flush",
                    "parallelism": f"replicas x{world}"},
         "roofline": roof, "e2e": e2e, "gpu_launches": args.steps, "clocks": clocks, "decode": decode,
-        "per_config": per_config,
+        "prelude": prelude, "per_config": per_config,
     }
     if rank == 0 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(args.cpu_seconds)

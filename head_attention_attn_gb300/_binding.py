@@ -14,9 +14,10 @@ from .build import LIB_PATH
 
 ATTN_OK, ATTN_ERR_INVALID_ARG, ATTN_ERR_UNSUPPORTED, ATTN_ERR_CUDA, ATTN_ERR_TIMEOUT = range(5)
 MASK_NONE, MASK_CAUSAL, MASK_WINDOW, MASK_CAUSAL_WINDOW = 0, 1, 2, 3
+QK_COPY, QK_NORM_ROPE, QK_ROPE, QK_ROPE_INTERLEAVED = 0, 1, 2, 3
 ATTN_BF16, ATTN_F32, ATTN_F16 = 0, 1, 2
 
-EXPORTED = ("attn_fwd", "attn_fwd_varlen", "attn_decode_caches", "attn_last_error", "attn_sync_status", "attn_selftest_timeout",
+EXPORTED = ("attn_fwd", "attn_fwd_varlen", "attn_decode_caches", "attn_qkv_prelude", "attn_last_error", "attn_sync_status", "attn_selftest_timeout",
             "attn_version")
 
 _STATUS_NAMES = {0: "ATTN_OK", 1: "ATTN_ERR_INVALID_ARG", 2: "ATTN_ERR_UNSUPPORTED", 3: "ATTN_ERR_CUDA",
@@ -54,6 +55,9 @@ def load(path: str | None = None):
         lib.attn_fwd.argtypes = [vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, ci, ci, ci, vp, ctypes.c_float, ci, vp]
         lib.attn_fwd_varlen.restype = ci
         lib.attn_fwd_varlen.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, ci, ci, ctypes.c_float, ci, vp]
+        lib.attn_qkv_prelude.restype = ci
+        lib.attn_qkv_prelude.argtypes = [vp, vp, vp, vp, vp, ci, vp, vp, vp, ci, ci, ci, ci, ci, ctypes.c_float, ci,
+                                         ci, ci, ci, vp]
         lib.attn_decode_caches.restype = ci
         lib.attn_decode_caches.argtypes = [vp, vp, vp, vp, ci, ci, ci, ci, ci, vp, ci, ctypes.c_float, ci, vp]
         lib.attn_last_error.restype = ctypes.c_char_p
@@ -183,6 +187,70 @@ def attn_fwd_varlen(q, k, v, cu_seqlens, max_seqlen: int, out=None, *, mask_mode
                                     _stream_handle(stream))
     _check(status)
     return out
+
+
+def attn_qkv_prelude(qkv, q_heads: int, kv_heads: int, head_dim: int, *, qk_mode: int = QK_ROPE, cos=None,
+                     sin=None, q_norm_w=None, k_norm_w=None, pos_offset: int = 0, eps: float = 1e-6,
+                     q_out=None, k_cache=None, v_cache=None, cache_len: int = 0, stream=None):
+    """The attention prelude (see attn_qkv_prelude in attn.h) on CUDA tensors.
+
+    qkv [tokens, (q_heads + 2*kv_heads) * head_dim] bf16 or fp16; cos, sin fp32
+    [positions, head_dim/2]; q_norm_w, k_norm_w fp32 [head_dim].  Without caches it
+    returns (q [q_heads, tokens, hd], k [kv_heads, tokens, hd], v [kv_heads, tokens, hd]);
+    with k_cache/v_cache [kv_heads, capacity, hd] it writes rows cache_len .. cache_len +
+    tokens - 1 of them and returns (q, k_cache, v_cache).  Synchronises nothing.
+    """
+    import torch
+    if not qkv.is_cuda or qkv.dim() != 2 or not qkv.is_contiguous():
+        raise ValueError("qkv must be a contiguous 2-D CUDA tensor [tokens, features]")
+    if qkv.dtype == torch.bfloat16:
+        dtype = ATTN_BF16
+    elif qkv.dtype == torch.float16:
+        dtype = ATTN_F16
+    else:
+        raise ValueError("qkv must be bf16 or fp16")
+    tokens = qkv.shape[0]
+    if qkv.shape[1] != (q_heads + 2 * kv_heads) * head_dim:
+        raise ValueError("qkv must have (q_heads + 2*kv_heads) * head_dim features")
+
+    def f32(t, name, n=None):
+        if t is None:
+            return None
+        if not t.is_cuda or t.dtype != torch.float32 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous fp32 CUDA tensor")
+        if n is not None and t.numel() != n:
+            raise ValueError(f"{name} must have {n} values")
+        return t
+
+    cos, sin = f32(cos, "cos"), f32(sin, "sin")
+    q_norm_w, k_norm_w = f32(q_norm_w, "q_norm_w", head_dim), f32(k_norm_w, "k_norm_w", head_dim)
+    positions = 0
+    if cos is not None:
+        if sin is None or cos.shape != sin.shape or cos.dim() != 2 or cos.shape[1] != head_dim // 2:
+            raise ValueError("cos and sin must be [positions, head_dim/2]")
+        positions = cos.shape[0]
+    if q_out is None:
+        q_out = torch.empty((q_heads, tokens, head_dim), dtype=qkv.dtype, device=qkv.device)
+    if k_cache is None:
+        if v_cache is not None:
+            raise ValueError("give both caches or neither")
+        k_out = torch.empty((kv_heads, tokens, head_dim), dtype=qkv.dtype, device=qkv.device)
+        v_out = torch.empty_like(k_out)
+        capacity = 0
+    else:
+        if v_cache is None or k_cache.shape != v_cache.shape or k_cache.dim() != 3:
+            raise ValueError("k_cache and v_cache must be [kv_heads, capacity, head_dim] of one shape")
+        if k_cache.shape[0] != kv_heads or k_cache.shape[2] != head_dim or k_cache.dtype != qkv.dtype:
+            raise ValueError("caches must be [kv_heads, capacity, head_dim] of qkv's dtype")
+        k_out, v_out = k_cache, v_cache
+        capacity = k_cache.shape[1]
+    ptr = (lambda t: None if t is None else t.data_ptr())
+    status = load().attn_qkv_prelude(qkv.data_ptr(), ptr(q_norm_w), ptr(k_norm_w), ptr(cos), ptr(sin), positions,
+                                     q_out.data_ptr(), k_out.data_ptr(), v_out.data_ptr(), tokens, q_heads, kv_heads,
+                                     head_dim, int(pos_offset), ctypes.c_float(eps), int(qk_mode), int(cache_len),
+                                     capacity, dtype, _stream_handle(stream))
+    _check(status)
+    return q_out, k_out, v_out
 
 
 def attn_decode_caches(q, k_caches, v_caches, kv_lens, out=None, *, sliding_window: int = 0,

@@ -224,6 +224,47 @@ attn_status attn_decode_caches(const void* q, const void* const* k_caches, const
     return ATTN_OK;
 }
 
+attn_status attn_qkv_prelude(const void* qkv, const float* q_norm_w, const float* k_norm_w, const float* cos,
+                             const float* sin, int rope_positions, void* q_out, void* k_out, void* v_out, int tokens,
+                             int q_heads, int kv_heads, int head_dim, int pos_offset, float eps, int qk_mode,
+                             int cache_len, int cache_capacity, int dtype, void* cuda_stream) {
+    t_last_error.clear();
+    if (tokens < 0 || pos_offset < 0 || cache_len < 0 || cache_capacity < 0 || rope_positions < 0)
+        return fail(ATTN_ERR_INVALID_ARG, "negative size or offset (tokens=%d, pos_offset=%d, cache_len=%d, "
+                    "cache_capacity=%d, rope_positions=%d)", tokens, pos_offset, cache_len, cache_capacity,
+                    rope_positions);
+    if (q_heads <= 0 || kv_heads <= 0 || head_dim <= 0)
+        return fail(ATTN_ERR_INVALID_ARG, "q_heads, kv_heads and head_dim must be positive (%d, %d, %d)", q_heads,
+                    kv_heads, head_dim);
+    if (qk_mode < 0 || qk_mode > 3) return fail(ATTN_ERR_INVALID_ARG, "qk_mode %d out of range", qk_mode);
+    if (dtype != ATTN_BF16 && dtype != ATTN_F32 && dtype != ATTN_F16)
+        return fail(ATTN_ERR_INVALID_ARG, "dtype %d out of range", dtype);
+    if (dtype == ATTN_F32) return fail(ATTN_ERR_UNSUPPORTED, "the prelude supports bf16 and fp16");
+    if (head_dim != 64 && head_dim != 128)
+        return fail(ATTN_ERR_UNSUPPORTED, "the prelude supports head_dim 64 and 128, not %d", head_dim);
+    if (qk_mode == 1 && (!isfinite(eps) || eps < 0.f))
+        return fail(ATTN_ERR_INVALID_ARG, "eps must be finite and >= 0");
+    if (cache_capacity > 0 && (long long)cache_len + tokens > cache_capacity)
+        return fail(ATTN_ERR_INVALID_ARG, "cache_len %d + tokens %d exceeds cache_capacity %d", cache_len, tokens,
+                    cache_capacity);
+    if (qk_mode != 0 && (long long)pos_offset + tokens > rope_positions)
+        return fail(ATTN_ERR_INVALID_ARG, "positions up to %lld exceed the %d rows of the cos/sin tables",
+                    (long long)pos_offset + tokens, rope_positions);
+    if (tokens == 0) return ATTN_OK;
+    if (!qkv || !q_out || !k_out || !v_out) return fail(ATTN_ERR_INVALID_ARG, "null qkv, q_out, k_out or v_out");
+    if (!aligned(qkv, 16) || !aligned(q_out, 16) || !aligned(k_out, 16) || !aligned(v_out, 16))
+        return fail(ATTN_ERR_INVALID_ARG, "qkv, q_out, k_out and v_out must be 16-byte aligned");
+    if (qk_mode != 0 && (!cos || !sin || !aligned(cos, 16) || !aligned(sin, 16)))
+        return fail(ATTN_ERR_INVALID_ARG, "cos and sin must be non-null and 16-byte aligned");
+    if (qk_mode == 1 && (!q_norm_w || !k_norm_w || !aligned(q_norm_w, 4) || !aligned(k_norm_w, 4)))
+        return fail(ATTN_ERR_INVALID_ARG, "q_norm_w and k_norm_w must be non-null and 4-byte aligned");
+    attn::PreludeProblem p{qkv, q_norm_w, k_norm_w, cos, sin, q_out, k_out, v_out, tokens, q_heads, kv_heads,
+                           head_dim, pos_offset, qk_mode, cache_len, cache_capacity, eps, dtype == ATTN_F16};
+    cudaError_t e = attn::launch_prelude(p, static_cast<cudaStream_t>(cuda_stream));
+    if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "prelude launch: %s", cudaGetErrorString(e));
+    return ATTN_OK;
+}
+
 const char* attn_last_error(void) { return t_last_error.c_str(); }
 
 attn_status attn_sync_status(void* cuda_stream) {

@@ -79,6 +79,24 @@ struct CachesProblem {
 };
 cudaError_t launch_decode_caches(const CachesProblem& p, const WaitCtl& wc, cudaStream_t stream, int num_sms);
 
+// K4: the attention prelude (split fused QKV, per-head RMS norm, RoPE, head-major
+// transpose, optionally into KV caches), bf16 or fp16, head_dim 64 or 128.
+struct PreludeProblem {
+    const void* qkv;
+    const float* q_norm_w;
+    const float* k_norm_w;
+    const float* cos;
+    const float* sin;
+    void* q_out;
+    void* k_out;
+    void* v_out;
+    int tokens, q_heads, kv_heads, head_dim, pos_offset, qk_mode;
+    int cache_len, cache_capacity;
+    float eps;
+    bool f16;
+};
+cudaError_t launch_prelude(const PreludeProblem& p, cudaStream_t stream);
+
 // K3: fp32 SIMT attention, any head_dim in [1, 256].
 cudaError_t launch_simt_f32(const Problem& p, const WaitCtl& wc, cudaStream_t stream);
 

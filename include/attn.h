@@ -176,6 +176,61 @@ ATTN_API attn_status attn_fwd_varlen(const void* q, const void* k, const void* v
                                      int q_heads, int kv_heads, int head_dim, int mask_mode, int window,
                                      float scale, int dtype, void* cuda_stream);
 
+/* qk_mode of attn_qkv_prelude (ferrum-kernels Backend::split_qkv_norm_rope). */
+typedef enum {
+    ATTN_QK_COPY = 0,              /* Q and K are only split and transposed, like V */
+    ATTN_QK_NORM_ROPE = 1,         /* per-head RMS norm, then half-split RoPE (QK-norm models) */
+    ATTN_QK_ROPE = 2,              /* half-split RoPE only: element j pairs with j + head_dim/2 */
+    ATTN_QK_ROPE_INTERLEAVED = 3   /* interleaved RoPE only: element 2j pairs with 2j + 1 */
+} attn_qk_mode;
+
+/*
+ * attn_qkv_prelude -- the step before attention, in one pass: split the fused QKV
+ * projection, apply the per-head RMS norm and RoPE to Q and K, and write Q, K and V
+ * head-major, K and V optionally straight into KV caches.
+ *
+ * Source: ferrum-kernels Backend::split_qkv_norm_rope (fused split-QKV + QK-norm + RoPE +
+ * head-major transpose) and Backend::split_qkv_norm_rope_into_cache (the same, writing K
+ * and V into pre-allocated head-major caches at rows cache_len .. cache_len + tokens - 1,
+ * in place of kv_cache_append_head_major); Backend::qk_norm_rope for the per-head RMS norm
+ * and the positions pos_offset + i.
+ *
+ * Layout (caller-owned device memory, contiguous):
+ *   qkv       [tokens, q_heads*head_dim + 2*kv_heads*head_dim]: Q, then K, then V per token
+ *   q_out     [q_heads, tokens, head_dim]
+ *   k_out, v_out
+ *             cache_capacity == 0: [kv_heads, tokens, head_dim];
+ *             cache_capacity  > 0: caches [kv_heads, cache_capacity, head_dim], rows
+ *             cache_len .. cache_len + tokens - 1 written, every other row untouched.
+ *   cos, sin  fp32 [rope_positions, head_dim/2]: row p holds cos and sin of the angles of
+ *             position p, column j the angle of rotation pair j.  Read for qk_mode != 0.
+ *   q_norm_w, k_norm_w
+ *             fp32 [head_dim]: RMS-norm weights shared by every head.  Read for qk_mode 1.
+ *
+ * Per token t (position p = pos_offset + t) and head of Q or K:
+ *   qk_mode 1: x <- x / sqrt(mean(x^2) + eps) * w, then half-split rotation;
+ *   qk_mode 2: half-split rotation; qk_mode 3: interleaved rotation; qk_mode 0: none.
+ * A rotation pair (a, b) with angle index j becomes (a cos[p][j] - b sin[p][j],
+ * b cos[p][j] + a sin[p][j]).  V is always copied.  Arithmetic is fp32; results are
+ * rounded to the input type.
+ *
+ * Arguments: dtype is ATTN_BF16 or ATTN_F16 (for qkv and every output).  head_dim 64 or
+ * 128; otherwise ATTN_ERR_UNSUPPORTED.  tokens 0 launches nothing.
+ *
+ * Errors (checked before the launch, ATTN_ERR_INVALID_ARG): negative sizes or offsets,
+ * qk_mode outside 0..3, pos_offset + tokens > rope_positions when a rotation is applied,
+ * cache_len + tokens > cache_capacity, eps negative or not finite (qk_mode 1), null or
+ * misaligned pointers (16 bytes for qkv, the outputs, cos and sin; 4 bytes for the norm
+ * weights).  The outputs must not overlap qkv.
+ *
+ * The library allocates nothing and keeps no pointer after the call.
+ */
+ATTN_API attn_status attn_qkv_prelude(const void* qkv, const float* q_norm_w, const float* k_norm_w,
+                                      const float* cos, const float* sin, int rope_positions, void* q_out,
+                                      void* k_out, void* v_out, int tokens, int q_heads, int kv_heads,
+                                      int head_dim, int pos_offset, float eps, int qk_mode, int cache_len,
+                                      int cache_capacity, int dtype, void* cuda_stream);
+
 /*
  * attn_decode_caches -- one decode step for m items, each against its own KV cache, in
  * one launch.

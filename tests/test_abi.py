@@ -178,3 +178,37 @@ def test_varlen_arguments(lib, change, status):
     assert _varlen_call(lib, **change) == status
     if status != attn.ATTN_OK:
         assert attn.last_error() != ""
+
+
+def _prelude_call(lib, **kw):
+    a = dict(qkv=16, qw=16, kw=16, cos=16, sin=16, npos=64, q=16, k=16, v=16, tokens=8, hq=4, hkv=2, d=128, pos=0,
+             eps=1e-6, mode=1, clen=0, cap=0, dtype=attn.ATTN_BF16, stream=None)
+    a.update(kw)
+    return lib.attn_qkv_prelude(a["qkv"], a["qw"], a["kw"], a["cos"], a["sin"], a["npos"], a["q"], a["k"], a["v"],
+                                a["tokens"], a["hq"], a["hkv"], a["d"], a["pos"], ctypes.c_float(a["eps"]), a["mode"],
+                                a["clen"], a["cap"], a["dtype"], a["stream"])
+
+
+@pytest.mark.parametrize("change,status", [
+    (dict(tokens=-1), attn.ATTN_ERR_INVALID_ARG),
+    (dict(hq=0), attn.ATTN_ERR_INVALID_ARG),
+    (dict(mode=4), attn.ATTN_ERR_INVALID_ARG),
+    (dict(dtype=7), attn.ATTN_ERR_INVALID_ARG),
+    (dict(dtype=attn.ATTN_F32), attn.ATTN_ERR_UNSUPPORTED),
+    (dict(d=96), attn.ATTN_ERR_UNSUPPORTED),
+    (dict(eps=-1.0), attn.ATTN_ERR_INVALID_ARG),
+    (dict(eps=float("nan")), attn.ATTN_ERR_INVALID_ARG),
+    (dict(pos=60), attn.ATTN_ERR_INVALID_ARG),          # positions past the rope tables
+    (dict(cap=10, clen=5), attn.ATTN_ERR_INVALID_ARG),  # cache slot past the capacity
+    (dict(cos=None), attn.ATTN_ERR_INVALID_ARG),
+    (dict(sin=24), attn.ATTN_ERR_INVALID_ARG),
+    (dict(qw=None), attn.ATTN_ERR_INVALID_ARG),
+    (dict(qkv=8), attn.ATTN_ERR_INVALID_ARG),
+    (dict(v=None), attn.ATTN_ERR_INVALID_ARG),
+    (dict(tokens=0), attn.ATTN_OK),
+    (dict(mode=0, cos=None, sin=None, qw=None, kw=None, npos=0, tokens=0), attn.ATTN_OK),
+])
+def test_prelude_arguments(lib, change, status):
+    assert _prelude_call(lib, **change) == status
+    if status != attn.ATTN_OK:
+        assert attn.last_error() != ""
