@@ -108,8 +108,11 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, const 
     }
 }
 
+// Two CTAs per SM, except with 8 query heads per kv head: their accumulators need more
+// registers than two CTAs leave (the two-CTA build spills about 600 bytes per thread), and
+// one CTA per SM without spills measured twice as fast.
 template <int D, int G, bool F16>
-__global__ void __launch_bounds__(kThreads, 2) decode_splitkv_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(kThreads, (G == 8) ? 1 : 2) decode_splitkv_kernel(const DecodeParams p) {
     using C = DCfg<D, G>;
     constexpr int LPK = C::LPK, KPP = C::KPP, NP = C::NP, KB = C::KB, NV = C::NV;
     static_assert(KB * kWarps == kChunk, "a chunk is split evenly over the compute warps");
