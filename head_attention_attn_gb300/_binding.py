@@ -17,7 +17,7 @@ MASK_NONE, MASK_CAUSAL, MASK_WINDOW, MASK_CAUSAL_WINDOW = 0, 1, 2, 3
 QK_COPY, QK_NORM_ROPE, QK_ROPE, QK_ROPE_INTERLEAVED = 0, 1, 2, 3
 ATTN_BF16, ATTN_F32, ATTN_F16 = 0, 1, 2
 
-EXPORTED = ("attn_fwd", "attn_fwd_varlen", "attn_decode_caches", "attn_qkv_prelude", "attn_last_error", "attn_sync_status", "attn_selftest_timeout",
+EXPORTED = ("attn_fwd", "attn_fwd_varlen", "attn_decode_caches", "attn_qkv_prelude", "attn_qkv_prelude_caches", "attn_last_error", "attn_sync_status", "attn_selftest_timeout",
             "attn_version")
 
 _STATUS_NAMES = {0: "ATTN_OK", 1: "ATTN_ERR_INVALID_ARG", 2: "ATTN_ERR_UNSUPPORTED", 3: "ATTN_ERR_CUDA",
@@ -58,6 +58,9 @@ def load(path: str | None = None):
         lib.attn_qkv_prelude.restype = ci
         lib.attn_qkv_prelude.argtypes = [vp, vp, vp, vp, vp, ci, vp, vp, vp, ci, ci, ci, ci, ci, ctypes.c_float, ci,
                                          ci, ci, ci, vp]
+        lib.attn_qkv_prelude_caches.restype = ci
+        lib.attn_qkv_prelude_caches.argtypes = [vp, vp, vp, vp, vp, ci, vp, vp, vp, vp, ci, ci, ci, ci, ci,
+                                                ctypes.c_float, ci, ci, vp]
         lib.attn_decode_caches.restype = ci
         lib.attn_decode_caches.argtypes = [vp, vp, vp, vp, ci, ci, ci, ci, ci, vp, ci, ctypes.c_float, ci, vp]
         lib.attn_last_error.restype = ctypes.c_char_p
@@ -251,6 +254,61 @@ def attn_qkv_prelude(qkv, q_heads: int, kv_heads: int, head_dim: int, *, qk_mode
                                      capacity, dtype, _stream_handle(stream))
     _check(status)
     return q_out, k_out, v_out
+
+
+def attn_qkv_prelude_caches(qkv, k_caches, v_caches, cache_lens, q_heads: int, kv_heads: int, head_dim: int, *,
+                            qk_mode: int = QK_ROPE, cos=None, sin=None, q_norm_w=None, k_norm_w=None,
+                            eps: float = 1e-6, q_out=None, capacity: int | None = None, stream=None):
+    """Decode-step prelude for m items (see attn_qkv_prelude_caches in attn.h).
+
+    qkv [m, (q_heads + 2*kv_heads) * head_dim] bf16 or fp16; k_caches, v_caches: sequences
+    of m [kv_heads, capacity, head_dim] CUDA tensors of qkv's dtype (or int64 CUDA address
+    arrays with `capacity` given); cache_lens int32 CUDA [m].  Returns q [m, q_heads, hd].
+    """
+    import torch
+    if not qkv.is_cuda or qkv.dim() != 2 or not qkv.is_contiguous() or qkv.dtype not in (torch.bfloat16, torch.float16):
+        raise ValueError("qkv must be a contiguous bf16 or fp16 CUDA tensor [m, features]")
+    dtype = ATTN_BF16 if qkv.dtype == torch.bfloat16 else ATTN_F16
+    m = qkv.shape[0]
+    if qkv.shape[1] != (q_heads + 2 * kv_heads) * head_dim:
+        raise ValueError("qkv must have (q_heads + 2*kv_heads) * head_dim features")
+
+    def ptrs(caches):
+        if isinstance(caches, torch.Tensor) and caches.dtype == torch.int64:
+            if capacity is None or caches.numel() != m or not caches.is_cuda:
+                raise ValueError("address arrays need m entries on the device and an explicit capacity")
+            return caches.contiguous(), int(capacity)
+        caches = list(caches)
+        if len(caches) != m:
+            raise ValueError("one cache per item is required")
+        shape = tuple(caches[0].shape)
+        for t in caches:
+            if (not t.is_cuda or t.dtype != qkv.dtype or not t.is_contiguous() or tuple(t.shape) != shape
+                    or len(shape) != 3 or shape[0] != kv_heads or shape[2] != head_dim):
+                raise ValueError("caches must be contiguous [kv_heads, capacity, head_dim] tensors of qkv's dtype")
+        return torch.tensor([t.data_ptr() for t in caches], dtype=torch.int64, device=qkv.device), shape[1]
+
+    kp, kcap = ptrs(k_caches)
+    vp_, vcap = ptrs(v_caches)
+    if kcap != vcap:
+        raise ValueError("k and v caches must have one capacity")
+    if cache_lens.dtype != torch.int32 or not cache_lens.is_cuda or cache_lens.numel() != m:
+        raise ValueError("cache_lens must be an int32 CUDA tensor with m entries")
+    positions = 0
+    if cos is not None:
+        if sin is None or cos.shape != sin.shape or cos.dim() != 2 or cos.shape[1] != head_dim // 2:
+            raise ValueError("cos and sin must be [positions, head_dim/2]")
+        positions = cos.shape[0]
+    if q_out is None:
+        q_out = torch.empty((m, q_heads, head_dim), dtype=qkv.dtype, device=qkv.device)
+    ptr = (lambda t: None if t is None else t.data_ptr())
+    status = load().attn_qkv_prelude_caches(qkv.data_ptr(), ptr(q_norm_w), ptr(k_norm_w), ptr(cos), ptr(sin),
+                                            positions, q_out.data_ptr(), kp.data_ptr(), vp_.data_ptr(),
+                                            cache_lens.data_ptr(), m, q_heads, kv_heads, head_dim, kcap,
+                                            ctypes.c_float(eps), int(qk_mode), dtype, _stream_handle(stream))
+    _check(status)
+    q_out._attn_keepalive = (kp, vp_)
+    return q_out
 
 
 def attn_decode_caches(q, k_caches, v_caches, kv_lens, out=None, *, sliding_window: int = 0,

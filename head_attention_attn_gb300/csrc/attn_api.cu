@@ -258,9 +258,57 @@ attn_status attn_qkv_prelude(const void* qkv, const float* q_norm_w, const float
         return fail(ATTN_ERR_INVALID_ARG, "cos and sin must be non-null and 16-byte aligned");
     if (qk_mode == 1 && (!q_norm_w || !k_norm_w || !aligned(q_norm_w, 4) || !aligned(k_norm_w, 4)))
         return fail(ATTN_ERR_INVALID_ARG, "q_norm_w and k_norm_w must be non-null and 4-byte aligned");
+    DeviceState* st = nullptr;
+    attn_status s = device_state(&st);
+    if (s != ATTN_OK) return s;
+    attn::WaitCtl wc{st->status, kWaitLimitNs};
     attn::PreludeProblem p{qkv, q_norm_w, k_norm_w, cos, sin, q_out, k_out, v_out, tokens, q_heads, kv_heads,
-                           head_dim, pos_offset, qk_mode, cache_len, cache_capacity, eps, dtype == ATTN_F16};
-    cudaError_t e = attn::launch_prelude(p, static_cast<cudaStream_t>(cuda_stream));
+                           head_dim, pos_offset, qk_mode, cache_len, cache_capacity, eps, dtype == ATTN_F16,
+                           rope_positions, nullptr, nullptr, nullptr};
+    cudaError_t e = attn::launch_prelude(p, wc, static_cast<cudaStream_t>(cuda_stream));
+    if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "prelude launch: %s", cudaGetErrorString(e));
+    return ATTN_OK;
+}
+
+attn_status attn_qkv_prelude_caches(const void* qkv, const float* q_norm_w, const float* k_norm_w, const float* cos,
+                                    const float* sin, int rope_positions, void* q_out, const void* const* k_caches,
+                                    const void* const* v_caches, const int32_t* cache_lens, int m, int q_heads,
+                                    int kv_heads, int head_dim, int capacity, float eps, int qk_mode, int dtype,
+                                    void* cuda_stream) {
+    t_last_error.clear();
+    if (m < 0 || capacity < 0 || rope_positions < 0)
+        return fail(ATTN_ERR_INVALID_ARG, "negative size (m=%d, capacity=%d, rope_positions=%d)", m, capacity,
+                    rope_positions);
+    if (q_heads <= 0 || kv_heads <= 0 || head_dim <= 0)
+        return fail(ATTN_ERR_INVALID_ARG, "q_heads, kv_heads and head_dim must be positive (%d, %d, %d)", q_heads,
+                    kv_heads, head_dim);
+    if (qk_mode < 0 || qk_mode > 3) return fail(ATTN_ERR_INVALID_ARG, "qk_mode %d out of range", qk_mode);
+    if (dtype != ATTN_BF16 && dtype != ATTN_F32 && dtype != ATTN_F16)
+        return fail(ATTN_ERR_INVALID_ARG, "dtype %d out of range", dtype);
+    if (dtype == ATTN_F32) return fail(ATTN_ERR_UNSUPPORTED, "the prelude supports bf16 and fp16");
+    if (head_dim != 64 && head_dim != 128)
+        return fail(ATTN_ERR_UNSUPPORTED, "the prelude supports head_dim 64 and 128, not %d", head_dim);
+    if (qk_mode == 1 && (!isfinite(eps) || eps < 0.f))
+        return fail(ATTN_ERR_INVALID_ARG, "eps must be finite and >= 0");
+    if (m == 0) return ATTN_OK;
+    if (capacity == 0) return fail(ATTN_ERR_INVALID_ARG, "capacity must be positive to append a row");
+    if (!qkv || !q_out || !k_caches || !v_caches || !cache_lens)
+        return fail(ATTN_ERR_INVALID_ARG, "null qkv, q_out, k_caches, v_caches or cache_lens");
+    if (!aligned(qkv, 16) || !aligned(q_out, 16) || !aligned(k_caches, 8) || !aligned(v_caches, 8) ||
+        !aligned(cache_lens, 4))
+        return fail(ATTN_ERR_INVALID_ARG, "qkv/q_out must be 16-byte, pointer arrays 8-byte, cache_lens 4-byte aligned");
+    if (qk_mode != 0 && (!cos || !sin || !aligned(cos, 16) || !aligned(sin, 16)))
+        return fail(ATTN_ERR_INVALID_ARG, "cos and sin must be non-null and 16-byte aligned");
+    if (qk_mode == 1 && (!q_norm_w || !k_norm_w || !aligned(q_norm_w, 4) || !aligned(k_norm_w, 4)))
+        return fail(ATTN_ERR_INVALID_ARG, "q_norm_w and k_norm_w must be non-null and 4-byte aligned");
+    DeviceState* st = nullptr;
+    attn_status s = device_state(&st);
+    if (s != ATTN_OK) return s;
+    attn::WaitCtl wc{st->status, kWaitLimitNs};
+    attn::PreludeProblem p{qkv, q_norm_w, k_norm_w, cos, sin, q_out, nullptr, nullptr, m, q_heads, kv_heads,
+                           head_dim, 0, qk_mode, 0, capacity, eps, dtype == ATTN_F16, rope_positions,
+                           k_caches, v_caches, cache_lens};
+    cudaError_t e = attn::launch_prelude(p, wc, static_cast<cudaStream_t>(cuda_stream));
     if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "prelude launch: %s", cudaGetErrorString(e));
     return ATTN_OK;
 }
@@ -286,7 +334,8 @@ attn_status attn_sync_status(void* cuda_stream) {
             return fail(ATTN_ERR_INVALID_ARG, "a per-item cache pointer is null or not 16-byte aligned");
         if (word == attn::kStatusBadSeqlens)
             return fail(ATTN_ERR_INVALID_ARG,
-                        "cu_seqlens is not non-decreasing from >= 0 to <= total with lengths <= max_seqlen");
+                        "a device-side length is out of range: cu_seqlens not non-decreasing within total and "
+                        "max_seqlen, or a cache length outside the capacity or the rope tables");
         return fail(ATTN_ERR_CUDA, "device status word %u", word);
     }
     return ATTN_OK;

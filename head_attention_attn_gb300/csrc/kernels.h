@@ -94,8 +94,14 @@ struct PreludeProblem {
     int cache_len, cache_capacity;
     float eps;
     bool f16;
+    int rope_positions;
+    // Per-item form (null otherwise): item i = token i, position cache_lens[i], Q item-major,
+    // K/V into row cache_lens[i] of k_caches[i] / v_caches[i] ([kv_heads, capacity, hd]).
+    const void* const* k_caches;
+    const void* const* v_caches;
+    const int32_t* cache_lens;
 };
-cudaError_t launch_prelude(const PreludeProblem& p, cudaStream_t stream);
+cudaError_t launch_prelude(const PreludeProblem& p, const WaitCtl& wc, cudaStream_t stream);
 
 // K3: fp32 SIMT attention, any head_dim in [1, 256].
 cudaError_t launch_simt_f32(const Problem& p, const WaitCtl& wc, cudaStream_t stream);

@@ -14,9 +14,17 @@
 // Backend::split_qkv_norm_rope_into_cache (which folds kv_cache_append_head_major
 // into the same pass), with Backend::qk_norm_rope's per-head RMS norm and positions.
 //
-// Layout of the work: a row is one (token, head slot) of hd values, head slots ordered
-// Q heads, K heads, V heads as in qkv.  hd/16 threads share a row, 16 values each, all
-// loads and stores 16 bytes wide:
+// Per-item form (decode): token i is item i, its position is cache_lens[i] (device), Q is
+// written item-major [items, q_heads, hd] and K, V go to row cache_lens[i] of item i's own
+// caches k_caches[i], v_caches[i] ([kv_heads, capacity, hd]), as ferrum-kernels
+// qk_norm_rope_batched_per_item (per-item positions, item-major) and
+// kv_cache_append_batched_per_cache (one row per item at its cache length) describe.
+//
+// Layout of the work: a group of hd/16 threads handles 4 consecutive head slots of one
+// token (slots ordered Q heads, K heads, V heads as in qkv), 16 values of each row per
+// thread, all loads and stores 16 bytes wide.  A thread issues the loads of its 4 rows
+// before any arithmetic and loads the token's rotation angles and the norm weights once
+// for the 4 rows:
 //   half-split (and copy): thread c holds values [8c, 8c+8) and [hd/2+8c, hd/2+8c+8),
 //   interleaved:           thread c holds values [16c, 16c+16);
 // either way its rotation pairs use angle indices [8c, 8c+8).  Arithmetic is fp32; the
@@ -35,22 +43,14 @@ struct PreludeParams {
     uint16_t* q_out;
     uint16_t* k_out;
     uint16_t* v_out;
-    int tokens, q_heads, kv_heads, pos_offset, qk_mode;
-    int cache_len, cache_capacity;  // capacity 0: k_out/v_out are [kv_heads, tokens, hd]
+    const void* const* k_caches;  // per-item form: device arrays of `tokens` cache pointers
+    const void* const* v_caches;
+    const int32_t* cache_lens;    // per-item form: position and cache row of item i
+    int tokens, q_heads, kv_heads, pos_offset, qk_mode, rope_positions;
+    int cache_len, cache_capacity;  // capacity 0 (contiguous form): k_out/v_out are [kv_heads, tokens, hd]
     float eps;
-    long long rows;                 // tokens * (q_heads + 2 * kv_heads)
+    WaitCtl wc;                     // only its status word is used
 };
-
-__device__ __forceinline__ void load8(const uint16_t* p, float (&f)[8], bool f16) {
-    const uint4 u = *reinterpret_cast<const uint4*>(p);
-    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const float2 t = f16 ? unpack2<true>(w[i]) : unpack2<false>(w[i]);
-        f[2 * i] = t.x;
-        f[2 * i + 1] = t.y;
-    }
-}
 
 __device__ __forceinline__ void store8(uint16_t* p, const float (&f)[8], bool f16) {
     uint32_t w[4];
@@ -59,105 +59,154 @@ __device__ __forceinline__ void store8(uint16_t* p, const float (&f)[8], bool f1
     *reinterpret_cast<uint4*>(p) = make_uint4(w[0], w[1], w[2], w[3]);
 }
 
+__device__ __forceinline__ void load8f(const float* p, float* f) {
+    const float4 a = __ldg(reinterpret_cast<const float4*>(p)), b = __ldg(reinterpret_cast<const float4*>(p) + 1);
+    f[0] = a.x, f[1] = a.y, f[2] = a.z, f[3] = a.w, f[4] = b.x, f[5] = b.y, f[6] = b.z, f[7] = b.w;
+}
+
+constexpr int kRowsPerGroup = 4;  // head rows of one token handled by one thread group
+
 template <int HD, bool F16>
-__global__ void __launch_bounds__(256) prelude_kernel(const PreludeParams p) {
-    constexpr int TPR = HD / 16;  // threads per row
-    const long long gid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-    const long long row = gid / TPR;
-    const int c = (int)(gid % TPR);
-    const bool live = row < p.rows;
+__global__ void __launch_bounds__(256) prelude_kernel(const __grid_constant__ PreludeParams p) {
+    constexpr int TPR = HD / 16;  // threads per group (and per head row)
+    constexpr int R = kRowsPerGroup;
     const int slots = p.q_heads + 2 * p.kv_heads;
-    const int t = live ? (int)(row / slots) : 0;
-    const int hs = live ? (int)(row % slots) : 0;
-    const bool is_q = hs < p.q_heads;
-    const bool is_k = !is_q && hs < p.q_heads + p.kv_heads;
-    const bool rotate = (is_q || is_k) && p.qk_mode != 0;
+    const int groups_per_token = (slots + R - 1) / R;
+    const long long gid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    const long long group = gid / TPR;
+    const int c = (int)(gid % TPR);
+    bool valid = group < (long long)p.tokens * groups_per_token;
+    const int t = valid ? (int)(group / groups_per_token) : 0;        // token (item)
+    const int hs0 = valid ? (int)(group % groups_per_token) * R : 0;  // first head slot of the group
+    const bool items = p.cache_lens != nullptr;
     const bool interleaved = p.qk_mode == 3;
-    // element offsets of my two 8-value pieces inside the row
     const int o0 = interleaved ? 16 * c : 8 * c;
     const int o1 = interleaved ? 16 * c + 8 : HD / 2 + 8 * c;
 
-    float a[8], b[8];  // a: first piece, b: second piece
-    if (live) {
-        const uint16_t* src = p.qkv + ((long long)t * slots + hs) * HD;
-        load8(src + o0, a, F16);
-        load8(src + o1, b, F16);
-    } else {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) a[i] = b[i] = 0.f;
-    }
-
-    // per-head RMS norm (qk_mode 1, Q and K): every lane of the row group takes part in the
-    // reduction, whatever its row needs, so the shuffles never run with a partial group
-    float ss = 0.f;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) ss = fmaf(a[i], a[i], fmaf(b[i], b[i], ss));
-#pragma unroll
-    for (int m = 1; m < TPR; m <<= 1) ss += __shfl_xor_sync(0xffffffffu, ss, m, TPR);
-    if (live && rotate && p.qk_mode == 1) {
-        const float r = rsqrtf(ss * (1.f / HD) + p.eps);
-        const float* w = is_q ? p.q_norm_w : p.k_norm_w;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            a[i] = a[i] * r * __ldg(w + o0 + i);
-            b[i] = b[i] * r * __ldg(w + o1 + i);
-        }
-    }
-
-    if (live && rotate) {
-        const long long pos = (long long)p.pos_offset + t;
-        const float4* cp = reinterpret_cast<const float4*>(p.cos + pos * (HD / 2) + 8 * c);
-        const float4* sp = reinterpret_cast<const float4*>(p.sin + pos * (HD / 2) + 8 * c);
-        const float4 c0 = __ldg(cp), c1 = __ldg(cp + 1), s0 = __ldg(sp), s1 = __ldg(sp + 1);
-        const float cs[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-        const float sn[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
-        if (interleaved) {
-            // pairs (a[0], a[1]), ..., (b[6], b[7]): angle indices 8c .. 8c+7
-            float x[16];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                x[i] = a[i];
-                x[8 + i] = b[i];
-            }
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const float u = x[2 * j], v = x[2 * j + 1];
-                x[2 * j] = u * cs[j] - v * sn[j];
-                x[2 * j + 1] = v * cs[j] + u * sn[j];
-            }
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                a[i] = x[i];
-                b[i] = x[8 + i];
-            }
+    long long pos = (long long)p.pos_offset + t;
+    uint16_t* kdst = p.k_out;
+    uint16_t* vdst = p.v_out;
+    long long kv_row = t, head_stride = p.tokens;  // contiguous form: [kv_heads, tokens, hd]
+    if (valid && items) {
+        const int len = __ldg(p.cache_lens + t);
+        const uintptr_t kp = reinterpret_cast<uintptr_t>(p.k_caches[t]);
+        const uintptr_t vp = reinterpret_cast<uintptr_t>(p.v_caches[t]);
+        const bool bad_len = len < 0 || len >= p.cache_capacity || (p.qk_mode != 0 && len >= p.rope_positions);
+        const bool bad_ptr = kp == 0 || vp == 0 || (kp & 15u) != 0 || (vp & 15u) != 0;
+        if (bad_len || bad_ptr) {
+            // this item is neither read nor written; the lanes stay for the shuffles below
+            if (c == 0 && hs0 == 0) record_status(p.wc.status, bad_len ? kStatusBadSeqlens : kStatusBadPointer);
+            valid = false;
         } else {
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const float u = a[j], v = b[j];
-                a[j] = u * cs[j] - v * sn[j];
-                b[j] = v * cs[j] + u * sn[j];
-            }
+            pos = len;
+            kdst = reinterpret_cast<uint16_t*>(kp);
+            vdst = reinterpret_cast<uint16_t*>(vp);
+            kv_row = len;
+            head_stride = p.cache_capacity;
         }
+    } else if (p.cache_capacity > 0) {
+        kv_row = (long long)p.cache_len + t;
+        head_stride = p.cache_capacity;
     }
 
-    if (!live) return;
-    uint16_t* dst;
-    if (is_q) {
-        dst = p.q_out + ((long long)hs * p.tokens + t) * HD;
-    } else {
-        const int h = is_k ? hs - p.q_heads : hs - p.q_heads - p.kv_heads;
-        uint16_t* base = is_k ? p.k_out : p.v_out;
-        dst = p.cache_capacity > 0 ? base + ((long long)h * p.cache_capacity + p.cache_len + t) * HD
-                                   : base + ((long long)h * p.tokens + t) * HD;
+    // the group's rows: every load first, so R rows are in flight per thread
+    uint4 raw[R][2];
+    const uint16_t* src = p.qkv + ((long long)t * slots + hs0) * HD;
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        if (valid && hs0 + r < slots) {
+            raw[r][0] = *reinterpret_cast<const uint4*>(src + r * HD + o0);
+            raw[r][1] = *reinterpret_cast<const uint4*>(src + r * HD + o1);
+        } else {
+            raw[r][0] = raw[r][1] = make_uint4(0u, 0u, 0u, 0u);
+        }
     }
-    store8(dst + o0, a, F16);
-    store8(dst + o1, b, F16);
+    // the token's rotation angles and the norm weights of my 16 value indices, once per group
+    float cs[8], sn[8];
+    if (valid && p.qk_mode != 0) {
+        load8f(p.cos + pos * (HD / 2) + 8 * c, cs);
+        load8f(p.sin + pos * (HD / 2) + 8 * c, sn);
+    }
+    float wq[16], wk[16];
+    if (valid && p.qk_mode == 1) {
+        load8f(p.q_norm_w + o0, wq);
+        load8f(p.q_norm_w + o1, wq + 8);
+        load8f(p.k_norm_w + o0, wk);
+        load8f(p.k_norm_w + o1, wk + 8);
+    }
+
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        const int hs = hs0 + r;
+        const bool live = valid && hs < slots;
+        const bool is_q = hs < p.q_heads;
+        const bool is_k = !is_q && hs < p.q_heads + p.kv_heads;
+        const bool rotate = live && (is_q || is_k) && p.qk_mode != 0;
+        float a[8], b[8];
+        {
+            const uint32_t wa[4] = {raw[r][0].x, raw[r][0].y, raw[r][0].z, raw[r][0].w};
+            const uint32_t wb[4] = {raw[r][1].x, raw[r][1].y, raw[r][1].z, raw[r][1].w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float2 x = unpack2<F16>(wa[i]), y = unpack2<F16>(wb[i]);
+                a[2 * i] = x.x, a[2 * i + 1] = x.y, b[2 * i] = y.x, b[2 * i + 1] = y.y;
+            }
+        }
+        // per-head RMS norm (qk_mode 1): every lane takes part in the reduction, whatever
+        // its row needs, so the shuffles never run with a partial warp
+        float ss = 0.f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) ss = fmaf(a[i], a[i], fmaf(b[i], b[i], ss));
+#pragma unroll
+        for (int m = 1; m < TPR; m <<= 1) ss += __shfl_xor_sync(0xffffffffu, ss, m, TPR);
+        if (rotate && p.qk_mode == 1) {
+            const float rs = rsqrtf(ss * (1.f / HD) + p.eps);
+            const float* w = is_q ? wq : wk;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                a[i] = a[i] * rs * w[i];
+                b[i] = b[i] * rs * w[8 + i];
+            }
+        }
+        if (rotate) {
+            if (interleaved) {
+                // pairs (a[0], a[1]), ..., (b[6], b[7]): angle indices 8c .. 8c+7
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const float u = a[2 * j], v = a[2 * j + 1];
+                    a[2 * j] = u * cs[j] - v * sn[j];
+                    a[2 * j + 1] = v * cs[j] + u * sn[j];
+                    const float u2 = b[2 * j], v2 = b[2 * j + 1];
+                    b[2 * j] = u2 * cs[4 + j] - v2 * sn[4 + j];
+                    b[2 * j + 1] = v2 * cs[4 + j] + u2 * sn[4 + j];
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const float u = a[j], v = b[j];
+                    a[j] = u * cs[j] - v * sn[j];
+                    b[j] = v * cs[j] + u * sn[j];
+                }
+            }
+        }
+        if (!live) continue;
+        uint16_t* dst;
+        if (is_q) {
+            dst = items ? p.q_out + ((long long)t * p.q_heads + hs) * HD : p.q_out + ((long long)hs * p.tokens + t) * HD;
+        } else {
+            const int h = is_k ? hs - p.q_heads : hs - p.q_heads - p.kv_heads;
+            dst = (is_k ? kdst : vdst) + ((long long)h * head_stride + kv_row) * HD;
+        }
+        store8(dst + o0, a, F16);
+        store8(dst + o1, b, F16);
+    }
 }
 
 template <int HD, bool F16>
 cudaError_t launch_t(const PreludeParams& p, cudaStream_t stream) {
-    const long long threads = p.rows * (HD / 16);
-    const long long blocks = (threads + 255) / 256;
+    const int slots = p.q_heads + 2 * p.kv_heads;
+    const long long groups = (long long)p.tokens * ((slots + kRowsPerGroup - 1) / kRowsPerGroup);
+    const long long blocks = (groups * (HD / 16) + 255) / 256;
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     prelude_kernel<HD, F16><<<(unsigned)blocks, 256, 0, stream>>>(p);
     return cudaGetLastError();
@@ -165,7 +214,7 @@ cudaError_t launch_t(const PreludeParams& p, cudaStream_t stream) {
 
 }  // namespace
 
-cudaError_t launch_prelude(const PreludeProblem& pr, cudaStream_t stream) {
+cudaError_t launch_prelude(const PreludeProblem& pr, const WaitCtl& wc, cudaStream_t stream) {
     PreludeParams p;
     p.qkv = static_cast<const uint16_t*>(pr.qkv);
     p.q_norm_w = pr.q_norm_w;
@@ -175,15 +224,19 @@ cudaError_t launch_prelude(const PreludeProblem& pr, cudaStream_t stream) {
     p.q_out = static_cast<uint16_t*>(pr.q_out);
     p.k_out = static_cast<uint16_t*>(pr.k_out);
     p.v_out = static_cast<uint16_t*>(pr.v_out);
+    p.k_caches = pr.k_caches;
+    p.v_caches = pr.v_caches;
+    p.cache_lens = pr.cache_lens;
     p.tokens = pr.tokens;
     p.q_heads = pr.q_heads;
     p.kv_heads = pr.kv_heads;
     p.pos_offset = pr.pos_offset;
     p.qk_mode = pr.qk_mode;
+    p.rope_positions = pr.rope_positions;
     p.cache_len = pr.cache_len;
     p.cache_capacity = pr.cache_capacity;
     p.eps = pr.eps;
-    p.rows = (long long)pr.tokens * (pr.q_heads + 2 * pr.kv_heads);
+    p.wc = wc;
     if (pr.head_dim == 64) return pr.f16 ? launch_t<64, true>(p, stream) : launch_t<64, false>(p, stream);
     if (pr.head_dim == 128) return pr.f16 ? launch_t<128, true>(p, stream) : launch_t<128, false>(p, stream);
     return cudaErrorInvalidValue;

@@ -232,6 +232,38 @@ ATTN_API attn_status attn_qkv_prelude(const void* qkv, const float* q_norm_w, co
                                       int cache_capacity, int dtype, void* cuda_stream);
 
 /*
+ * attn_qkv_prelude_caches -- the decode-step prelude for m items with per-item KV caches,
+ * in one launch: item i's single token is row i of qkv, its position is cache_lens[i], its
+ * Q goes to q_out item-major and its K and V are appended at row cache_lens[i] of its own
+ * caches.  The output feeds attn_decode_caches (with kv_lens[i] = cache_lens[i] + 1).
+ *
+ * Source: ferrum-kernels Backend::split_qkv_norm_rope_into_cache (split, QK norm, RoPE,
+ * K/V straight into the cache), Backend::qk_norm_rope_batched_per_item (per-item
+ * positions from a device buffer, item-major Q) and
+ * Backend::kv_cache_append_batched_per_cache (each item writes its row into its own cache
+ * at the offset read from cache_lens[i]).
+ *
+ * Layout: qkv [m, q_heads*head_dim + 2*kv_heads*head_dim]; q_out [m, q_heads, head_dim];
+ * k_caches, v_caches device arrays of m device pointers to [kv_heads, capacity, head_dim]
+ * caches (16-byte aligned); cache_lens device int32 [m].  cos, sin, q_norm_w, k_norm_w,
+ * qk_mode, eps and dtype as for attn_qkv_prelude.
+ *
+ * Errors: host-visible arguments as for attn_qkv_prelude (capacity must be positive).
+ * Items are checked on the device: an item whose cache_lens[i] is outside [0, capacity),
+ * or (with a rotation) at or past rope_positions, or whose cache pointer is null or
+ * misaligned, is neither read nor written, and attn_sync_status() reports
+ * ATTN_ERR_INVALID_ARG.
+ *
+ * The library allocates nothing and keeps no pointer after the call.
+ */
+ATTN_API attn_status attn_qkv_prelude_caches(const void* qkv, const float* q_norm_w, const float* k_norm_w,
+                                             const float* cos, const float* sin, int rope_positions, void* q_out,
+                                             const void* const* k_caches, const void* const* v_caches,
+                                             const int32_t* cache_lens, int m, int q_heads, int kv_heads,
+                                             int head_dim, int capacity, float eps, int qk_mode, int dtype,
+                                             void* cuda_stream);
+
+/*
  * attn_decode_caches -- one decode step for m items, each against its own KV cache, in
  * one launch.
  *

@@ -212,3 +212,29 @@ def test_prelude_arguments(lib, change, status):
     assert _prelude_call(lib, **change) == status
     if status != attn.ATTN_OK:
         assert attn.last_error() != ""
+
+
+def _prelude_caches_call(lib, **kw):
+    a = dict(qkv=16, qw=16, kw=16, cos=16, sin=16, npos=64, q=16, kc=16, vc=16, lens=16, m=4, hq=4, hkv=2, d=128,
+             cap=32, eps=1e-6, mode=1, dtype=attn.ATTN_BF16, stream=None)
+    a.update(kw)
+    return lib.attn_qkv_prelude_caches(a["qkv"], a["qw"], a["kw"], a["cos"], a["sin"], a["npos"], a["q"], a["kc"],
+                                       a["vc"], a["lens"], a["m"], a["hq"], a["hkv"], a["d"], a["cap"],
+                                       ctypes.c_float(a["eps"]), a["mode"], a["dtype"], a["stream"])
+
+
+@pytest.mark.parametrize("change,status", [
+    (dict(m=-1), attn.ATTN_ERR_INVALID_ARG),
+    (dict(cap=0), attn.ATTN_ERR_INVALID_ARG),
+    (dict(mode=9), attn.ATTN_ERR_INVALID_ARG),
+    (dict(dtype=attn.ATTN_F32), attn.ATTN_ERR_UNSUPPORTED),
+    (dict(d=32), attn.ATTN_ERR_UNSUPPORTED),
+    (dict(lens=None), attn.ATTN_ERR_INVALID_ARG),
+    (dict(kc=12), attn.ATTN_ERR_INVALID_ARG),
+    (dict(q=8), attn.ATTN_ERR_INVALID_ARG),
+    (dict(cos=None), attn.ATTN_ERR_INVALID_ARG),
+    (dict(kw=None), attn.ATTN_ERR_INVALID_ARG),
+    (dict(m=0), attn.ATTN_OK),
+])
+def test_prelude_caches_arguments(lib, change, status):
+    assert _prelude_caches_call(lib, **change) == status

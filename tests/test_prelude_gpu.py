@@ -114,3 +114,57 @@ def test_prelude_feeds_attention():
     torch.cuda.synchronize()
     assert attn.sync_status() == attn.ATTN_OK, attn.last_error()
     assert torch.isfinite(out.float()).all()
+
+
+@pytest.mark.parametrize("mode", [1, 3])
+def test_decode_step_prelude_then_attention(mode):
+    """One decode step for 5 items with their own caches: the per-item prelude appends each
+    item's K/V at its cache length and writes its Q, then attn_decode_caches attends over
+    the grown caches.  Both against the oracles (prelude oracle, then attention oracle)."""
+    import oracle
+    m, Hq, Hkv, hd, cap = 5, 8, 2, 128, 300
+    lens = [0, 17, 128, 250, 299]
+    g = torch.Generator().manual_seed(9400 + mode)
+    # N(0, 1) like every attention input here: the bf16 output bound (1e-2) assumes |o| <~ 5
+    qkv = torch.randn(m, (Hq + 2 * Hkv) * hd, generator=g).to(torch.bfloat16)
+    qw, kw = torch.rand(hd, generator=g) + 0.5, torch.rand(hd, generator=g) + 0.5
+    cos, sin = rope_tables(cap, hd)
+    ks = [torch.randn(Hkv, cap, hd, generator=g).to(torch.bfloat16) for _ in range(m)]
+    vs = [torch.randn(Hkv, cap, hd, generator=g).to(torch.bfloat16) for _ in range(m)]
+    kd, vd = [k.to(DEV) for k in ks], [v.to(DEV) for v in vs]
+    cl = torch.tensor(lens, dtype=torch.int32, device=DEV)
+    q = attn.attn_qkv_prelude_caches(qkv.to(DEV), kd, vd, cl, Hq, Hkv, hd, qk_mode=mode, cos=cos.to(DEV),
+                                     sin=sin.to(DEV), q_norm_w=qw.to(DEV), k_norm_w=kw.to(DEV), eps=1e-6)
+    out = attn.attn_decode_caches(q, kd, vd, cl + 1)
+    torch.cuda.synchronize()
+    assert attn.sync_status() == attn.ATTN_OK, attn.last_error()
+    for i in range(m):
+        rq, rk, rv = P.split_qkv_norm_rope(qkv[i:i + 1], qw, kw, cos, sin, q_heads=Hq, kv_heads=Hkv, head_dim=hd,
+                                           pos_offset=lens[i], eps=1e-6, qk_mode=mode)
+        assert_elementwise(q[i], rq[:, 0], torch.bfloat16, f"q item {i}")
+        assert_elementwise(kd[i][:, lens[i]], rk[:, 0], torch.bfloat16, f"k item {i}")
+        assert torch.equal(vd[i][:, lens[i]].cpu(), torch.from_numpy(rv[:, 0]).to(torch.bfloat16))
+        keep = torch.ones(cap, dtype=torch.bool)
+        keep[lens[i]] = False
+        assert torch.equal(kd[i][:, keep].cpu(), ks[i][:, keep]) and torch.equal(vd[i][:, keep].cpu(), vs[i][:, keep])
+        n = lens[i] + 1
+        ref = oracle.attention(q[i].cpu()[None, :, None, :], kd[i].cpu()[None], vd[i].cpu()[None], pos_offset=n - 1,
+                               mask_mode=attn.MASK_CAUSAL, key_lens=[n],
+                               scale=float(torch.tensor(1.0 / hd ** 0.5, dtype=torch.float32)))
+        from parity_util import assert_close
+        assert_close(out[i].double().cpu().numpy(), ref[0, :, 0, :], "bf16", f"decode item {i}")
+
+
+def test_prelude_caches_bad_items_are_reported_not_written():
+    m, Hq, Hkv, hd, cap = 3, 4, 2, 64, 16
+    g = torch.Generator().manual_seed(9500)
+    qkv = torch.randn(m, (Hq + 2 * Hkv) * hd, generator=g).to(torch.bfloat16).to(DEV)
+    kd = [torch.zeros(Hkv, cap, hd, dtype=torch.bfloat16, device=DEV) for _ in range(m)]
+    vd = [torch.zeros(Hkv, cap, hd, dtype=torch.bfloat16, device=DEV) for _ in range(m)]
+    cl = torch.tensor([3, cap, -1], dtype=torch.int32, device=DEV)  # items 1 and 2 are out of range
+    q = torch.full((m, Hq, hd), 9.0, dtype=torch.bfloat16, device=DEV)
+    attn.attn_qkv_prelude_caches(qkv, kd, vd, cl, Hq, Hkv, hd, qk_mode=attn.QK_COPY, q_out=q)
+    assert attn.sync_status() == attn.ATTN_ERR_INVALID_ARG
+    assert attn.sync_status() == attn.ATTN_OK
+    assert torch.all(kd[1] == 0) and torch.all(kd[2] == 0) and torch.all(q[1:] == 9.0)
+    assert torch.equal(q[0], qkv[0, :Hq * hd].view(Hq, hd))  # item 0 went through (copy mode)
