@@ -380,7 +380,7 @@ def run_ours(args, rank, world, local):
               "ms_per_step": round(dsec * 1e3, 4),
               "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                            "frac": round(gbs / peaks["hbm_gbs"], 4), "peak_source": f"{peak_src} HBM copy",
-                           "traffic": None, "kernel": "decode_splitkv_kernel<128, G4, bf16>",
+                           "traffic": None, "kernel": "decode_tc_kernel<G4, bf16>",
                            "algorithmic_bytes_per_launch": dec_bytes},
               "l2": f"inputs {dec_bytes / 1e6:.0f} MB > {L2_BYTES / 1e6:.0f} MB L2, no flush"}
     del host_d, devt_d

@@ -3,7 +3,8 @@
 //
 // Kernel choice:
 //   f32                          -> K3 (SIMT fp32, any head_dim 1..256)
-//   bf16/fp16, q_len == 1, group 1/2/4/8 -> K2 (split-KV decode)
+//   bf16/fp16, q_len == 1, head_dim 128, group 4/8 -> K5 (tensor-core split-KV decode)
+//   bf16/fp16, q_len == 1, group 1/2/4/8 -> K2 (split-KV decode, the other shapes)
 //   bf16/fp16 otherwise          -> K1 (tcgen05 + TMA fused prefill)
 // There is no host fallback: an unsupported shape is refused (ferrum-kernels:
 // CUDA ops fail rather than copy data through host memory).
@@ -129,6 +130,9 @@ attn_status attn_fwd(const void* q, const void* k, const void* v, void* out, int
             return fail(ATTN_ERR_UNSUPPORTED, "f32 path limits q_heads and batch to 65535");
         which = "simt_f32";
         e = attn::launch_simt_f32(p, wc, stream);
+    } else if (attn::decode_tc_supported(p) && kv_heads <= 65535 && batch <= 65535) {
+        which = "decode_tc";
+        e = attn::launch_decode_tc(p, wc, stream, st->num_sms);
     } else if (attn::decode_supported(p) && kv_heads <= 65535 && batch <= 65535) {
         which = "decode_splitkv";
         e = attn::launch_decode_splitkv(p, wc, stream, st->num_sms);

@@ -1,0 +1,570 @@
+// decode_tc.cu -- K5: single-query (q_len == 1) attention against a KV cache on the
+// 5th-generation tensor cores, head_dim 128, 4 or 8 query heads per kv head, bf16 or fp16.
+//
+// With several query heads per kv head the per-key work of a CUDA-core decode (every head
+// against every key, then every head's probability into V) outgrows the HBM stream.  Here
+// the tensor core does both products for the whole group:
+//   S^T [128 keys x 16] = K_j Q^T        (A = the K tile, K-major; B = Q, the group's heads
+//                                         padded with zero rows to 16, K-major)
+//   O^T [128 dims x 16] += V_j^T P_j^T   (A = the V tile read MN-major; B = P^T, 16 rows of
+//                                         128 keys in shared memory, K-major)
+// with fp32 accumulators in TMEM (S^T double-buffered, 64 columns in all).
+//
+// Work unit: (batch b, kv head hk, split); the splits of one unit form a cluster and merge
+// their partial results through distributed shared memory in CTA rank 0.
+//   warp 0       TMA producer: 128-key K and V tiles through 3-stage rings.
+//   warp 1       TMEM owner and single-thread MMA issuer: QK(j) then PV(j-1).
+//   warps 2-5    one key per thread: it reads its key's 16 head scores from TMEM, the per-head
+//                block maxima come from a shuffle reduce-scatter and a 4-warp exchange,
+//                then it writes its key's probabilities (2^x on the special-function unit,
+//                scale*log2(e) folded in) into P^T; O^T is rescaled only when a head's
+//                maximum grows by more than 2^8.  In the epilogue the same threads own the
+//                128 head dims.
+//
+// The operation is the q_len = 1 case of ferrum-kernels Backend::flash_attention (the
+// GQA decode of a KV cache at pos_offset), with the masks of attn.h.
+#include "kernels.h"
+
+#include <algorithm>
+#include <mutex>
+
+namespace attn {
+namespace {
+
+constexpr int D = 128;
+constexpr int BN = 128;         // keys per block
+constexpr int NH = 16;          // MMA N: the group's query heads, padded
+constexpr int kStages = 3;
+constexpr int kThreads = 192;
+constexpr int kMaxSplits = 8;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kRescaleThreshold = 8.0f;
+
+struct L {
+    static constexpr int kKVBytes = BN * D * 2;  // one K or V tile
+    static constexpr int kQBytes = NH * D * 2;
+    static constexpr int kPBytes = NH * BN * 2;
+    static constexpr int kOffK = 0;
+    static constexpr int kOffV = kOffK + kStages * kKVBytes;
+    static constexpr int kOffQ = kOffV + kStages * kKVBytes;
+    static constexpr int kOffP = kOffQ + kQBytes;
+    static constexpr int kOffX = kOffP + kPBytes;            // [2 parities][4 warps][16] block maxima
+    static constexpr int kOffS = kOffX + 2 * 4 * NH * 4;     // [4 warps][16] row-sum parts
+    static constexpr int kOffBar = kOffS + 4 * NH * 4;
+    static constexpr int kSmem = kOffBar + 256 + 1024;        // + realignment slack
+    // after the last P V product the K ring is free; the combine reuses it
+    static constexpr int kOffCm = 0;                         // [16] log2-domain maxima
+    static constexpr int kOffCl = kOffCm + NH * 4;           // [16] row sums
+    static constexpr int kOffCo = kOffCl + NH * 4;           // [16][128] unnormalised outputs
+    static_assert(kOffQ % 1024 == 0 && kOffP % 1024 == 0, "swizzled tiles need 1024-byte alignment");
+    static_assert(kSmem <= 232448, "shared memory budget");
+};
+
+enum : int {
+    kBarKFull = 0,
+    kBarKEmpty = kBarKFull + kStages,
+    kBarVFull = kBarKEmpty + kStages,
+    kBarVEmpty = kBarVFull + kStages,
+    kBarSFull = kBarVEmpty + kStages,  // + buffer
+    kBarSFree = kBarSFull + 2,         // + buffer, 4 arrivals
+    kBarPFull = kBarSFree + 2,         // 4 arrivals
+    kBarPVDone = kBarPFull + 1,
+    kBarXch = kBarPVDone + 1,          // + parity, 4 arrivals
+    kBarSum = kBarXch + 2,             // 4 arrivals
+    kBarMmaDone = kBarSum + 1,
+    kNumBars = kBarMmaDone + 1,
+};
+static_assert(kNumBars * 8 <= 240, "barrier area");
+
+constexpr uint32_t kColS = 0;   // + 16 * buffer
+constexpr uint32_t kColO = 32;
+constexpr uint32_t kTmemCols = 64;
+
+struct DecodeTcParams {
+    const uint16_t* q;
+    uint16_t* out;
+    const int32_t* key_lens;
+    int Hq, Hkv, Lk, P, mode, window;
+    float scale_log2;
+    WaitCtl wc;
+};
+
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, const WaitCtl& wc) {
+    const unsigned long long t0 = globaltimer_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (globaltimer_ns() - t0 > wc.limit_ns) {
+            record_status(wc.status, kStatusTimeout);
+            return;
+        }
+    }
+}
+
+// Load 16 consecutive 32-bit columns of this warp's 32 TMEM lanes, then wait.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* r) {
+    uint32_t* u = reinterpret_cast<uint32_t*>(r);
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(u[0]), "=r"(u[1]), "=r"(u[2]), "=r"(u[3]), "=r"(u[4]), "=r"(u[5]), "=r"(u[6]), "=r"(u[7]),
+          "=r"(u[8]), "=r"(u[9]), "=r"(u[10]), "=r"(u[11]), "=r"(u[12]), "=r"(u[13]), "=r"(u[14]), "=r"(u[15])
+        : "r"(taddr)
+        : "memory");
+}
+
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const WaitCtl& wc, volatile int* abort) {
+    return __all_sync(0xffffffffu, mbar_wait(bar, parity, wc, abort));
+}
+
+// Per-head reduction of 16 values over the 32 lanes (max or sum).  A reduce-scatter halves
+// the values a lane keeps at each level (16 shuffles in all); afterwards lanes 2m and 2m + 1
+// both hold the result for head 8*b4 + 4*b3 + 2*b2 + b1, with b_k bit k of the lane index.
+template <bool MAX>
+__device__ __forceinline__ float head_reduce(const float (&x)[NH], int lane) {
+    const bool b4 = (lane >> 4) & 1, b3 = (lane >> 3) & 1, b2 = (lane >> 2) & 1, b1 = (lane >> 1) & 1;
+    float t8[8], t4[4], t2[2], t1;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const float keep = b4 ? x[8 + i] : x[i], send = b4 ? x[i] : x[8 + i];
+        const float o = __shfl_xor_sync(0xffffffffu, send, 16);
+        t8[i] = MAX ? fmaxf(keep, o) : keep + o;
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float keep = b3 ? t8[4 + i] : t8[i], send = b3 ? t8[i] : t8[4 + i];
+        const float o = __shfl_xor_sync(0xffffffffu, send, 8);
+        t4[i] = MAX ? fmaxf(keep, o) : keep + o;
+    }
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const float keep = b2 ? t4[2 + i] : t4[i], send = b2 ? t4[i] : t4[2 + i];
+        const float o = __shfl_xor_sync(0xffffffffu, send, 4);
+        t2[i] = MAX ? fmaxf(keep, o) : keep + o;
+    }
+    {
+        const float keep = b1 ? t2[1] : t2[0], send = b1 ? t2[0] : t2[1];
+        const float o = __shfl_xor_sync(0xffffffffu, send, 2);
+        t1 = MAX ? fmaxf(keep, o) : keep + o;
+    }
+    const float o = __shfl_xor_sync(0xffffffffu, t1, 1);
+    return MAX ? fmaxf(t1, o) : t1 + o;
+}
+
+__device__ __forceinline__ int head_of_lane(int lane) {
+    return 8 * ((lane >> 4) & 1) + 4 * ((lane >> 3) & 1) + 2 * ((lane >> 2) & 1) + ((lane >> 1) & 1);
+}
+
+template <int G, bool F16>
+__global__ void __launch_bounds__(kThreads, 1)
+    decode_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                     const DecodeTcParams p) {
+    static_assert(G >= 1 && G <= NH, "group size");
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_s = smem_u32(smem_raw);
+    uint8_t* smem = smem_raw + ((1024u - (raw_s & 1023u)) & 1023u);
+    const uint32_t sbase = smem_u32(smem);
+    const uint32_t bar0 = sbase + L::kOffBar;
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + L::kOffBar + 240);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kOffBar + 248);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int split = blockIdx.x, nsplit = gridDim.x;
+    const int hk = blockIdx.y, b = blockIdx.z;
+
+    // this split's keys [kbeg, kend) of the query's visible interval, in whole blocks
+    const int klen = valid_keys(p.key_lens, b, p.Lk);
+    long long lo, hi;
+    key_interval(p.mode, p.window, klen, p.P, p.P, &lo, &hi);
+    if (hi < lo) hi = lo;
+    long long per = (hi - lo + nsplit - 1) / nsplit;
+    per = (per + BN - 1) / BN * BN;
+    const long long kbeg = lo + (long long)split * per;
+    const long long kend = min(hi, kbeg + per);
+    const int nblk = (kend > kbeg) ? (int)((kend - kbeg + BN - 1) / BN) : 0;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kNumBars; ++i) {
+            uint32_t count = 1;
+            if (i == kBarSFree || i == kBarSFree + 1 || i == kBarPFull || i == kBarXch || i == kBarXch + 1 ||
+                i == kBarSum)
+                count = 4;  // one arrival per softmax warp
+            mbar_init(bar0 + 8 * i, count);
+        }
+        *abort_flag = 0;
+        mbar_fence_init();
+    }
+    if (warp >= 2) {
+        // Q of the group's heads into a 16-row K-major tile (128-byte swizzle), zero rows past G;
+        // 256 16-byte units, two per thread
+        const int t = threadIdx.x - 64;
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            const int ui = 2 * t + k;
+            const int r = ui >> 4, u = ui & 15;  // row (head) and 16-byte unit of the row
+            uint4 val = make_uint4(0u, 0u, 0u, 0u);
+            if (r < G) val = *reinterpret_cast<const uint4*>(p.q + ((long long)b * p.Hq + (long long)hk * G + r) * D + 8 * u);
+            const uint32_t addr = L::kOffQ + (u >> 3) * (NH * 128) + r * 128 + (((u & 7) ^ (r & 7)) << 4);
+            *reinterpret_cast<uint4*>(smem + addr) = val;
+        }
+        fence_proxy_async_smem();
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_holder), kTmemCols);
+        tmem_relinquish();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmK);
+        tma_prefetch_desc(&tmV);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_holder;
+
+    float m_run[NH];    // per head, log2 domain (identical in every softmax thread)
+    float l_part[NH];   // per head, this thread's share of the row sum
+#pragma unroll
+    for (int h = 0; h < NH; ++h) m_run[h] = -INFINITY, l_part[h] = 0.f;
+    bool ok = true;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0 && nblk > 0) {
+            const int kbh = b * p.Hkv + hk;
+            int issued = 0;
+            for (int j = 0; j < nblk; ++j) {
+                const int s = j % kStages;
+                const uint32_t n = (uint32_t)(j / kStages);
+                const int krow = (int)(kbeg + (long long)j * BN);
+                if (j >= kStages && !mbar_wait(bar0 + 8 * (kBarKEmpty + s), (n - 1) & 1, p.wc, abort_flag)) break;
+                mbar_arrive_expect_tx(bar0 + 8 * (kBarKFull + s), L::kKVBytes);
+                for (int c = 0; c < D / 64; ++c)
+                    tma_load_3d(sbase + L::kOffK + s * L::kKVBytes + c * (BN * 128), &tmK, bar0 + 8 * (kBarKFull + s),
+                                c * 64, krow, kbh);
+                if (j >= kStages && !mbar_wait(bar0 + 8 * (kBarVEmpty + s), (n - 1) & 1, p.wc, abort_flag)) {
+                    issued = 2 * j + 1;
+                    break;
+                }
+                mbar_arrive_expect_tx(bar0 + 8 * (kBarVFull + s), L::kKVBytes);
+                for (int c = 0; c < D / 64; ++c)
+                    tma_load_3d(sbase + L::kOffV + s * L::kKVBytes + c * (BN * 128), &tmV, bar0 + 8 * (kBarVFull + s),
+                                c * 64, krow, kbh);
+                issued = 2 * j + 2;
+            }
+            const int nk = (issued + 1) / 2, nv = issued / 2;
+            for (int j = (nk > kStages ? nk - kStages : 0); j < nk; ++j)
+                drain_wait(bar0 + 8 * (kBarKFull + j % kStages), (uint32_t)(j / kStages) & 1, p.wc);
+            for (int j = (nv > kStages ? nv - kStages : 0); j < nv; ++j)
+                drain_wait(bar0 + 8 * (kBarVFull + j % kStages), (uint32_t)(j / kStages) & 1, p.wc);
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0 && nblk > 0) {
+            constexpr uint32_t kIdescS = idesc_f16kind_f32(BN, NH, 0, 0, F16);  // M = keys, N = heads
+            constexpr uint32_t kIdescO = idesc_f16kind_f32(D, NH, 1, 0, F16);   // M = dims (V^T, MN-major)
+            bool mok = true;
+            auto pv = [&](int i) -> bool {
+                const int s = i % kStages;
+                if (!mbar_wait(bar0 + 8 * (kBarVFull + s), (uint32_t)(i / kStages) & 1, p.wc, abort_flag)) return false;
+                if (!mbar_wait(bar0 + 8 * kBarPFull, (uint32_t)i & 1, p.wc, abort_flag)) return false;
+                tc_fence_after();
+                const uint32_t vbase = sbase + L::kOffV + s * L::kKVBytes;
+                const uint32_t pbase = sbase + L::kOffP;
+#pragma unroll
+                for (int kk = 0; kk < BN / 16; ++kk) {
+                    const uint64_t a = smem_desc_sw128(vbase + kk * (16 * 128), BN * 128, 1024);
+                    const uint64_t bd = smem_desc_sw128(pbase + (kk >> 2) * (NH * 128) + (kk & 3) * 32, 16, 1024);
+                    tc_mma_ss(tmem + kColO, a, bd, kIdescO, (i > 0 || kk > 0) ? 1u : 0u);
+                }
+                tc_commit(bar0 + 8 * kBarPVDone);
+                tc_commit(bar0 + 8 * (kBarVEmpty + s));
+                return true;
+            };
+            for (int j = 0; mok && j < nblk; ++j) {
+                const int s = j % kStages;
+                if (!mbar_wait(bar0 + 8 * (kBarKFull + s), (uint32_t)(j / kStages) & 1, p.wc, abort_flag)) break;
+                if (j >= 2 && !mbar_wait(bar0 + 8 * (kBarSFree + (j & 1)), (uint32_t)((j - 2) >> 1) & 1, p.wc,
+                                         abort_flag))
+                    break;
+                tc_fence_after();
+                const uint32_t kbase = sbase + L::kOffK + s * L::kKVBytes;
+                const uint32_t qbase = sbase + L::kOffQ;
+#pragma unroll
+                for (int ks = 0; ks < D / 16; ++ks) {
+                    const uint64_t a = smem_desc_sw128(kbase + (ks >> 2) * (BN * 128) + (ks & 3) * 32, 16, 1024);
+                    const uint64_t bd = smem_desc_sw128(qbase + (ks >> 2) * (NH * 128) + (ks & 3) * 32, 16, 1024);
+                    tc_mma_ss(tmem + kColS + NH * (j & 1), a, bd, kIdescS, ks > 0 ? 1u : 0u);
+                }
+                tc_commit(bar0 + 8 * (kBarSFull + (j & 1)));
+                tc_commit(bar0 + 8 * (kBarKEmpty + s));
+                if (j >= 1) mok = pv(j - 1);
+            }
+            if (mok) pv(nblk - 1);
+            tc_commit(bar0 + 8 * kBarMmaDone);
+            drain_wait(bar0 + 8 * kBarMmaDone, 0, p.wc);
+        }
+    } else {
+        // ------------------------------------------------------------ softmax: one key per thread
+        const int sw = warp - 2;                     // softmax warp 0..3
+        const int key = 32 * (warp & 3) + lane;      // my TMEM lane: key of the block, later head dim
+        const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
+        const float sl = p.scale_log2;
+        float* xch = reinterpret_cast<float*>(smem + L::kOffX);
+        uint8_t* pt = smem + L::kOffP;
+        // where my key's 16 probabilities go in P^T: chunk, byte in the swizzled row
+        const int kc = key >> 6, ku = (key & 63) >> 3, kb = (key & 7) * 2;
+        const int my_head = head_of_lane(lane);
+
+        for (int j = 0; j < nblk; ++j) {
+            const int par = j & 1;
+            if (!warp_wait(bar0 + 8 * (kBarSFull + par), (uint32_t)(j >> 1) & 1, p.wc, abort_flag)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            float s[NH];
+            tmem_ld16(tmem + lane_off + kColS + NH * par, s);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar0 + 8 * (kBarSFree + par));
+
+            // scores in the log2 domain; keys outside [kend) and padding heads are -inf
+            const bool vis = kbeg + (long long)j * BN + key < kend;
+            float x[NH];
+#pragma unroll
+            for (int h = 0; h < NH; ++h) x[h] = (vis && h < G) ? s[h] * sl : -INFINITY;
+            // per-head block maxima: warp reduce-scatter, then the four warps through shared memory
+            const float wmax = head_reduce<true>(x, lane);
+            if ((lane & 1) == 0) xch[(par * 4 + sw) * NH + my_head] = wmax;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar0 + 8 * (kBarXch + par));
+            if (!warp_wait(bar0 + 8 * (kBarXch + par), (uint32_t)(j >> 1) & 1, p.wc, abort_flag)) {
+                ok = false;
+                break;
+            }
+            float alpha[NH];
+            bool rescale = false;
+#pragma unroll
+            for (int h = 0; h < NH; ++h) {
+                const float bm = fmaxf(fmaxf(xch[(par * 4 + 0) * NH + h], xch[(par * 4 + 1) * NH + h]),
+                                       fmaxf(xch[(par * 4 + 2) * NH + h], xch[(par * 4 + 3) * NH + h]));
+                alpha[h] = 1.f;
+                if (bm != -INFINITY) {
+                    if (m_run[h] == -INFINITY) {
+                        m_run[h] = bm;
+                    } else if (bm > m_run[h] + kRescaleThreshold) {
+                        alpha[h] = ex2_approx(m_run[h] - bm);
+                        m_run[h] = bm;
+                        rescale = true;
+                    }
+                }
+            }
+            // the previous P V product must be done before P^T and O^T are touched
+            if (j > 0 && !warp_wait(bar0 + 8 * kBarPVDone, (uint32_t)(j - 1) & 1, p.wc, abort_flag)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+#pragma unroll
+            for (int h = 0; h < NH; ++h) {
+                const float pr = (x[h] == -INFINITY) ? 0.f : ex2_approx(x[h] - m_run[h]);
+                const uint32_t w = pack2<F16>(pr, 0.f);
+                *reinterpret_cast<uint16_t*>(pt + kc * (NH * 128) + h * 128 + ((ku ^ (h & 7)) << 4) + kb) =
+                    (uint16_t)(w & 0xffffu);
+                l_part[h] = l_part[h] * alpha[h] + unpack2<F16>(w & 0xffffu).x;
+            }
+            if (rescale) {  // identical in every thread: O^T columns of grown heads scale by alpha
+                float o[NH];
+                tmem_ld16(tmem + lane_off + kColO, o);
+#pragma unroll
+                for (int h = 0; h < NH; ++h) o[h] *= alpha[h];
+                tmem_st16(tmem + lane_off + kColO, reinterpret_cast<const uint32_t*>(o));
+            }
+            fence_proxy_async_smem();  // P^T is read by the tensor core (async proxy)
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar0 + 8 * kBarPFull);
+        }
+
+        // ------------------------------------------------------------ epilogue: this split's partial
+        if (ok && nblk > 0) {
+            ok = warp_wait(bar0 + 8 * kBarPVDone, (uint32_t)(nblk - 1) & 1, p.wc, abort_flag);
+            tc_fence_after();
+        }
+        // row sums over the 128 keys: warp reduce-scatter, then the four warps
+        const float wsum = head_reduce<false>(l_part, lane);
+        float* sums = reinterpret_cast<float*>(smem + L::kOffS);
+        if ((lane & 1) == 0) sums[sw * NH + my_head] = wsum;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar0 + 8 * kBarSum);
+        if (ok) ok = warp_wait(bar0 + 8 * kBarSum, 0, p.wc, abort_flag);
+        float o[NH];
+        if (ok && nblk > 0) {
+            tmem_ld16(tmem + lane_off + kColO, o);
+        } else {
+#pragma unroll
+            for (int h = 0; h < NH; ++h) o[h] = 0.f;
+        }
+        // the partial (m, l, O) of this split into the (now free) K ring, for the combine
+        float* cm = reinterpret_cast<float*>(smem + L::kOffCm);
+        float* cl = reinterpret_cast<float*>(smem + L::kOffCl);
+        float* co = reinterpret_cast<float*>(smem + L::kOffCo);
+        if (threadIdx.x == 64) {
+#pragma unroll
+            for (int h = 0; h < NH; ++h) {
+                const bool has = ok && nblk > 0;
+                cm[h] = has ? m_run[h] : -INFINITY;
+                cl[h] = has ? sums[0 * NH + h] + sums[1 * NH + h] + sums[2 * NH + h] + sums[3 * NH + h] : 0.f;
+            }
+        }
+#pragma unroll
+        for (int h = 0; h < G; ++h) co[h * D + key] = o[h];
+    }
+
+    // ---------------------------------------------------------------- combine the splits in rank 0
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+    if (split == 0 && warp >= 2) {
+        const int dim = 32 * (warp & 3) + lane;
+        for (int h = 0; h < G; ++h) {
+            float ms[kMaxSplits], ls[kMaxSplits], os[kMaxSplits];
+            float mc = -INFINITY;
+            for (int r = 0; r < nsplit; ++r) {
+                uint32_t a_m, a_l, a_o;
+                asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a_m) : "r"(sbase + L::kOffCm + 4 * h), "r"(r));
+                asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a_l) : "r"(sbase + L::kOffCl + 4 * h), "r"(r));
+                asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a_o)
+                             : "r"(sbase + L::kOffCo + 4 * (h * D + dim)), "r"(r));
+                asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(ms[r]) : "r"(a_m) : "memory");
+                asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(ls[r]) : "r"(a_l) : "memory");
+                asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(os[r]) : "r"(a_o) : "memory");
+                mc = fmaxf(mc, ms[r]);
+            }
+            float acc = 0.f, l = 0.f;
+            if (mc != -INFINITY) {
+                for (int r = 0; r < nsplit; ++r) {
+                    const float f = (ms[r] == -INFINITY) ? 0.f : ex2_approx(ms[r] - mc);
+                    acc += f * os[r];
+                    l += f * ls[r];
+                }
+            }
+            const float res = (l > 0.f) ? acc / l : 0.f;
+            const long long oi = ((long long)b * p.Hq + (long long)hk * G + h) * D + dim;
+            p.out[oi] = (uint16_t)(pack2<F16>(res, 0.f) & 0xffffu);
+        }
+    }
+    // keep every CTA's shared memory alive until rank 0 has read it
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) {
+        __syncwarp();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// ---------------------------------------------------------------------- host side
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult qres;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &qres) ==
+                cudaSuccess &&
+            qres == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    });
+    return fn;
+}
+
+// [outer, L, 128] 16-bit tensor as 3-D (128, L, outer); box 64 x 128 x 1, 128-byte swizzle, zero fill.
+bool encode_kv(CUtensorMap* map, const void* base, int L, int outer, bool f16) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)L, (cuuint64_t)outer};
+    cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)L * D * 2};
+    cuuint32_t box[3] = {64, 128, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return fn(map, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base),
+              dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int G, bool F16>
+cudaError_t launch_g(const Problem& pr, const DecodeTcParams& p, int nsplit, cudaStream_t stream) {
+    CUtensorMap tk, tv;
+    if (!encode_kv(&tk, pr.k, pr.Lk, pr.B * pr.Hkv, F16) || !encode_kv(&tv, pr.v, pr.Lk, pr.B * pr.Hkv, F16))
+        return cudaErrorInvalidValue;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    static std::mutex mu;
+    static bool configured[64] = {};
+    {
+        std::lock_guard<std::mutex> g(mu);
+        if (dev < 64 && !configured[dev]) {
+            e = cudaFuncSetAttribute(decode_tc_kernel<G, F16>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmem);
+            if (e != cudaSuccess) return e;
+            configured[dev] = true;
+        }
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)nsplit, (unsigned)pr.Hkv, (unsigned)pr.B);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = L::kSmem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)nsplit;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, decode_tc_kernel<G, F16>, tk, tv, p);
+}
+
+}  // namespace
+
+bool decode_tc_supported(const Problem& p) {
+    if (p.Lq != 1 || p.D != 128) return false;
+    const int G = p.Hq / p.Hkv;
+    return G == 4 || G == 8;
+}
+
+cudaError_t launch_decode_tc(const Problem& pr, const WaitCtl& wc, cudaStream_t stream, int num_sms) {
+    if (pr.Hkv > 65535 || pr.B > 65535) return cudaErrorInvalidConfiguration;
+    DecodeTcParams p;
+    p.q = static_cast<const uint16_t*>(pr.q);
+    p.out = static_cast<uint16_t*>(pr.out);
+    p.key_lens = pr.key_lens;
+    p.Hq = pr.Hq;
+    p.Hkv = pr.Hkv;
+    p.Lk = pr.Lk;
+    p.P = pr.pos_offset;
+    p.mode = pr.mode;
+    p.window = pr.window;
+    p.scale_log2 = pr.scale * kLog2e;
+    p.wc = wc;
+    // One CTA per SM.  Measured on GB300 (batch 4-64, 2048-8192 keys): the best split count
+    // reaches about 0.84 CTAs per SM (128 on 152 SMs) and no more; clusters of 8 of these
+    // 200-KB CTAs schedule poorly (twice slower than 4 at batch 4), and a split should cover at
+    // least 1024 keys.
+    constexpr int kMaxUsedSplits = 4;
+    const long long units = (long long)pr.B * pr.Hkv;
+    const long long target = num_sms > 0 ? (27LL * num_sms) / 32 : 128;
+    int n = 1;
+    while (n < kMaxUsedSplits && units * n < target) n *= 2;
+    const int nsplit = (int)std::max(1LL, std::min<long long>(n, std::max(1LL, (long long)pr.Lk / 1024)));
+    const int G = pr.Hq / pr.Hkv;
+    if (G == 4) return pr.f16 ? launch_g<4, true>(pr, p, nsplit, stream) : launch_g<4, false>(pr, p, nsplit, stream);
+    if (G == 8) return pr.f16 ? launch_g<8, true>(pr, p, nsplit, stream) : launch_g<8, false>(pr, p, nsplit, stream);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace attn

@@ -64,6 +64,10 @@ cudaError_t launch_prefill_tc(const Problem& p, const WaitCtl& wc, cudaStream_t 
 bool decode_supported(const Problem& p);
 cudaError_t launch_decode_splitkv(const Problem& p, const WaitCtl& wc, cudaStream_t stream, int num_sms);
 
+// K5: tensor-core decode for q_len == 1, head_dim 128, 4 or 8 query heads per kv head.
+bool decode_tc_supported(const Problem& p);
+cudaError_t launch_decode_tc(const Problem& p, const WaitCtl& wc, cudaStream_t stream, int num_sms);
+
 // K2 over per-item caches: one single-query decode step for m items, item i reading its
 // own [Hkv, capacity, D] K and V caches through device pointer arrays.
 struct CachesProblem {
