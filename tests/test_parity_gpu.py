@@ -253,3 +253,22 @@ def test_bounded_wait_times_out_without_faulting():
     assert "timed out" in attn.last_error()
     assert attn.sync_status() == attn.ATTN_OK  # the word is cleared and the context stays usable
     full_check(Case("after", "bf16", B=1, Hq=2, Hkv=1, Lq=64, Lk=64, D=64, seed=13))
+
+
+# ------------------------------------------------------------------------------ tensor-core decode (K5)
+
+@pytest.mark.parametrize("G", [4, 8])
+@pytest.mark.parametrize("window", [10, 200, 1500])
+def test_decode_tc_short_window_leaves_splits_empty(G, window):
+    """One batch entry: the split count follows the cache length (up to 4 here), while a short
+    window leaves most splits without keys; their empty partials must not disturb the combine."""
+    c = Case("dectc", "bf16", B=1, Hq=2 * G, Hkv=2, Lq=1, Lk=8192, D=128, pos_offset=8191,
+             mask_mode=MASK_CAUSAL_WINDOW, window=window, seed=9600 + G + window)
+    full_check(c)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+def test_decode_tc_key_padding_multi_split(dtype):
+    c = Case("dectcpad", dtype, B=4, Hq=32, Hkv=4, Lq=1, Lk=6000, D=128, pos_offset=5999, mask_mode=MASK_CAUSAL,
+             key_len_range=(0, 6000), seed=9700)
+    full_check(c)
