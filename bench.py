@@ -40,6 +40,7 @@ METRIC = "attention TFLOP/s (prefill) and KV GB/s (decode) on 1 GB300, % of roof
 HEADLINE = "causal_gqa_bf16_4x32q8kv_4096x128"
 DECODE = "decode_bf16_64x32q8kv_8192x128"
 EXTRA_PREFILL = ["bidir_keypad_bf16_8x12x512x64", "window128_bf16_4x12x8192x64"]
+PRELUDE = "qkv_prelude_bf16_16384x32q8kv_128_normrope"
 L2_BYTES = 129 * 1024 * 1024
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
@@ -230,7 +231,7 @@ def prelude_leg(args, world, dev, peaks, peak_src):
         raise RuntimeError("device status after the prelude: " + attn.last_error())
     nbytes = 2.0 * qkv.numel() * 2 + cos.numel() * 4 * 2 + 2 * hd * 4  # qkv in, q/k/v out, tables, weights
     gbs = nbytes / sec / 1e9
-    return {"workload": "qkv_prelude_bf16_16384x32q8kv_128_normrope", "value": round(gbs * world, 1), "unit": "GB/s",
+    return {"workload": PRELUDE, "value": round(gbs * world, 1), "unit": "GB/s",
             "steps": steps, "ms_per_step": round(sec * 1e3, 4),
             "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                          "frac": round(gbs / peaks["hbm_gbs"], 4), "peak_source": f"{peak_src} HBM copy",
@@ -510,6 +511,20 @@ def run_profile_case(args):
     from head_attention_attn_gb300 import build
     build.build_library()
     attn.load()
+    if args.profile == PRELUDE:
+        T, Hq, Hkv, hd = 16384, 32, 8, 128
+        g = torch.Generator().manual_seed(1005)
+        qkv = torch.randn(T, (Hq + 2 * Hkv) * hd, generator=g).to(torch.bfloat16).to("cuda:0")
+        w = (torch.rand(hd, generator=g) + 0.5).to("cuda:0")
+        ang = torch.arange(T, dtype=torch.float64)[:, None] * 1.0e6 ** (-2.0 * torch.arange(hd // 2) / hd)[None, :]
+        cos, sin = torch.cos(ang).float().to("cuda:0"), torch.sin(ang).float().to("cuda:0")
+        for _ in range(args.warmup + args.steps):
+            attn.attn_qkv_prelude(qkv, Hq, Hkv, hd, qk_mode=attn.QK_NORM_ROPE, cos=cos, sin=sin, q_norm_w=w,
+                                  k_norm_w=w)
+        torch.cuda.synchronize()
+        attn.check_device_status()
+        print(json.dumps({"profile": args.profile, "launches": args.warmup + args.steps}))
+        return
     c = WORKLOADS[args.profile] if args.batch is None else case(args.profile, B=args.batch)
     q, k, v, kl = make_inputs(c, device="cuda:0")
     out = torch.empty_like(q)
@@ -529,7 +544,7 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-rows", type=int, default=64)
-    ap.add_argument("--profile", choices=sorted(WORKLOADS), default=None,
+    ap.add_argument("--profile", choices=sorted(WORKLOADS) + [PRELUDE], default=None,
                     help="only run --warmup + --steps launches of one workload (for profilers)")
     ap.add_argument("--batch", type=int, default=None, help="batch size override for --profile")
     args = ap.parse_args(argv)
