@@ -284,6 +284,12 @@ __device__ __forceinline__ float ex2_approx(float x) {
     return y;
 }
 
+// Named hardware barrier ID over N threads (whole warps); orders shared-memory accesses.
+template <int ID, int N>
+__device__ __forceinline__ void named_bar_sync() {
+    asm volatile("bar.sync %0, %1;" ::"n"(ID), "n"(N) : "memory");
+}
+
 // Maximum of three floats (PTX three-input max).
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
     float r;

@@ -9,7 +9,8 @@
 //   warps 2..    softmax, 8 warps per query tile: a row of S is split between two
 //                threads, one per half of the 128 key columns.  Each thread reads its 64
 //                scores from TMEM, the two halves exchange their row maxima through
-//                shared memory, and each writes its 64 probabilities (2^x on the
+//                shared memory at a named barrier of the tile's 8 warps (hardware, no
+//                polling), and each writes its 64 probabilities (2^x on the
 //                special-function unit, scale*log2(e) folded in) back into TMEM as
 //                packed 16-bit pairs (the input type: bf16 or fp16).  After the tile's last key block each half normalises
 //                and stores its half of the head dims of the row.
@@ -73,8 +74,7 @@ enum : int {
     kBarPFull = kBarSFull + kTiles,    // + tile
     kBarOFull = kBarPFull + kTiles,    // + tile: the tile's last P V product completed
     kBarMmaDone = kBarOFull + kTiles,
-    kBarXch = kBarMmaDone + 1,          // + tile: both halves of the tile posted their row values
-    kNumBars = kBarXch + kTiles,
+    kNumBars = kBarMmaDone + 1,
 };
 static_assert(kNumBars * 8 <= 240, "barrier area");
 
@@ -143,6 +143,12 @@ __device__ __forceinline__ float row_min64(const float* s) {
 struct TileRange {
     int jb, je;
 };
+
+// The 8 softmax warps of query tile t meet at named barrier 1 + t.
+__device__ __forceinline__ void tile_bar_sync(int t) {
+    if (t == 0) named_bar_sync<1, 256>();
+    else named_bar_sync<2, 256>();
+}
 
 template <int D, int NT, bool F16, bool TOK>
 __global__ void __launch_bounds__(threads_for<NT>(), 3 - NT)
@@ -218,7 +224,7 @@ __global__ void __launch_bounds__(threads_for<NT>(), 3 - NT)
     if (threadIdx.x == 0) {
         for (int i = 0; i < kNumBars; ++i) {
             uint32_t count = 1;
-            if ((i >= kBarPFull && i < kBarPFull + kTiles) || (i >= kBarXch && i < kBarXch + kTiles))
+            if (i >= kBarPFull && i < kBarPFull + kTiles)
                 count = 8;  // one arrival per softmax warp of the tile
             mbar_init(bar0 + 8 * i, count);
         }
@@ -364,16 +370,14 @@ __global__ void __launch_bounds__(threads_for<NT>(), 3 - NT)
         bool ok = true;
         const int jb = rng[t].jb, je = rng[t].je;
         float* xch = reinterpret_cast<float*>(smem + C::kOffX) + (t * 2) * BM;  // [2 halves][128 rows]
-        uint32_t x_it = 0;  // phases of the tile's exchange barrier
 
         for (int j = jb; j < je; ++j) {
             const int i = j - jb;
             // every lane waits; the warp continues only if all lanes saw the phase, so the
             // warp-collective tcgen05 operations below never run with a partial warp
-            if (!__all_sync(0xffffffffu, mbar_wait(bar0 + 8 * (kBarSFull + t), (uint32_t)i & 1, p.wc, abort_flag))) {
-                ok = false;
-                break;
-            }
+            // A warp that gave up stays in the loop and keeps meeting the tile's named barrier
+            // once per key block, so the other warps of the tile never wait for it.
+            if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar0 + 8 * (kBarSFull + t), (uint32_t)i & 1, p.wc, abort_flag));
             tc_fence_after();
             const long long tb = kv0 + (long long)j * BN + 64 * h;  // first key of my 64 columns
             const int c_lo = (int)max(0LL, min(64LL, rlo - tb));
@@ -382,6 +386,7 @@ __global__ void __launch_bounds__(threads_for<NT>(), 3 - NT)
 
             // My 64 scores stay in registers for both passes: the other half writes P into
             // columns 32..63 after the exchange below, so nothing is read back from TMEM.
+            // (after a give-up the load below reads allocated but stale columns; nothing uses them)
             float s[64];
             tmem_ld64(tS + 64 * h, s);
             float hext;
@@ -398,16 +403,13 @@ __global__ void __launch_bounds__(threads_for<NT>(), 3 - NT)
                 }
                 hext = row_min64(s);
             }
-            // exchange the half extremes of each row between the two halves of the tile
-            // (a bounded barrier wait: a partner that gave up cannot hang this warp)
+            // exchange the half extremes of each row between the two halves of the tile; every
+            // warp of the tile meets this barrier once per key block on every path, so it
+            // cannot hang (the order of S_t(j+1) after every P_t(j) keeps the slots from
+            // being overwritten before the partner has read them)
             xch[h * BM + row] = hext;
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar0 + 8 * (kBarXch + t));
-            if (!__all_sync(0xffffffffu, mbar_wait(bar0 + 8 * (kBarXch + t), x_it & 1, p.wc, abort_flag))) {
-                ok = false;
-                break;
-            }
-            ++x_it;
+            tile_bar_sync(t);
+            if (!ok) continue;
             const float oext = xch[(1 - h) * BM + row];
             const float ext = (sl >= 0.f) ? fmaxf(hext, oext) : fminf(hext, oext);
             const bool any = (sl >= 0.f) ? (ext != -INFINITY) : (ext != INFINITY);
@@ -476,13 +478,9 @@ __global__ void __launch_bounds__(threads_for<NT>(), 3 - NT)
         // row sum = both halves' shares; each half stores its D/2 head dims of the row
         float* lch = reinterpret_cast<float*>(smem + C::kOffL) + (t * 2) * BM;
         float l_tot = l_run;
-        if (ok) {
-            lch[h * BM + row] = l_run;
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar0 + 8 * (kBarXch + t));
-            ok = __all_sync(0xffffffffu, mbar_wait(bar0 + 8 * (kBarXch + t), x_it & 1, p.wc, abort_flag));
-            if (ok) l_tot += lch[(1 - h) * BM + row];
-        }
+        if (ok) lch[h * BM + row] = l_run;
+        tile_bar_sync(t);
+        if (ok) l_tot += lch[(1 - h) * BM + row];
         const bool has = je > jb;
         if (ok && has) {
             ok = __all_sync(0xffffffffu, mbar_wait(bar0 + 8 * (kBarOFull + t), 0, p.wc, abort_flag));
