@@ -67,7 +67,7 @@ __device__ __forceinline__ void load8f(const float* p, float* f) {
 constexpr int kRowsPerGroup = 4;  // head rows of one token handled by one thread group
 
 template <int HD, bool F16>
-__global__ void __launch_bounds__(256) prelude_kernel(const __grid_constant__ PreludeParams p) {
+__global__ void __launch_bounds__(256, 3) prelude_kernel(const __grid_constant__ PreludeParams p) {
     constexpr int TPR = HD / 16;  // threads per group (and per head row)
     constexpr int R = kRowsPerGroup;
     const int slots = p.q_heads + 2 * p.kv_heads;
@@ -127,13 +127,6 @@ __global__ void __launch_bounds__(256) prelude_kernel(const __grid_constant__ Pr
         load8f(p.cos + pos * (HD / 2) + 8 * c, cs);
         load8f(p.sin + pos * (HD / 2) + 8 * c, sn);
     }
-    float wq[16], wk[16];
-    if (valid && p.qk_mode == 1) {
-        load8f(p.q_norm_w + o0, wq);
-        load8f(p.q_norm_w + o1, wq + 8);
-        load8f(p.k_norm_w + o0, wk);
-        load8f(p.k_norm_w + o1, wk + 8);
-    }
 
 #pragma unroll
     for (int r = 0; r < R; ++r) {
@@ -161,7 +154,10 @@ __global__ void __launch_bounds__(256) prelude_kernel(const __grid_constant__ Pr
         for (int m = 1; m < TPR; m <<= 1) ss += __shfl_xor_sync(0xffffffffu, ss, m, TPR);
         if (rotate && p.qk_mode == 1) {
             const float rs = rsqrtf(ss * (1.f / HD) + p.eps);
-            const float* w = is_q ? wq : wk;
+            float w[16];  // the row's norm weights of my 16 value indices (cached reads)
+            const float* wsrc = is_q ? p.q_norm_w : p.k_norm_w;
+            load8f(wsrc + o0, w);
+            load8f(wsrc + o1, w + 8);
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 a[i] = a[i] * rs * w[i];
