@@ -2,7 +2,10 @@
 // bf16 or fp16 inputs and outputs, fp32 accumulation.
 //
 // One CTA computes NT 128-row query tiles (NT = 2 for head_dim 128, NT = 1 for
-// head_dim 64) of one (batch, query head), sharing every K and V tile between them:
+// head_dim 64), sharing every K and V tile between them.  With two tiles and an even number
+// of query heads per kv head, the tiles are two query heads of one kv group over the same
+// rows (both visit exactly the same key tiles, so neither idles at the end); otherwise they
+// are two consecutive row blocks of one (batch, query head).
 //   warp 0       TMA producer: the Q tiles once, then 128-key K and V tiles
 //                through 2-stage shared-memory rings (128-byte swizzle).
 //   warp 1       TMEM owner and single-thread MMA issuer.
@@ -150,7 +153,10 @@ __device__ __forceinline__ void tile_bar_sync(int t) {
     else named_bar_sync<2, 256>();
 }
 
-template <int D, int NT, bool F16, bool TOK>
+// PAIR (two tiles, even group size): the tiles are two query heads of one kv group over the
+// same 128 query rows, so both visit exactly the same key tiles.  Otherwise the tiles are two
+// consecutive 128-row blocks of one query head.
+template <int D, int NT, bool F16, bool TOK, bool PAIR>
 __global__ void __launch_bounds__(threads_for<NT>(), 3 - NT)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV, const PrefillParams p) {
@@ -168,13 +174,17 @@ __global__ void __launch_bounds__(threads_for<NT>(), 3 - NT)
     const int lane = threadIdx.x & 31;
 
     int idx = blockIdx.x;
-    const int hq = idx % p.Hq;
-    idx /= p.Hq;
+    const int nh = PAIR ? p.Hq / 2 : p.Hq;
+    const int hq = (idx % nh) * (PAIR ? 2 : 1);  // query head of tile 0
+    idx /= nh;
     const int b = idx % p.B;
     idx /= p.B;
     const int mblk = p.num_m - 1 - idx;  // heaviest blocks first
     const int hk = hq / (p.Hq / p.Hkv);
-    const int q0 = mblk * (kTiles * BM);
+    const int q0 = mblk * (PAIR ? BM : kTiles * BM);  // first query row of tile 0
+    // tile t: query head hq + tile_dh(t), rows from q0 + tile_dq(t)
+    auto tile_dh = [](int t) { return PAIR ? t : 0; };
+    auto tile_dq = [](int t) { return PAIR ? 0 : t * BM; };
     // Rows of this item: the batch entry's Lq queries / Lk keys (head-major), or (TOK) packed
     // sequence b, rows [row0, row0 + len) of the token-major tensors (self-attention).
     constexpr bool tok = TOK;
@@ -197,7 +207,7 @@ __global__ void __launch_bounds__(threads_for<NT>(), 3 - NT)
     long long kv0 = -1;
 #pragma unroll
     for (int t = 0; t < kTiles; ++t) {
-        const int qa = q0 + t * BM;
+        const int qa = q0 + tile_dq(t);
         if (qa >= Lq) {
             tlo[t] = 0;
             thi[t] = 0;
@@ -248,17 +258,16 @@ __global__ void __launch_bounds__(threads_for<NT>(), 3 - NT)
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0 && ntiles > 0) {
-            const int qbh = b * p.Hq + hq;
             const int kbh = b * p.Hkv + hk;
             mbar_arrive_expect_tx(bar0 + 8 * kBarQFull, kTiles * C::kQBytes);
             for (int t = 0; t < kTiles; ++t)
                 for (int c = 0; c < C::kChunks; ++c)
                     if constexpr (TOK)
                         tma_load_3d(sbase + C::kOffQ + t * C::kQBytes + c * (BM * 128), &tmQ, bar0 + 8 * kBarQFull,
-                                    c * 64, hq, row0 + q0 + t * BM);
+                                    c * 64, hq + tile_dh(t), row0 + q0 + tile_dq(t));
                     else
                         tma_load_3d(sbase + C::kOffQ + t * C::kQBytes + c * (BM * 128), &tmQ, bar0 + 8 * kBarQFull,
-                                    c * 64, q0 + t * BM, qbh);
+                                    c * 64, q0 + tile_dq(t), b * p.Hq + hq + tile_dh(t));
             int issued = 0;
             for (int j = 0; j < ntiles; ++j) {
                 const int s = j % kStages;
@@ -357,7 +366,8 @@ __global__ void __launch_bounds__(threads_for<NT>(), 3 - NT)
         const int h = (sw >> 2) & 1;
         const int wq = warp & 3;                 // TMEM lane quarter
         const int row = wq * 32 + lane;
-        const int qi = q0 + t * BM + row;
+        const int qi = q0 + tile_dq(t) + row;
+        const int hqt = hq + tile_dh(t);
         const long long qpos = (long long)p.P + qi;
         long long rlo, rhi;
         key_interval(p.mode, p.window, klen, qpos, qpos, &rlo, &rhi);
@@ -486,10 +496,10 @@ __global__ void __launch_bounds__(threads_for<NT>(), 3 - NT)
             ok = __all_sync(0xffffffffu, mbar_wait(bar0 + 8 * (kBarOFull + t), 0, p.wc, abort_flag));
             tc_fence_after();
         }
-        if (ok && q0 + t * BM < Lq) {
+        if (ok && q0 + tile_dq(t) < Lq) {
             const float inv = (l_tot > 0.f) ? 1.f / l_tot : 0.f;
             __nv_bfloat16* orow =
-                p.out + (tok ? ((size_t)(row0 + qi) * p.Hq + hq) * D : ((size_t)(b * p.Hq + hq) * Lq + qi) * D) +
+                p.out + (tok ? ((size_t)(row0 + qi) * p.Hq + hqt) * D : ((size_t)(b * p.Hq + hqt) * Lq + qi) * D) +
                 (D / 2) * h;
 #pragma unroll
             for (int c = 0; c < D / 64; ++c) {
@@ -574,7 +584,7 @@ bool encode_16bit_3d_tok(CUtensorMap* map, const void* base, int D, int H, int t
     return r == CUDA_SUCCESS;
 }
 
-template <int D, int NT, bool F16, bool TOK>
+template <int D, int NT, bool F16, bool TOK, bool PAIR = false>
 cudaError_t launch_impl(const Problem& pr, const WaitCtl& wc, cudaStream_t stream) {
     using C = Cfg<D, NT>;
     constexpr int kTiles = NT;
@@ -597,7 +607,7 @@ cudaError_t launch_impl(const Problem& pr, const WaitCtl& wc, cudaStream_t strea
     {
         std::lock_guard<std::mutex> g(mu);
         if (dev < 64 && !configured[dev]) {
-            e = cudaFuncSetAttribute(prefill_tc_kernel<D, NT, F16, TOK>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+            e = cudaFuncSetAttribute(prefill_tc_kernel<D, NT, F16, TOK, PAIR>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
             if (e != cudaSuccess) return e;
             configured[dev] = true;
         }
@@ -613,14 +623,15 @@ cudaError_t launch_impl(const Problem& pr, const WaitCtl& wc, cudaStream_t strea
     p.P = pr.pos_offset;
     p.mode = pr.mode;
     p.window = pr.window;
-    p.num_m = (pr.Lq + kTiles * BM - 1) / (kTiles * BM);  // pr.Lq is max_seqlen for packed sequences
+    constexpr int rows = PAIR ? BM : kTiles * BM;  // query rows per work item
+    p.num_m = (pr.Lq + rows - 1) / rows;  // pr.Lq is max_seqlen for packed sequences
     p.cu_seqlens = pr.cu_seqlens;
     p.total = pr.total;
     p.scale_log2 = pr.scale * kLog2e;
     p.wc = wc;
-    const long long grid = (long long)p.num_m * pr.B * pr.Hq;
+    const long long grid = (long long)p.num_m * pr.B * (PAIR ? pr.Hq / 2 : pr.Hq);
     if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    prefill_tc_kernel<D, NT, F16, TOK><<<(unsigned)grid, threads_for<NT>(), C::kSmem, stream>>>(tq, tk, tv, p);
+    prefill_tc_kernel<D, NT, F16, TOK, PAIR><<<(unsigned)grid, threads_for<NT>(), C::kSmem, stream>>>(tq, tk, tv, p);
     return cudaGetLastError();
 }
 
@@ -636,6 +647,13 @@ cudaError_t launch_prefill_tc(const Problem& p, const WaitCtl& wc, cudaStream_t 
         return p.f16 ? launch_impl<64, 1, true, false>(p, wc, stream) : launch_impl<64, 1, false, false>(p, wc, stream);
     }
     if (p.D == 128) {
+        // an even group size pairs two query heads of one kv group over the same rows
+        if ((p.Hq / p.Hkv) % 2 == 0) {
+            if (tok) return p.f16 ? launch_impl<128, 2, true, true, true>(p, wc, stream)
+                                  : launch_impl<128, 2, false, true, true>(p, wc, stream);
+            return p.f16 ? launch_impl<128, 2, true, false, true>(p, wc, stream)
+                         : launch_impl<128, 2, false, false, true>(p, wc, stream);
+        }
         if (tok) return p.f16 ? launch_impl<128, 2, true, true>(p, wc, stream) : launch_impl<128, 2, false, true>(p, wc, stream);
         return p.f16 ? launch_impl<128, 2, true, false>(p, wc, stream) : launch_impl<128, 2, false, false>(p, wc, stream);
     }
