@@ -231,6 +231,31 @@ __global__ void __launch_bounds__(threads_for<NT>(), 3 - NT)
     }
     if (kv0 < 0) kv0 = 0;
 
+    const int kbh = b * p.Hkv + hk;
+    auto load_q = [&]() {
+        mbar_arrive_expect_tx(bar0 + 8 * kBarQFull, kTiles * C::kQBytes);
+        for (int t = 0; t < kTiles; ++t)
+            for (int c = 0; c < C::kChunks; ++c)
+                if constexpr (TOK)
+                    tma_load_3d(sbase + C::kOffQ + t * C::kQBytes + c * (BM * 128), &tmQ, bar0 + 8 * kBarQFull,
+                                c * 64, hq + tile_dh(t), row0 + q0 + tile_dq(t));
+                else
+                    tma_load_3d(sbase + C::kOffQ + t * C::kQBytes + c * (BM * 128), &tmQ, bar0 + 8 * kBarQFull,
+                                c * 64, q0 + tile_dq(t), b * p.Hq + hq + tile_dh(t));
+    };
+    auto load_kv = [&](const CUtensorMap* map, int off, int bar, int j) {
+        const int s = j % kStages;
+        const int krow = (int)kv0 + j * BN;
+        mbar_arrive_expect_tx(bar0 + 8 * (bar + s), C::kKVBytes);
+        for (int c = 0; c < C::kChunks; ++c)
+            tma_load_3d(sbase + off + s * C::kKVBytes + c * (BN * 128), map, bar0 + 8 * (bar + s), c * 64,
+                        TOK ? hk : krow, TOK ? row0 + krow : kbh);
+    };
+    // With one tile per CTA (two CTAs per SM) the first copies go out before the CTA
+    // synchronises; with two tiles (one CTA per SM) that delays the CTA's start more than
+    // the copies gain, so the producer starts them after the barrier.
+    const int nearly = kTiles == 1 ? min(kStages, ntiles) : 0;  // K/V tiles loaded at entry
+
     if (threadIdx.x == 0) {
         for (int i = 0; i < kNumBars; ++i) {
             uint32_t count = 1;
@@ -240,12 +265,21 @@ __global__ void __launch_bounds__(threads_for<NT>(), 3 - NT)
         }
         *abort_flag = 0;
         mbar_fence_init();
+        // Thread 0 is the producer: its first copies start now and land while TMEM is
+        // allocated and the CTA synchronises.
+        if (kTiles == 1 && ntiles > 0) {
+            load_q();
+            for (int j = 0; j < nearly; ++j) {
+                load_kv(&tmK, C::kOffK, kBarKFull, j);
+                load_kv(&tmV, C::kOffV, kBarVFull, j);
+            }
+        }
     }
     if (warp == 1) {
         tmem_alloc(smem_u32(tmem_holder), C::kTmemCols);
         tmem_relinquish();
     }
-    if (warp == 0 && lane == 0) {
+    if (kTiles == 2 && warp == 0 && lane == 0) {
         tma_prefetch_desc(&tmQ);
         tma_prefetch_desc(&tmK);
         tma_prefetch_desc(&tmV);
@@ -258,34 +292,18 @@ __global__ void __launch_bounds__(threads_for<NT>(), 3 - NT)
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0 && ntiles > 0) {
-            const int kbh = b * p.Hkv + hk;
-            mbar_arrive_expect_tx(bar0 + 8 * kBarQFull, kTiles * C::kQBytes);
-            for (int t = 0; t < kTiles; ++t)
-                for (int c = 0; c < C::kChunks; ++c)
-                    if constexpr (TOK)
-                        tma_load_3d(sbase + C::kOffQ + t * C::kQBytes + c * (BM * 128), &tmQ, bar0 + 8 * kBarQFull,
-                                    c * 64, hq + tile_dh(t), row0 + q0 + tile_dq(t));
-                    else
-                        tma_load_3d(sbase + C::kOffQ + t * C::kQBytes + c * (BM * 128), &tmQ, bar0 + 8 * kBarQFull,
-                                    c * 64, q0 + tile_dq(t), b * p.Hq + hq + tile_dh(t));
-            int issued = 0;
-            for (int j = 0; j < ntiles; ++j) {
+            if (kTiles == 2) load_q();
+            int issued = 2 * nearly;  // K/V copies issued at entry
+            for (int j = nearly; j < ntiles; ++j) {
                 const int s = j % kStages;
                 const uint32_t n = (uint32_t)(j / kStages);
-                const int krow = (int)kv0 + j * BN;
                 if (j >= kStages && !mbar_wait(bar0 + 8 * (kBarKEmpty + s), (n - 1) & 1, p.wc, abort_flag)) break;
-                mbar_arrive_expect_tx(bar0 + 8 * (kBarKFull + s), C::kKVBytes);
-                for (int c = 0; c < C::kChunks; ++c)
-                    tma_load_3d(sbase + C::kOffK + s * C::kKVBytes + c * (BN * 128), &tmK,
-                                bar0 + 8 * (kBarKFull + s), c * 64, tok ? hk : krow, tok ? row0 + krow : kbh);
+                load_kv(&tmK, C::kOffK, kBarKFull, j);
                 if (j >= kStages && !mbar_wait(bar0 + 8 * (kBarVEmpty + s), (n - 1) & 1, p.wc, abort_flag)) {
                     issued = 2 * j + 1;
                     break;
                 }
-                mbar_arrive_expect_tx(bar0 + 8 * (kBarVFull + s), C::kKVBytes);
-                for (int c = 0; c < C::kChunks; ++c)
-                    tma_load_3d(sbase + C::kOffV + s * C::kKVBytes + c * (BN * 128), &tmV,
-                                bar0 + 8 * (kBarVFull + s), c * 64, tok ? hk : krow, tok ? row0 + krow : kbh);
+                load_kv(&tmV, C::kOffV, kBarVFull, j);
                 issued = 2 * j + 2;
             }
             drain_wait(bar0 + 8 * kBarQFull, 0, p.wc);
