@@ -411,6 +411,11 @@ __global__ void __launch_bounds__(threads_for<NT>(), 3 - NT)
             const int c_lo = (int)max(0LL, min(64LL, rlo - tb));
             const int c_hi = (int)max(0LL, min(64LL, rhi - tb));
             const bool full = (c_lo == 0 && c_hi == 64);
+            // every row of my warp sees none of my 64 keys (a band edge on a 32-row boundary):
+            // no max and no exponentials, just zeros for my half of P.  Only with one tile per
+            // CTA (head_dim 64): there every window key tile has such warps, while at two tiles
+            // only diagonal tiles do and the test costs more than it saves.
+            const bool skip = kTiles == 1 && __all_sync(0xffffffffu, c_lo >= c_hi);
 
             // My 64 scores stay in registers for both passes: the other half writes P into
             // columns 32..63 after the exchange below, so nothing is read back from TMEM.
@@ -418,7 +423,9 @@ __global__ void __launch_bounds__(threads_for<NT>(), 3 - NT)
             float s[64];
             tmem_ld64(tS + 64 * h, s);
             float hext;
-            if (sl >= 0.f) {
+            if (skip) {
+                hext = (sl >= 0.f) ? -INFINITY : INFINITY;
+            } else if (sl >= 0.f) {
                 if (!full) {
 #pragma unroll
                     for (int c = 0; c < 64; ++c) s[c] = (c >= c_lo && c < c_hi) ? s[c] : -INFINITY;
@@ -460,6 +467,13 @@ __global__ void __launch_bounds__(threads_for<NT>(), 3 - NT)
             // P for my 64 keys -> TMEM columns [32h, 32h + 32) of S_t, as bf16 or fp16 pairs; the row
             // sum adds the rounded values the tensor core will multiply into V.
             float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+            if (skip) {
+                uint32_t z[16];
+#pragma unroll
+                for (int q = 0; q < 16; ++q) z[q] = 0u;
+                tmem_st16_async(tS + 32 * h, z);
+                tmem_st16_async(tS + 32 * h + 16, z);
+            } else {
 #pragma unroll
             for (int k = 0; k < 2; ++k) {
                 uint32_t pk[16];
@@ -482,6 +496,7 @@ __global__ void __launch_bounds__(threads_for<NT>(), 3 - NT)
                     if ((c2 / 2) & 1) acc1 = __fadd2_rn(acc1, r2); else acc0 = __fadd2_rn(acc0, r2);
                 }
                 tmem_st16_async(tS + 32 * h + 16 * k, pk);
+            }
             }
             tmem_st_wait();
             acc0 = __fadd2_rn(acc0, acc1);
