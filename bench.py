@@ -46,7 +46,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 
 # DRAM bytes per launch measured by ncu (dram__bytes_read.sum + dram__bytes_write.sum) for a
 # kernel source state; the entry stops applying as soon as the kernel source changes.
-NCU_TRAFFIC = {"cbf3c7a38eca": 444619776.0}  # prefill_tc_kernel<128, 2, bf16, paired heads>: 341.50 MB read + 103.12 MB written
+NCU_TRAFFIC = {"538431232122": 460976896.0}  # prefill_tc_kernel<128, 2, bf16, paired heads>: 357.80 MB read + 103.18 MB written
 
 
 # ----------------------------------------------------------------------------- distributed plumbing

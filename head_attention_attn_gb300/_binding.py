@@ -17,7 +17,7 @@ MASK_NONE, MASK_CAUSAL, MASK_WINDOW, MASK_CAUSAL_WINDOW = 0, 1, 2, 3
 QK_COPY, QK_NORM_ROPE, QK_ROPE, QK_ROPE_INTERLEAVED = 0, 1, 2, 3
 ATTN_BF16, ATTN_F32, ATTN_F16 = 0, 1, 2
 
-EXPORTED = ("attn_fwd", "attn_fwd_varlen", "attn_decode_caches", "attn_qkv_prelude", "attn_qkv_prelude_caches", "attn_last_error", "attn_sync_status", "attn_selftest_timeout",
+EXPORTED = ("attn_fwd", "attn_fwd_out_token_major", "attn_fwd_varlen", "attn_decode_caches", "attn_qkv_prelude", "attn_qkv_prelude_caches", "attn_last_error", "attn_sync_status", "attn_selftest_timeout",
             "attn_version")
 
 _STATUS_NAMES = {0: "ATTN_OK", 1: "ATTN_ERR_INVALID_ARG", 2: "ATTN_ERR_UNSUPPORTED", 3: "ATTN_ERR_CUDA",
@@ -53,6 +53,8 @@ def load(path: str | None = None):
         vp, ci = ctypes.c_void_p, ctypes.c_int
         lib.attn_fwd.restype = ci
         lib.attn_fwd.argtypes = [vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, ci, ci, ci, vp, ctypes.c_float, ci, vp]
+        lib.attn_fwd_out_token_major.restype = ci
+        lib.attn_fwd_out_token_major.argtypes = lib.attn_fwd.argtypes
         lib.attn_fwd_varlen.restype = ci
         lib.attn_fwd_varlen.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, ci, ci, ctypes.c_float, ci, vp]
         lib.attn_qkv_prelude.restype = ci
@@ -103,11 +105,12 @@ def attn_fwd_raw(q_ptr, k_ptr, v_ptr, out_ptr, batch, q_heads, kv_heads, q_len, 
 
 
 def attn_fwd(q, k, v, out=None, *, pos_offset: int = 0, mask_mode: int = MASK_NONE, window: int = 0,
-             key_lens=None, scale: float | None = None, stream=None):
+             key_lens=None, scale: float | None = None, stream=None, out_token_major: bool = False):
     """Attention forward on CUDA tensors (head-major, contiguous).
 
     q [B, Hq, Lq, D], k and v [B, Hkv, Lk, D] (bf16, fp16 or fp32, same dtype),
     key_lens: int32 CUDA tensor [B] or None; out: preallocated [B, Hq, Lq, D] or None.
+    out_token_major: out is [B, Lq, Hq, D] instead (attn_fwd_out_token_major).
     scale None means 1/sqrt(D) rounded to fp32.  Enqueues on `stream`
     (default: torch's current stream) and returns out without synchronising.
     """
@@ -133,10 +136,11 @@ def attn_fwd(q, k, v, out=None, *, pos_offset: int = 0, mask_mode: int = MASK_NO
     Bk, Hkv, Lk, Dk = k.shape
     if tuple(v.shape) != tuple(k.shape) or Bk != B or Dk != D:
         raise ValueError("shape mismatch between q, k and v")
+    out_shape = (B, Lq, Hq, D) if out_token_major else (B, Hq, Lq, D)
     if out is None:
-        out = torch.empty_like(q)
-    elif out.shape != q.shape or out.dtype != q.dtype or not out.is_contiguous() or not out.is_cuda:
-        raise ValueError("out must be a contiguous CUDA tensor shaped and typed like q")
+        out = torch.empty(out_shape, dtype=q.dtype, device=q.device)
+    elif tuple(out.shape) != out_shape or out.dtype != q.dtype or not out.is_contiguous() or not out.is_cuda:
+        raise ValueError(f"out must be a contiguous CUDA tensor of shape {out_shape} and q's dtype")
     kl_ptr = None
     if key_lens is not None:
         if key_lens.dtype != torch.int32 or not key_lens.is_cuda or key_lens.numel() != B:
@@ -144,9 +148,9 @@ def attn_fwd(q, k, v, out=None, *, pos_offset: int = 0, mask_mode: int = MASK_NO
         kl_ptr = key_lens.data_ptr()
     if scale is None:
         scale = float(torch.tensor(1.0 / math.sqrt(D), dtype=torch.float32).item())
-    status = attn_fwd_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), B, Hq, Hkv, Lq, Lk, D,
-                          int(pos_offset), int(mask_mode), int(window), kl_ptr, float(scale), dtype,
-                          _stream_handle(stream))
+    fn = load().attn_fwd_out_token_major if out_token_major else load().attn_fwd
+    status = fn(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), B, Hq, Hkv, Lq, Lk, D, int(pos_offset),
+                int(mask_mode), int(window), kl_ptr, ctypes.c_float(float(scale)), dtype, _stream_handle(stream))
     _check(status)
     return out
 

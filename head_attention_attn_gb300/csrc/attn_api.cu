@@ -70,13 +70,11 @@ attn_status device_state(DeviceState** out) {
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-}  // namespace
-
-extern "C" {
-
-attn_status attn_fwd(const void* q, const void* k, const void* v, void* out, int batch, int q_heads, int kv_heads,
-                     int q_len, int kv_len, int head_dim, int pos_offset, int mask_mode, int window,
-                     const int32_t* key_lens, float scale, int dtype, void* cuda_stream) {
+// attn_fwd and attn_fwd_out_token_major: the same checks and kernels, out_tok choosing the
+// layout of out.
+attn_status fwd(const void* q, const void* k, const void* v, void* out, int batch, int q_heads, int kv_heads,
+                int q_len, int kv_len, int head_dim, int pos_offset, int mask_mode, int window,
+                const int32_t* key_lens, float scale, int dtype, void* cuda_stream, bool out_tok) {
     t_last_error.clear();
     if (batch < 0 || q_len < 0 || kv_len < 0)
         return fail(ATTN_ERR_INVALID_ARG, "negative size (batch=%d, q_len=%d, kv_len=%d)", batch, q_len, kv_len);
@@ -122,6 +120,7 @@ attn_status attn_fwd(const void* q, const void* k, const void* v, void* out, int
     attn::WaitCtl wc{st->status, kWaitLimitNs};
     attn::Problem p{q, k, v, out, batch, q_heads, kv_heads, q_len, kv_len, head_dim,
                     pos_offset, mask_mode, window, key_lens, scale, dtype == ATTN_F16};
+    p.out_tok = out_tok;  // the decode kernels run only for q_len 1, where both layouts coincide
 
     cudaError_t e;
     const char* which;
@@ -142,6 +141,25 @@ attn_status attn_fwd(const void* q, const void* k, const void* v, void* out, int
     }
     if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "%s launch: %s", which, cudaGetErrorString(e));
     return ATTN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+attn_status attn_fwd(const void* q, const void* k, const void* v, void* out, int batch, int q_heads, int kv_heads,
+                     int q_len, int kv_len, int head_dim, int pos_offset, int mask_mode, int window,
+                     const int32_t* key_lens, float scale, int dtype, void* cuda_stream) {
+    return fwd(q, k, v, out, batch, q_heads, kv_heads, q_len, kv_len, head_dim, pos_offset, mask_mode, window,
+               key_lens, scale, dtype, cuda_stream, false);
+}
+
+attn_status attn_fwd_out_token_major(const void* q, const void* k, const void* v, void* out, int batch,
+                                     int q_heads, int kv_heads, int q_len, int kv_len, int head_dim, int pos_offset,
+                                     int mask_mode, int window, const int32_t* key_lens, float scale, int dtype,
+                                     void* cuda_stream) {
+    return fwd(q, k, v, out, batch, q_heads, kv_heads, q_len, kv_len, head_dim, pos_offset, mask_mode, window,
+               key_lens, scale, dtype, cuda_stream, true);
 }
 
 attn_status attn_fwd_varlen(const void* q, const void* k, const void* v, void* out, const int32_t* cu_seqlens,

@@ -25,6 +25,8 @@ struct Problem {
     // Null for the head-major batch layout.
     const int32_t* cu_seqlens;
     int total;
+    // Head-major batch only: out is token-major [B, Lq, Hq, D] instead of [B, Hq, Lq, D].
+    bool out_tok = false;
 };
 
 // Visible key interval [lo, hi) for queries at positions [qpos_lo, qpos_hi]

@@ -88,6 +88,7 @@ struct PrefillParams {
     int num_m;          // query blocks (NT tiles each) per head
     const int32_t* cu_seqlens;  // packed token-major sequences [B + 1], or null (head-major batch)
     int total;          // packed rows (token-major)
+    int out_tok;        // head-major batch: out is [B, Lq, Hq, D] instead of [B, Hq, Lq, D]
     float scale_log2;
     WaitCtl wc;
 };
@@ -532,7 +533,9 @@ __global__ void __launch_bounds__(threads_for<NT>(), 3 - NT)
         if (ok && q0 + tile_dq(t) < Lq) {
             const float inv = (l_tot > 0.f) ? 1.f / l_tot : 0.f;
             __nv_bfloat16* orow =
-                p.out + (tok ? ((size_t)(row0 + qi) * p.Hq + hqt) * D : ((size_t)(b * p.Hq + hqt) * Lq + qi) * D) +
+                p.out + (tok        ? ((size_t)(row0 + qi) * p.Hq + hqt) * D
+                         : p.out_tok ? (((size_t)b * Lq + qi) * p.Hq + hqt) * D
+                                     : ((size_t)(b * p.Hq + hqt) * Lq + qi) * D) +
                 (D / 2) * h;
 #pragma unroll
             for (int c = 0; c < D / 64; ++c) {
@@ -660,6 +663,7 @@ cudaError_t launch_impl(const Problem& pr, const WaitCtl& wc, cudaStream_t strea
     p.num_m = (pr.Lq + rows - 1) / rows;  // pr.Lq is max_seqlen for packed sequences
     p.cu_seqlens = pr.cu_seqlens;
     p.total = pr.total;
+    p.out_tok = pr.out_tok ? 1 : 0;
     p.scale_log2 = pr.scale * kLog2e;
     p.wc = wc;
     const long long grid = (long long)p.num_m * pr.B * (PAIR ? pr.Hq / 2 : pr.Hq);

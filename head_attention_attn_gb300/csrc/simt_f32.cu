@@ -29,6 +29,7 @@ struct SimtParams {
     float* out;
     const int32_t* key_lens;
     int Hq, Hkv, Lq, Lk, D, P, mode, window;
+    int out_tok;  // out is [B, Lq, Hq, D] instead of [B, Hq, Lq, D]
     float scale;
 };
 
@@ -101,7 +102,7 @@ __global__ void __launch_bounds__(kRowsPerBlock * 32) simt_f32_kernel(const Simt
     }
 
     const float inv = (l > 0.f) ? 1.f / l : 0.f;
-    float* orow = p.out + (((size_t)b * p.Hq + hq) * p.Lq + i) * D;
+    float* orow = p.out + (p.out_tok ? (((size_t)b * p.Lq + i) * p.Hq + hq) * D : (((size_t)b * p.Hq + hq) * p.Lq + i) * D);
 #pragma unroll
     for (int t = 0; t < kMaxD / 32; ++t) {
         const int d = lane + 32 * t;
@@ -127,6 +128,7 @@ cudaError_t launch_simt_f32(const Problem& pr, const WaitCtl& wc, cudaStream_t s
     p.P = pr.pos_offset;
     p.mode = pr.mode;
     p.window = pr.window;
+    p.out_tok = pr.out_tok ? 1 : 0;
     p.scale = pr.scale;
     if (pr.Hq > 65535 || pr.B > 65535) return cudaErrorInvalidConfiguration;
     dim3 grid((unsigned)((pr.Lq + kRowsPerBlock - 1) / kRowsPerBlock), (unsigned)pr.Hq, (unsigned)pr.B);

@@ -133,6 +133,23 @@ ATTN_API attn_status attn_fwd(const void* q, const void* k, const void* v, void*
                      float scale, int dtype, void* cuda_stream);
 
 /*
+ * attn_fwd_out_token_major -- attn_fwd with the output written token-major.
+ *
+ * Source: ferrum-kernels Backend::transpose_head_to_token, which turns the head-major
+ * attention output [heads, tokens, head_dim] into [tokens, heads * head_dim] for the output
+ * projection; here that transposition is part of the kernels' store, so no extra pass exists.
+ *
+ * Every argument, check and status is the one attn_fwd has, except the layout of out:
+ *   out  [batch, q_len, q_heads, head_dim]   (row (b, i) holds all heads of query i)
+ * and the same value out_token_major[b][i][h][:] == out_head_major[b][h][i][:].  For
+ * q_len 1 the two layouts are the same bytes.  kv_len 0 zero-fills out.
+ */
+ATTN_API attn_status attn_fwd_out_token_major(const void* q, const void* k, const void* v, void* out,
+                     int batch, int q_heads, int kv_heads, int q_len, int kv_len, int head_dim,
+                     int pos_offset, int mask_mode, int window, const int32_t* key_lens,
+                     float scale, int dtype, void* cuda_stream);
+
+/*
  * attn_fwd_varlen -- attention over a batch of packed (unpadded) sequences.
  *
  * Source: ripvec-core Driver::prepare_batch_unpadded, which concatenates all tokens flat

@@ -94,6 +94,25 @@ def test_empty_problems_launch_nothing(lib, change):
     assert attn.last_error() == ""
 
 
+@pytest.mark.parametrize("change,fragment", [
+    (dict(batch=-1), "negative size"),
+    (dict(q_heads=3, kv_heads=2), "not a multiple"),
+    (dict(mask_mode=4), "mask_mode"),
+    (dict(dtype=3), "dtype"),
+    (dict(out_ptr=None), "null q or out"),
+    (dict(out_ptr=24), "aligned"),
+])
+def test_token_major_entry_checks_like_attn_fwd(lib, change, fragment):
+    args = dict(q_ptr=16, k_ptr=16, v_ptr=16, out_ptr=16, batch=1, q_heads=4, kv_heads=2, q_len=8, kv_len=8,
+                head_dim=64, pos_offset=0, mask_mode=0, window=0, key_lens_ptr=None, scale=0.125,
+                dtype=attn.ATTN_BF16, stream_handle=None)
+    args.update(change)
+    a = list(args.values())
+    a[14] = ctypes.c_float(a[14])
+    assert lib.attn_fwd_out_token_major(*a) == attn.ATTN_ERR_INVALID_ARG
+    assert fragment in attn.last_error()
+
+
 def test_selftest_limit_is_checked(lib):
     assert lib.attn_selftest_timeout(0, None) == attn.ATTN_ERR_INVALID_ARG
     assert lib.attn_selftest_timeout(2_000_000, None) == attn.ATTN_ERR_INVALID_ARG
