@@ -80,6 +80,20 @@ def test_varlen_f16_gqa():
     assert_close(out.double().cpu().numpy(), ref, "f16", "varlen f16")
 
 
+@pytest.mark.parametrize("Hq,Hkv", [(3, 1), (6, 2)])
+def test_varlen_odd_group_head_dim_128(Hq, Hkv):
+    # an odd group size keeps two consecutive row blocks of one head per CTA (an even one
+    # pairs two query heads over the same rows); both layouts are covered for packed rows
+    lens = [260, 1, 129, 400]
+    q, k, v, cu = packed(lens, Hq, Hkv, 128, torch.bfloat16, seed=8150 + Hq)
+    out = attn.attn_fwd_varlen(q.to(DEV), k.to(DEV), v.to(DEV), cu.to(DEV), max(lens), mask_mode=MASK_CAUSAL,
+                               scale=scale_of(128))
+    torch.cuda.synchronize()
+    assert attn.sync_status() == attn.ATTN_OK, attn.last_error()
+    ref = reference(q, k, v, cu, MASK_CAUSAL, 0, scale_of(128))
+    assert_close(out.double().cpu().numpy(), ref, "bf16", f"varlen odd group {Hq}/{Hkv}")
+
+
 def test_varlen_rows_after_the_last_sequence_are_not_written():
     q, k, v, cu = packed([100, 50], 2, 2, 64, torch.bfloat16, seed=8200, extra_rows=30)
     out = torch.full(q.shape, 7.0, dtype=q.dtype, device=DEV)
