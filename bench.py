@@ -19,6 +19,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import re
 import json
 import math
 import os
@@ -46,7 +47,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 
 # DRAM bytes per launch measured by ncu (dram__bytes_read.sum + dram__bytes_write.sum) for a
 # kernel source state; the entry stops applying as soon as the kernel source changes.
-NCU_TRAFFIC = {"538431232122": 460976896.0}  # prefill_tc_kernel<128, 2, bf16, paired heads>: 357.80 MB read + 103.18 MB written
+NCU_TRAFFIC = {"07f11fa938f9": 460976896.0}  # prefill_tc_kernel<128, 2, bf16, paired heads>: 357.80 MB read + 103.18 MB written
 
 
 # ----------------------------------------------------------------------------- distributed plumbing
@@ -240,10 +241,15 @@ def prelude_leg(args, world, dev, peaks, peak_src):
 
 
 def kernel_source_hash() -> str:
+    """Identifies the prefill kernel's code (comments and blank lines do not count), so a
+    DRAM-traffic figure stays attached to the code it was measured on."""
     h = hashlib.sha1()
     for rel in ("head_attention_attn_gb300/csrc/prefill_tc.cu", "head_attention_attn_gb300/csrc/common.cuh"):
-        with open(os.path.join(ROOT, rel), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, rel), encoding="utf-8") as f:
+            text = f.read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", "", text)
+        h.update("\n".join(line.rstrip() for line in text.splitlines() if line.strip()).encode())
     return h.hexdigest()[:12]
 
 

@@ -15,8 +15,12 @@
 //                shared memory at a named barrier of the tile's 8 warps (hardware, no
 //                polling), and each writes its 64 probabilities (2^x on the
 //                special-function unit, scale*log2(e) folded in) back into TMEM as
-//                packed 16-bit pairs (the input type: bf16 or fp16).  After the tile's last key block each half normalises
-//                and stores its half of the head dims of the row.
+//                packed 16-bit pairs (the input type: bf16 or fp16).  After the tile's
+//                last key block each half normalises and stores its half of the head
+//                dims of the row (head-major, token-major or packed rows).
+// With one tile per CTA (head_dim 64, two CTAs per SM), thread 0 issues the Q copy and the
+// first K/V copies before the CTA barrier, and a softmax warp whose 32 rows see none of its
+// 64 key columns skips the mask, the max and the exponentials (it writes zero P).
 // TMEM: S_0 .. S_{NT-1} | O_0 .. O_{NT-1}, 128 columns each; P_t aliases the first 64
 // columns of S_t.  With two tiles the MMA order is the ping-pong
 //   PV0(j-1), QK0(j), PV1(j-1), QK1(j)
