@@ -17,7 +17,7 @@ MASK_NONE, MASK_CAUSAL, MASK_WINDOW, MASK_CAUSAL_WINDOW = 0, 1, 2, 3
 QK_COPY, QK_NORM_ROPE, QK_ROPE, QK_ROPE_INTERLEAVED = 0, 1, 2, 3
 ATTN_BF16, ATTN_F32, ATTN_F16 = 0, 1, 2
 
-EXPORTED = ("attn_fwd", "attn_fwd_out_token_major", "attn_fwd_varlen", "attn_decode_caches", "attn_qkv_prelude", "attn_qkv_prelude_caches", "attn_last_error", "attn_sync_status", "attn_selftest_timeout",
+EXPORTED = ("attn_fwd", "attn_fwd_out_token_major", "attn_fwd_varlen", "attn_decode_caches", "attn_decode_paged", "attn_qkv_prelude", "attn_qkv_prelude_caches", "attn_last_error", "attn_sync_status", "attn_selftest_timeout",
             "attn_version")
 
 _STATUS_NAMES = {0: "ATTN_OK", 1: "ATTN_ERR_INVALID_ARG", 2: "ATTN_ERR_UNSUPPORTED", 3: "ATTN_ERR_CUDA",
@@ -65,6 +65,9 @@ def load(path: str | None = None):
                                                 ctypes.c_float, ci, ci, vp]
         lib.attn_decode_caches.restype = ci
         lib.attn_decode_caches.argtypes = [vp, vp, vp, vp, ci, ci, ci, ci, ci, vp, ci, ctypes.c_float, ci, vp]
+        lib.attn_decode_paged.restype = ci
+        lib.attn_decode_paged.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, ci, vp, ci, ctypes.c_float,
+                                          ci, vp]
         lib.attn_last_error.restype = ctypes.c_char_p
         lib.attn_last_error.argtypes = []
         lib.attn_sync_status.restype = ci
@@ -370,6 +373,48 @@ def attn_decode_caches(q, k_caches, v_caches, kv_lens, out=None, *, sliding_wind
                                        dtype, _stream_handle(stream))
     _check(status)
     out._attn_keepalive = (kp, vp_)  # the pointer arrays must outlive the queued launch
+    return out
+
+
+def attn_decode_paged(q, k_pool, v_pool, page_table, kv_lens, out=None, *, sliding_window: int = 0,
+                      scale: float | None = None, stream=None):
+    """One decode step for m items over paged caches (see attn_decode_paged in attn.h).
+
+    q: [m, Hq, D] bf16 or fp16 CUDA tensor; k_pool, v_pool: [num_pages, Hkv, page_size, D]
+    CUDA tensors of q's dtype; page_table: int32 CUDA [m, max_pages]; kv_lens: int32 CUDA [m].
+    Enqueues on `stream` (default: torch's current stream) and returns out.
+    """
+    import torch
+    if q.dtype == torch.bfloat16:
+        dtype = ATTN_BF16
+    elif q.dtype == torch.float16:
+        dtype = ATTN_F16
+    else:
+        raise ValueError("q must be bf16 or fp16")
+    if not q.is_cuda or q.dim() != 3 or not q.is_contiguous():
+        raise ValueError("q must be a contiguous CUDA tensor [m, Hq, D]")
+    m, Hq, D = q.shape
+    for name, t in (("k_pool", k_pool), ("v_pool", v_pool)):
+        if not t.is_cuda or t.dtype != q.dtype or not t.is_contiguous() or t.dim() != 4 or t.shape[3] != D:
+            raise ValueError(f"{name} must be a contiguous CUDA tensor [num_pages, Hkv, page_size, D] of q's dtype")
+    if tuple(k_pool.shape) != tuple(v_pool.shape):
+        raise ValueError("k_pool and v_pool must share a shape")
+    num_pages, Hkv, page_size, _ = (int(x) for x in k_pool.shape)
+    if page_table.dtype != torch.int32 or not page_table.is_cuda or page_table.dim() != 2 or \
+            page_table.shape[0] != m or not page_table.is_contiguous():
+        raise ValueError("page_table must be a contiguous int32 CUDA tensor [m, max_pages]")
+    max_pages = int(page_table.shape[1])
+    if kv_lens.dtype != torch.int32 or not kv_lens.is_cuda or kv_lens.numel() != m:
+        raise ValueError("kv_lens must be an int32 CUDA tensor with m entries")
+    if out is None:
+        out = torch.empty_like(q)
+    if scale is None:
+        scale = float(torch.tensor(1.0 / math.sqrt(D), dtype=torch.float32).item())
+    status = load().attn_decode_paged(q.data_ptr(), k_pool.data_ptr(), v_pool.data_ptr(), page_table.data_ptr(),
+                                      out.data_ptr(), m, Hq, Hkv, num_pages, page_size, max_pages, D,
+                                      kv_lens.data_ptr(), int(sliding_window), ctypes.c_float(scale), dtype,
+                                      _stream_handle(stream))
+    _check(status)
     return out
 
 

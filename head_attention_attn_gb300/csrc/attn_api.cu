@@ -246,6 +246,55 @@ attn_status attn_decode_caches(const void* q, const void* const* k_caches, const
     return ATTN_OK;
 }
 
+attn_status attn_decode_paged(const void* q, const void* k_pool, const void* v_pool, const int32_t* page_table,
+                              void* out, int m, int q_heads, int kv_heads, int num_pages, int page_size,
+                              int max_pages, int head_dim, const int32_t* kv_lens, int sliding_window, float scale,
+                              int dtype, void* cuda_stream) {
+    t_last_error.clear();
+    if (m < 0 || num_pages < 0 || max_pages < 0)
+        return fail(ATTN_ERR_INVALID_ARG, "negative size (m=%d, num_pages=%d, max_pages=%d)", m, num_pages,
+                    max_pages);
+    if (page_size < 1) return fail(ATTN_ERR_INVALID_ARG, "page_size must be at least 1, not %d", page_size);
+    if ((long long)page_size * max_pages > 0x7fffffffLL)
+        return fail(ATTN_ERR_INVALID_ARG, "max_pages * page_size exceeds 2^31-1");
+    if (q_heads <= 0 || kv_heads <= 0 || head_dim <= 0)
+        return fail(ATTN_ERR_INVALID_ARG, "q_heads, kv_heads and head_dim must be positive (%d, %d, %d)", q_heads,
+                    kv_heads, head_dim);
+    if (q_heads % kv_heads != 0)
+        return fail(ATTN_ERR_INVALID_ARG, "q_heads (%d) is not a multiple of kv_heads (%d)", q_heads, kv_heads);
+    if (sliding_window < 0) return fail(ATTN_ERR_INVALID_ARG, "negative sliding_window %d", sliding_window);
+    if (!isfinite(scale)) return fail(ATTN_ERR_INVALID_ARG, "scale is not finite");
+    if (dtype != ATTN_BF16 && dtype != ATTN_F16)
+        return fail(ATTN_ERR_UNSUPPORTED, "paged caches support bf16 and fp16 only");
+    if (head_dim != 64 && head_dim != 128)
+        return fail(ATTN_ERR_UNSUPPORTED, "bf16 and fp16 support head_dim 64 and 128, not %d", head_dim);
+    const int G = q_heads / kv_heads;
+    if (G != 1 && G != 2 && G != 4 && G != 8)
+        return fail(ATTN_ERR_UNSUPPORTED, "paged caches support 1, 2, 4 or 8 query heads per kv head, not %d", G);
+    if (m > 65535 || kv_heads > 65535) return fail(ATTN_ERR_UNSUPPORTED, "m and kv_heads are limited to 65535");
+    if (m == 0) return ATTN_OK;
+    if (!q || !out || !kv_lens) return fail(ATTN_ERR_INVALID_ARG, "null q, out or kv_lens pointer");
+    cudaStream_t stream = static_cast<cudaStream_t>(cuda_stream);
+    if ((long long)page_size * max_pages == 0) {
+        cudaError_t e = cudaMemsetAsync(out, 0, (size_t)m * q_heads * head_dim * 2, stream);
+        if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "cudaMemsetAsync: %s", cudaGetErrorString(e));
+        return ATTN_OK;
+    }
+    if (!k_pool || !v_pool || !page_table) return fail(ATTN_ERR_INVALID_ARG, "null k_pool, v_pool or page_table pointer");
+    if (!aligned(q, 16) || !aligned(out, 16) || !aligned(k_pool, 16) || !aligned(v_pool, 16) ||
+        !aligned(page_table, 4) || !aligned(kv_lens, 4))
+        return fail(ATTN_ERR_INVALID_ARG, "q, out and the pools must be 16-byte, page_table and kv_lens 4-byte aligned");
+    DeviceState* st = nullptr;
+    attn_status s = device_state(&st);
+    if (s != ATTN_OK) return s;
+    attn::WaitCtl wc{st->status, kWaitLimitNs};
+    attn::PagedProblem p{q, k_pool, v_pool, page_table, out, m, q_heads, kv_heads, num_pages, page_size,
+                         max_pages, head_dim, kv_lens, sliding_window, scale, dtype == ATTN_F16};
+    cudaError_t e = attn::launch_decode_paged(p, wc, stream, st->num_sms);
+    if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "decode_paged launch: %s", cudaGetErrorString(e));
+    return ATTN_OK;
+}
+
 attn_status attn_qkv_prelude(const void* qkv, const float* q_norm_w, const float* k_norm_w, const float* cos,
                              const float* sin, int rope_positions, void* q_out, void* k_out, void* v_out, int tokens,
                              int q_heads, int kv_heads, int head_dim, int pos_offset, float eps, int qk_mode,
@@ -354,6 +403,8 @@ attn_status attn_sync_status(void* cuda_stream) {
         if (word == attn::kStatusTimeout) return fail(ATTN_ERR_TIMEOUT, "a device-side wait timed out");
         if (word == attn::kStatusBadPointer)
             return fail(ATTN_ERR_INVALID_ARG, "a per-item cache pointer is null or not 16-byte aligned");
+        if (word == attn::kStatusBadPage)
+            return fail(ATTN_ERR_INVALID_ARG, "a page-table entry names no page of the pool");
         if (word == attn::kStatusBadSeqlens)
             return fail(ATTN_ERR_INVALID_ARG,
                         "a device-side length is out of range: cu_seqlens not non-decreasing within total and "

@@ -56,6 +56,10 @@ struct DecodeParams {
     int sliding;                      // per-item caches: attend to the last `sliding` keys (0: all)
     float scale_log2;
     WaitCtl wc;
+    // Paged caches (null: not paged): k/v are pools [num_pages, Hkv, page_size, D]; item b's
+    // position j lives in pool page page_table[b * max_pages + j / page_size], row j % page_size.
+    const int32_t* page_table = nullptr;
+    int page_size = 0, max_pages = 0, num_pages = 0;
 };
 
 template <int D, int G>
@@ -144,7 +148,28 @@ __global__ void __launch_bounds__(kThreads, (G == 8) ? 1 : 2) decode_splitkv_ker
     long long lo, hi;
     const __nv_bfloat16* kbase;
     const __nv_bfloat16* vbase;
-    if (p.kc != nullptr) {
+    const int32_t* pages = nullptr;  // paged: this item's row of the page table
+    if (p.page_table != nullptr) {
+        // Paged caches: like per-item caches, with the item's positions spread over pool
+        // pages.  Every CTA of the cluster checks all of the item's visible pages, so they
+        // agree: an item with an entry outside the pool is not read and gets zeros.
+        pages = p.page_table + (size_t)b * p.max_pages;
+        lo = (p.sliding > 0 && klen > p.sliding) ? (long long)(klen - p.sliding) : 0;
+        hi = klen;
+        bool bad = false;
+        if (hi > lo) {
+            for (long long x = lo / p.page_size + threadIdx.x; x <= (hi - 1) / p.page_size; x += blockDim.x) {
+                const int id = __ldg(pages + x);
+                bad |= (id < 0 || id >= p.num_pages);
+            }
+        }
+        if (__syncthreads_or(bad)) {
+            if (threadIdx.x == 0) record_status(p.wc.status, kStatusBadPage);
+            lo = hi = 0;
+        }
+        kbase = p.k;  // pool bases: a chunk's rows are addressed page by page
+        vbase = p.v;
+    } else if (p.kc != nullptr) {
         kbase = p.kc[b];
         vbase = p.vc[b];
         lo = (p.sliding > 0 && klen > p.sliding) ? (long long)(klen - p.sliding) : 0;
@@ -206,8 +231,24 @@ __global__ void __launch_bounds__(kThreads, (G == 8) ? 1 : 2) decode_splitkv_ker
                 const uint32_t dst = ring + st * C::kStageBytes;
                 const uint32_t bar = smem_u32(&s_full[st]);
                 mbar_arrive_expect_tx(bar, 2 * bytes);
-                bulk_load(dst, kbase + k0 * D, bytes, bar);
-                bulk_load(dst + kChunk * C::kRowBytes, vbase + k0 * D, bytes, bar);
+                if (pages != nullptr) {
+                    // the chunk's rows may span pages: one copy per page piece, same bytes in total
+                    uint32_t off = 0;
+                    for (long long a = k0; a < k0 + rows;) {
+                        const long long pg = a / p.page_size;
+                        const long long e = min(k0 + rows, (pg + 1) * (long long)p.page_size);
+                        const size_t src = (((size_t)__ldg(pages + pg) * p.Hkv + hk) * p.page_size +
+                                            (size_t)(a - pg * p.page_size)) * D;
+                        const uint32_t nb = (uint32_t)(e - a) * C::kRowBytes;
+                        bulk_load(dst + off, kbase + src, nb, bar);
+                        bulk_load(dst + kChunk * C::kRowBytes + off, vbase + src, nb, bar);
+                        off += nb;
+                        a = e;
+                    }
+                } else {
+                    bulk_load(dst, kbase + k0 * D, bytes, bar);
+                    bulk_load(dst + kChunk * C::kRowBytes, vbase + k0 * D, bytes, bar);
+                }
                 issued = c + 1;
             }
             // no copy may still be writing shared memory when the block moves on
@@ -589,6 +630,35 @@ cudaError_t launch_decode_splitkv(const Problem& pr, const WaitCtl& wc, cudaStre
     const int nsplit = choose_splits((long long)pr.B * pr.Hkv, pr.Lk, num_sms);
     const int G = pr.Hq / pr.Hkv;
     return launch_any(p, pr.D, pr.f16, G, pr.B, nsplit, stream);
+}
+
+cudaError_t launch_decode_paged(const PagedProblem& pp, const WaitCtl& wc, cudaStream_t stream, int num_sms) {
+    DecodeParams p;
+    p.q = reinterpret_cast<const __nv_bfloat16*>(pp.q);
+    p.k = reinterpret_cast<const __nv_bfloat16*>(pp.k_pool);
+    p.v = reinterpret_cast<const __nv_bfloat16*>(pp.v_pool);
+    p.kc = nullptr;
+    p.vc = nullptr;
+    p.out = reinterpret_cast<__nv_bfloat16*>(pp.out);
+    p.key_lens = pp.kv_lens;
+    p.Hq = pp.Hq;
+    p.Hkv = pp.Hkv;
+    p.Lk = pp.page_size * pp.max_pages;  // the item's capacity: kv_lens clamp to it
+    p.P = 0;
+    p.mode = 0;
+    p.window = 0;
+    p.sliding = pp.sliding;
+    p.scale_log2 = pp.scale * kLog2e;
+    p.wc = wc;
+    p.page_table = pp.page_table;
+    p.page_size = pp.page_size;
+    p.max_pages = pp.max_pages;
+    p.num_pages = pp.num_pages;
+    if (pp.Hkv > 65535 || pp.m > 65535) return cudaErrorInvalidConfiguration;
+    const long long span = pp.sliding > 0 ? std::min(pp.sliding, p.Lk) : p.Lk;
+    const int nsplit = choose_splits((long long)pp.m * pp.Hkv, span, num_sms);
+    const int G = pp.Hq / pp.Hkv;
+    return launch_any(p, pp.D, pp.f16, G, pp.m, nsplit, stream);
 }
 
 cudaError_t launch_decode_caches(const CachesProblem& cp, const WaitCtl& wc, cudaStream_t stream, int num_sms) {

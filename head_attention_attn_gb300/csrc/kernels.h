@@ -85,6 +85,22 @@ struct CachesProblem {
 };
 cudaError_t launch_decode_caches(const CachesProblem& p, const WaitCtl& wc, cudaStream_t stream, int num_sms);
 
+// K2 over paged caches: pools [num_pages, Hkv, page_size, D], item i's position j in pool page
+// page_table[i * max_pages + j / page_size], row j % page_size.
+struct PagedProblem {
+    const void* q;
+    const void* k_pool;
+    const void* v_pool;
+    const int32_t* page_table;  // device [m, max_pages]
+    void* out;
+    int m, Hq, Hkv, num_pages, page_size, max_pages, D;
+    const int32_t* kv_lens;
+    int sliding;
+    float scale;
+    bool f16;
+};
+cudaError_t launch_decode_paged(const PagedProblem& p, const WaitCtl& wc, cudaStream_t stream, int num_sms);
+
 // K4: the attention prelude (split fused QKV, per-head RMS norm, RoPE, head-major
 // transpose, optionally into KV caches), bf16 or fp16, head_dim 64 or 128.
 struct PreludeProblem {

@@ -320,6 +320,49 @@ ATTN_API attn_status attn_decode_caches(const void* q, const void* const* k_cach
                                         void* cuda_stream);
 
 /*
+ * attn_decode_paged -- attn_decode_caches over paged KV caches: every item's cache lives in
+ * fixed-size pages of two shared pools, addressed through a per-item page table.
+ *
+ * Source: the pages name ferrum-kernels' paged decode path (paged_decode_attention over
+ * paged_varlen_attention) without giving its layout.  The reading taken here keeps the
+ * per-item cache form of flash_attention_batched_per_cache, [kv_heads, capacity, head_dim],
+ * and cuts it into pages of page_size positions: a page is [kv_heads, page_size, head_dim].
+ *
+ * Arguments:
+ *   q, out      [m, q_heads, head_dim] bf16 or fp16, item-major, contiguous, 16-byte aligned.
+ *   k_pool, v_pool
+ *               [num_pages, kv_heads, page_size, head_dim] of the same type, contiguous,
+ *               16-byte aligned.
+ *   page_table  Device int32 [m, max_pages]: item i's positions j*page_size .. (j+1)*page_size-1
+ *               are rows 0 .. page_size-1 of pool page page_table[i][j].  Pages may be shared
+ *               between items.  Only the entries of an item's visible positions are read.
+ *   kv_lens     Device int32 [m]: the valid positions of item i, clamped to
+ *               [0, max_pages * page_size].
+ *   sliding_window, scale, dtype
+ *               As attn_decode_caches: item i's query is the newest position kv_lens[i]-1 and
+ *               sees all of its positions, or only the last sliding_window of them.
+ *
+ * Query head h reads kv head h / (q_heads / kv_heads).  The result equals
+ * attn_decode_caches over caches gathered from the pages, bit for bit.
+ *
+ * Supported: as attn_decode_caches (head_dim 64 or 128, q_heads / kv_heads in {1, 2, 4, 8});
+ * page_size >= 1.  An item with kv_lens[i] == 0 gets zeros.  max_pages * page_size == 0
+ * zero-fills out.
+ *
+ * Errors: host-visible arguments are checked as for attn_decode_caches (null or misaligned
+ * pointers, negative sizes, page_size < 1, max_pages * page_size above 2^31-1).  A visible
+ * page-table entry outside [0, num_pages) is found on the device: that item is not read, its
+ * output is zeros, and attn_sync_status() reports ATTN_ERR_INVALID_ARG.
+ *
+ * The library allocates nothing and keeps no pointer after the call.
+ */
+ATTN_API attn_status attn_decode_paged(const void* q, const void* k_pool, const void* v_pool,
+                                       const int32_t* page_table, void* out, int m, int q_heads, int kv_heads,
+                                       int num_pages, int page_size, int max_pages, int head_dim,
+                                       const int32_t* kv_lens, int sliding_window, float scale, int dtype,
+                                       void* cuda_stream);
+
+/*
  * attn_last_error -- message for the last non-OK status returned on this host thread.
  * The string belongs to the library and stays valid until the next call on this
  * thread.  The result is "" when there has been no error.

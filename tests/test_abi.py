@@ -113,6 +113,34 @@ def test_token_major_entry_checks_like_attn_fwd(lib, change, fragment):
     assert fragment in attn.last_error()
 
 
+@pytest.mark.parametrize("change,status", [
+    (dict(m=-1), attn.ATTN_ERR_INVALID_ARG),
+    (dict(num_pages=-1), attn.ATTN_ERR_INVALID_ARG),
+    (dict(page_size=0), attn.ATTN_ERR_INVALID_ARG),
+    (dict(max_pages=1 << 20, page_size=1 << 12), attn.ATTN_ERR_INVALID_ARG),
+    (dict(q_heads=6, kv_heads=4), attn.ATTN_ERR_INVALID_ARG),
+    (dict(q_heads=12, kv_heads=4), attn.ATTN_ERR_UNSUPPORTED),
+    (dict(head_dim=96), attn.ATTN_ERR_UNSUPPORTED),
+    (dict(dtype=attn.ATTN_F32), attn.ATTN_ERR_UNSUPPORTED),
+    (dict(sliding=-1), attn.ATTN_ERR_INVALID_ARG),
+    (dict(scale=float("nan")), attn.ATTN_ERR_INVALID_ARG),
+    (dict(page_table=None), attn.ATTN_ERR_INVALID_ARG),
+    (dict(k_pool=None), attn.ATTN_ERR_INVALID_ARG),
+    (dict(kv_lens=None), attn.ATTN_ERR_INVALID_ARG),
+    (dict(k_pool=24), attn.ATTN_ERR_INVALID_ARG),
+    (dict(page_table=18), attn.ATTN_ERR_INVALID_ARG),
+    (dict(m=0), attn.ATTN_OK),
+])
+def test_decode_paged_arguments(lib, change, status):
+    a = dict(q=16, k_pool=16, v_pool=16, page_table=16, out=16, m=2, q_heads=8, kv_heads=2, num_pages=4,
+             page_size=16, max_pages=4, head_dim=128, kv_lens=16, sliding=0, scale=0.1, dtype=attn.ATTN_BF16)
+    a.update(change)
+    got = lib.attn_decode_paged(a["q"], a["k_pool"], a["v_pool"], a["page_table"], a["out"], a["m"], a["q_heads"],
+                                a["kv_heads"], a["num_pages"], a["page_size"], a["max_pages"], a["head_dim"],
+                                a["kv_lens"], a["sliding"], ctypes.c_float(a["scale"]), a["dtype"], None)
+    assert got == status, attn.last_error()
+
+
 def test_selftest_limit_is_checked(lib):
     assert lib.attn_selftest_timeout(0, None) == attn.ATTN_ERR_INVALID_ARG
     assert lib.attn_selftest_timeout(2_000_000, None) == attn.ATTN_ERR_INVALID_ARG

@@ -1,0 +1,131 @@
+"""Decode over paged KV caches (attn_decode_paged) on the GPU.
+
+Item i's cache is cut into pages of page_size positions, [Hkv, page_size, D] each, held in
+two pools [num_pages, Hkv, page_size, D] and addressed by page_table[i][j] for positions
+j*page_size .. (j+1)*page_size - 1.  Gathering item i's pages back into one [Hkv, capacity, D]
+cache and running attn_decode_caches over it computes the same numbers in the same order, so
+the two agree bit for bit; the gathered caches are also checked against the fp64 oracle.
+"""
+import numpy as np
+import pytest
+import torch
+
+import head_attention_attn_gb300 as attn
+import oracle
+from head_attention_attn_gb300.inputs import MASK_CAUSAL, MASK_CAUSAL_WINDOW
+from parity_util import assert_close
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _library():
+    from head_attention_attn_gb300 import build
+    build.build_library()
+    attn.load()
+    yield
+    assert attn.sync_status() == attn.ATTN_OK, attn.last_error()
+
+
+def paged_case(m, Hq, Hkv, D, page_size, max_pages, num_pages, lens, seed, dtype=torch.bfloat16):
+    g = torch.Generator().manual_seed(seed)
+    q = torch.randn(m, Hq, D, generator=g).to(dtype)
+    k_pool = torch.randn(num_pages, Hkv, page_size, D, generator=g).to(dtype)
+    v_pool = torch.randn(num_pages, Hkv, page_size, D, generator=g).to(dtype)
+    # a random page table (pages may repeat across and within items)
+    table = torch.randint(0, num_pages, (m, max_pages), generator=g, dtype=torch.int32)
+    return q, k_pool, v_pool, table, torch.tensor(lens, dtype=torch.int32)
+
+
+def gathered(pool, table):
+    """[m, Hkv, max_pages * page_size, D] per-item caches assembled from the pool pages."""
+    m, max_pages = table.shape
+    _, Hkv, ps, D = pool.shape
+    x = pool[table.long()]                      # [m, max_pages, Hkv, ps, D]
+    return x.permute(0, 2, 1, 3, 4).reshape(m, Hkv, max_pages * ps, D).contiguous()
+
+
+def reference(q, kc, vc, lens, window, scale):
+    rows = []
+    for i in range(q.shape[0]):
+        n = int(min(max(int(lens[i]), 0), kc.shape[2]))
+        if n == 0:
+            rows.append(np.zeros((q.shape[1], q.shape[2])))
+            continue
+        mode = MASK_CAUSAL_WINDOW if window > 0 else MASK_CAUSAL
+        r = oracle.attention(q[i][None, :, None, :], kc[i][None], vc[i][None], pos_offset=n - 1, mask_mode=mode,
+                             window=window, key_lens=[n], scale=scale)
+        rows.append(r[0, :, 0, :])
+    return np.stack(rows)
+
+
+def run_both(q, k_pool, v_pool, table, kl, window):
+    scale = float(torch.tensor(1.0 / q.shape[2] ** 0.5, dtype=torch.float32))
+    qd, kp, vp, td, kld = q.to(DEV), k_pool.to(DEV), v_pool.to(DEV), table.to(DEV), kl.to(DEV)
+    paged = attn.attn_decode_paged(qd, kp, vp, td, kld, sliding_window=window, scale=scale)
+    kc, vc = gathered(kp, td), gathered(vp, td)
+    cont = attn.attn_decode_caches(qd, list(kc), list(vc), kld, sliding_window=window, scale=scale)
+    torch.cuda.synchronize()
+    assert attn.sync_status() == attn.ATTN_OK, attn.last_error()
+    return paged, cont, kc.cpu(), vc.cpu(), scale
+
+
+@pytest.mark.parametrize("D,G", [(128, 4), (128, 1), (64, 8), (64, 2)])
+@pytest.mark.parametrize("page_size,window", [(16, 0), (48, 300), (100, 0), (1, 0), (2048, 64)])
+def test_paged_equals_gathered_caches(D, G, page_size, window):
+    Hkv, m = 2, 4
+    max_pages = max(1, 1500 // page_size) if page_size > 1 else 300
+    cap = max_pages * page_size
+    lens = [1, cap // 3, cap, cap + 500]  # the last clamps to the capacity
+    q, kp, vp, table, kl = paged_case(m, G * Hkv, Hkv, D, page_size, max_pages, 2 * max_pages + 3, lens,
+                                      seed=31 * D + G + page_size + window)
+    paged, cont, kc, vc, scale = run_both(q, kp, vp, table, kl, window)
+    assert torch.equal(paged, cont)
+    ref = reference(q, kc, vc, kl, window, scale)
+    assert_close(paged.double().cpu().numpy(), ref, "bf16", f"paged D={D} G={G} ps={page_size} w={window}")
+
+
+def test_paged_f16_against_oracle():
+    q, kp, vp, table, kl = paged_case(3, 8, 2, 128, 64, 20, 50, [1000, 17, 1280], seed=77, dtype=torch.float16)
+    paged, cont, kc, vc, scale = run_both(q, kp, vp, table, kl, 0)
+    assert torch.equal(paged, cont)
+    ref = reference(q, kc, vc, kl, 0, scale)
+    assert_close(paged.double().cpu().numpy(), ref, "f16", "paged f16")
+
+
+def test_bad_page_entry_is_reported_and_that_item_zeroed():
+    q, kp, vp, table, kl = paged_case(3, 4, 2, 64, 32, 8, 10, [200, 200, 200], seed=78)
+    table[1, 3] = 10  # one past the pool: item 1 sees positions up to 199, page 3 is visible
+    table[2, 7] = -1  # outside item 2's visible positions (pages 0..6): never read, no error
+    scale = float(torch.tensor(1.0 / 8.0, dtype=torch.float32))
+    out = attn.attn_decode_paged(q.to(DEV), kp.to(DEV), vp.to(DEV), table.to(DEV), kl.to(DEV), scale=scale)
+    torch.cuda.synchronize()
+    assert attn.sync_status() == attn.ATTN_ERR_INVALID_ARG
+    assert "page" in attn.last_error()
+    assert attn.sync_status() == attn.ATTN_OK
+    assert torch.all(out[1] == 0)
+    good = table.clone()
+    good[1, 3] = 0
+    kc, vc = gathered(kp, good), gathered(vp, good)
+    ref = reference(q, kc, vc, kl, 0, scale)
+    assert_close(out[[0, 2]].double().cpu().numpy(), ref[[0, 2]], "bf16", "paged, good items")
+
+
+def test_zero_lengths_give_zeros():
+    q, kp, vp, table, kl = paged_case(2, 4, 4, 128, 16, 4, 4, [0, 0], seed=79)
+    out = torch.full_like(q, 3.0).to(DEV)
+    attn.attn_decode_paged(q.to(DEV), kp.to(DEV), vp.to(DEV), table.to(DEV), kl.to(DEV), out)
+    torch.cuda.synchronize()
+    assert attn.sync_status() == attn.ATTN_OK, attn.last_error()
+    assert torch.all(out == 0)
+
+
+def test_zero_capacity_zero_fills():
+    q, kp, vp, _, kl = paged_case(2, 4, 4, 128, 16, 4, 4, [5, 9], seed=80)
+    table = torch.zeros((2, 0), dtype=torch.int32, device=DEV)  # max_pages 0
+    out = torch.full_like(q, 3.0).to(DEV)
+    attn.attn_decode_paged(q.to(DEV), kp.to(DEV), vp.to(DEV), table, kl.to(DEV), out)
+    torch.cuda.synchronize()
+    assert attn.sync_status() == attn.ATTN_OK, attn.last_error()
+    assert torch.all(out == 0)
