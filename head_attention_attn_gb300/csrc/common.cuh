@@ -17,7 +17,6 @@ namespace attn {
 constexpr unsigned kStatusTimeout = 4u;
 constexpr unsigned kStatusBadPointer = 5u;  // a device-side pointer argument was null or misaligned
 constexpr unsigned kStatusBadSeqlens = 6u;  // cu_seqlens is not a prefix sum within total and max_seqlen
-constexpr unsigned kStatusBadPage = 7u;     // a page-table entry names no page of the pool
 
 // Arguments every kernel receives for its bounded waits.
 struct WaitCtl {

@@ -9,6 +9,10 @@
 
 namespace attn {
 
+// Status code of the paged decode (with those in common.cuh): a page-table entry names no
+// page of the pool.
+constexpr unsigned kStatusBadPage = 7u;
+
 // One validated attention problem (see attn.h for argument meaning).
 struct Problem {
     const void* q;
