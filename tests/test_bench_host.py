@@ -78,3 +78,22 @@ def test_two_rank_aggregation_on_gloo():
         assert p.exitcode == 0
     res = sorted(q.get(timeout=10) for _ in range(world))
     assert res == [(0, 1.5, 3.0), (1, 1.5, 3.0)]
+
+
+def test_kernel_hash_follows_code_not_comments(tmp_path, monkeypatch):
+    # the DRAM-traffic figure is keyed by this hash: a comment edit keeps it, a code edit drops it
+    import shutil
+    src = os.path.join(bench.ROOT, "head_attention_attn_gb300", "csrc")
+    dst = tmp_path / "head_attention_attn_gb300" / "csrc"
+    dst.mkdir(parents=True)
+    for name in ("prefill_tc.cu", "common.cuh"):
+        shutil.copy(os.path.join(src, name), dst / name)
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    h0 = bench.kernel_source_hash()
+    assert h0 == bench.kernel_source_hash()
+    with open(dst / "prefill_tc.cu", "a") as f:
+        f.write("\n// a comment\n/* and a block\n   comment */\n\n")
+    assert bench.kernel_source_hash() == h0
+    with open(dst / "common.cuh", "a") as f:
+        f.write("\nconstexpr int kUnused = 1;\n")
+    assert bench.kernel_source_hash() != h0
