@@ -240,16 +240,26 @@ def prelude_leg(args, world, dev, peaks, peak_src):
             "l2": f"inputs {qkv.numel() * 2 / 1e6:.0f} MB > {L2_BYTES / 1e6:.0f} MB L2, no flush"}
 
 
-def kernel_source_hash() -> str:
-    """Identifies the prefill kernel's code (comments and blank lines do not count), so a
-    DRAM-traffic figure stays attached to the code it was measured on."""
+KERNEL_SOURCES = {
+    "prefill": ("head_attention_attn_gb300/csrc/prefill_tc.cu",),
+    "decode_tc": ("head_attention_attn_gb300/csrc/decode_tc.cu",),
+}
+SHARED_SOURCES = ("head_attention_attn_gb300/csrc/common.cuh", "head_attention_attn_gb300/csrc/kernels.h")
+
+
+def kernel_source_hash(kernel: str = "prefill") -> str:
+    """Identifies a kernel's code: its source, the shared device headers and the nvcc flags
+    (comments and blank lines do not count), so a DRAM-traffic figure stays attached to the
+    code it was measured on."""
+    from head_attention_attn_gb300 import build as _build
     h = hashlib.sha1()
-    for rel in ("head_attention_attn_gb300/csrc/prefill_tc.cu", "head_attention_attn_gb300/csrc/common.cuh"):
+    for rel in KERNEL_SOURCES[kernel] + SHARED_SOURCES:
         with open(os.path.join(ROOT, rel), encoding="utf-8") as f:
             text = f.read()
         text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
         text = re.sub(r"//[^\n]*", "", text)
         h.update("\n".join(line.rstrip() for line in text.splitlines() if line.strip()).encode())
+    h.update(" ".join(_build.ARCH_FLAGS + _build.NVCC_FLAGS).encode())
     return h.hexdigest()[:12]
 
 
@@ -309,7 +319,7 @@ def run_ours(args, rank, world, local):
     value = tflops * world  # replicas: every rank processes one full workload per step
     roof = {"bound": "tensor", "achieved": round(tflops, 2), "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
             "frac": round(tflops / peaks["bf16_tflops"], 4), "peak_source": f"{peak_src} bf16 dense (burst)",
-            "traffic": NCU_TRAFFIC.get(kernel_source_hash()), "kernel": "prefill_tc_kernel<128, 2 tiles, bf16>",
+            "traffic": NCU_TRAFFIC.get(kernel_source_hash("prefill")), "kernel": "prefill_tc_kernel<128, 2 tiles, bf16>",
             "algorithmic_flops_per_launch": flops}
 
     # ---- end to end through the public call with pinned host buffers: every step copies its

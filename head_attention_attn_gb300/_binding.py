@@ -318,6 +318,32 @@ def attn_qkv_prelude_caches(qkv, k_caches, v_caches, cache_lens, q_heads: int, k
     return q_out
 
 
+def _check_kv_lens(kv_lens, m: int):
+    """kv_lens must be m contiguous int32 values on the device (the kernels index it flat)."""
+    import torch
+    if not isinstance(kv_lens, torch.Tensor) or kv_lens.dtype != torch.int32 or kv_lens.numel() != m:
+        raise ValueError("kv_lens must be an int32 tensor with m entries")
+    if not kv_lens.is_contiguous():
+        raise ValueError("kv_lens must be contiguous")
+    if not kv_lens.is_cuda:
+        raise ValueError("kv_lens must be a CUDA tensor")
+
+
+def _decode_out(q, out):
+    """The output of a per-item decode: a new tensor like q, or a checked caller tensor
+    (the kernels write m * Hq * D contiguous elements of q's type)."""
+    import torch
+    if out is None:
+        return torch.empty_like(q)
+    if not isinstance(out, torch.Tensor) or tuple(out.shape) != tuple(q.shape) or out.dtype != q.dtype:
+        raise ValueError(f"out must have shape {tuple(q.shape)} and q's dtype {q.dtype}")
+    if not out.is_contiguous():
+        raise ValueError("out must be contiguous")
+    if not out.is_cuda:
+        raise ValueError("out must be a CUDA tensor")
+    return out
+
+
 def attn_decode_caches(q, k_caches, v_caches, kv_lens, out=None, *, sliding_window: int = 0,
                        scale: float | None = None, stream=None, kv_heads: int | None = None,
                        capacity: int | None = None):
@@ -362,10 +388,8 @@ def attn_decode_caches(q, k_caches, v_caches, kv_lens, out=None, *, sliding_wind
     if len(kshape) != 3 or kshape != vshape or kshape[2] != D:
         raise ValueError("k and v caches must share a shape [Hkv, capacity, D] matching q")
     Hkv, cap = int(kshape[0]), int(kshape[1])
-    if kv_lens.dtype != torch.int32 or not kv_lens.is_cuda or kv_lens.numel() != m:
-        raise ValueError("kv_lens must be an int32 CUDA tensor with m entries")
-    if out is None:
-        out = torch.empty_like(q)
+    _check_kv_lens(kv_lens, m)
+    out = _decode_out(q, out)
     if scale is None:
         scale = float(torch.tensor(1.0 / math.sqrt(D), dtype=torch.float32).item())
     status = load().attn_decode_caches(q.data_ptr(), kp.data_ptr(), vp_.data_ptr(), out.data_ptr(), m, Hq, Hkv,
@@ -404,10 +428,8 @@ def attn_decode_paged(q, k_pool, v_pool, page_table, kv_lens, out=None, *, slidi
             page_table.shape[0] != m or not page_table.is_contiguous():
         raise ValueError("page_table must be a contiguous int32 CUDA tensor [m, max_pages]")
     max_pages = int(page_table.shape[1])
-    if kv_lens.dtype != torch.int32 or not kv_lens.is_cuda or kv_lens.numel() != m:
-        raise ValueError("kv_lens must be an int32 CUDA tensor with m entries")
-    if out is None:
-        out = torch.empty_like(q)
+    _check_kv_lens(kv_lens, m)
+    out = _decode_out(q, out)
     if scale is None:
         scale = float(torch.tensor(1.0 / math.sqrt(D), dtype=torch.float32).item())
     status = load().attn_decode_paged(q.data_ptr(), k_pool.data_ptr(), v_pool.data_ptr(), page_table.data_ptr(),

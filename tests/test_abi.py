@@ -285,3 +285,27 @@ def _prelude_caches_call(lib, **kw):
 ])
 def test_prelude_caches_arguments(lib, change, status):
     assert _prelude_caches_call(lib, **change) == status
+
+
+def test_per_item_decode_wrappers_check_out_and_kv_lens():
+    """A caller's out and kv_lens are checked before the library sees them: the kernels
+    write m * Hq * D contiguous elements of q's type and read m contiguous lengths."""
+    import torch
+    from head_attention_attn_gb300._binding import _check_kv_lens, _decode_out
+    q = torch.zeros(3, 4, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="shape"):
+        _decode_out(q, torch.zeros(3, 4, 32, dtype=torch.bfloat16))
+    with pytest.raises(ValueError, match="shape"):
+        _decode_out(q, torch.zeros(3, 4, 64, dtype=torch.float16))
+    with pytest.raises(ValueError, match="contiguous"):
+        _decode_out(q, torch.zeros(3, 64, 4, dtype=torch.bfloat16).transpose(1, 2))
+    with pytest.raises(ValueError, match="CUDA"):
+        _decode_out(q, torch.zeros(3, 4, 64, dtype=torch.bfloat16))
+    with pytest.raises(ValueError, match="m entries"):
+        _check_kv_lens(torch.zeros(2, dtype=torch.int32), 3)
+    with pytest.raises(ValueError, match="m entries"):
+        _check_kv_lens(torch.zeros(3, dtype=torch.int64), 3)
+    with pytest.raises(ValueError, match="contiguous"):
+        _check_kv_lens(torch.zeros(6, dtype=torch.int32)[::2], 3)
+    with pytest.raises(ValueError, match="CUDA"):
+        _check_kv_lens(torch.zeros(3, dtype=torch.int32), 3)

@@ -81,19 +81,30 @@ def test_two_rank_aggregation_on_gloo():
 
 
 def test_kernel_hash_follows_code_not_comments(tmp_path, monkeypatch):
-    # the DRAM-traffic figure is keyed by this hash: a comment edit keeps it, a code edit drops it
+    # the DRAM-traffic figure is keyed by this hash: a comment edit keeps it, a code edit in the
+    # kernel, in the shared headers (kernels.h decides which key tiles a CTA visits) or in the
+    # compile flags drops it
     import shutil
+    from head_attention_attn_gb300 import build as _build
     src = os.path.join(bench.ROOT, "head_attention_attn_gb300", "csrc")
     dst = tmp_path / "head_attention_attn_gb300" / "csrc"
     dst.mkdir(parents=True)
-    for name in ("prefill_tc.cu", "common.cuh"):
+    for name in ("prefill_tc.cu", "decode_tc.cu", "common.cuh", "kernels.h"):
         shutil.copy(os.path.join(src, name), dst / name)
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
     h0 = bench.kernel_source_hash()
-    assert h0 == bench.kernel_source_hash()
+    assert h0 == bench.kernel_source_hash("prefill")
+    assert h0 != bench.kernel_source_hash("decode_tc")
     with open(dst / "prefill_tc.cu", "a") as f:
         f.write("\n// a comment\n/* and a block\n   comment */\n\n")
     assert bench.kernel_source_hash() == h0
+    with open(dst / "kernels.h", "a") as f:
+        f.write("\nconstexpr int kUnusedInKernels = 1;\n")
+    h1 = bench.kernel_source_hash()
+    assert h1 != h0
     with open(dst / "common.cuh", "a") as f:
         f.write("\nconstexpr int kUnused = 1;\n")
-    assert bench.kernel_source_hash() != h0
+    h2 = bench.kernel_source_hash()
+    assert h2 != h1
+    monkeypatch.setattr(_build, "NVCC_FLAGS", _build.NVCC_FLAGS + ["-DSOMETHING"])
+    assert bench.kernel_source_hash() != h2
