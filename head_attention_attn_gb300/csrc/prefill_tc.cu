@@ -81,7 +81,8 @@ enum : int {
     kBarPFull = kBarSFull + kTiles,    // + tile
     kBarOFull = kBarPFull + kTiles,    // + tile: the tile's last P V product completed
     kBarMmaDone = kBarOFull + kTiles,
-    kNumBars = kBarMmaDone + 1,
+    kBarVLand = kBarMmaDone + 1,       // the tail V tile's copy, before its invisible rows are zeroed
+    kNumBars = kBarVLand + 1,
 };
 static_assert(kNumBars * 8 <= 240, "barrier area");
 
@@ -235,6 +236,19 @@ __global__ void __launch_bounds__(threads_for<NT>(), 3 - NT)
         }
     }
     if (kv0 < 0) kv0 = 0;
+    // Rows of the last key tile past every visible key of this CTA's queries get weight 0, and
+    // the tensor core multiplies that 0 into the V row: an Inf or NaN there would still make
+    // the product NaN.  Such rows of the tail V tile are zeroed in shared memory before its P V
+    // products (rows past the tensor already read as zeros from the copy).
+    long long hi_all = 0;
+#pragma unroll
+    for (int t = 0; t < kTiles; ++t)
+        if (thi[t] > tlo[t] && thi[t] > hi_all) hi_all = thi[t];
+    const long long tail_row = kv0 + (long long)(ntiles - 1) * BN;
+    const long long row_limit = TOK ? (long long)p.total - row0 : (long long)Lk;
+    const int zero_lo = (int)(hi_all - tail_row);
+    const int zero_hi = (int)min((long long)BN, row_limit - tail_row);
+    const bool zero_tail = ntiles > 0 && zero_hi > zero_lo;
 
     const int kbh = b * p.Hkv + hk;
     auto load_q = [&]() {
@@ -251,9 +265,12 @@ __global__ void __launch_bounds__(threads_for<NT>(), 3 - NT)
     auto load_kv = [&](const CUtensorMap* map, int off, int bar, int j) {
         const int s = j % kStages;
         const int krow = (int)kv0 + j * BN;
-        mbar_arrive_expect_tx(bar0 + 8 * (bar + s), C::kKVBytes);
+        // the tail V tile lands on its own barrier when some of its rows must be zeroed first
+        const uint32_t done = (zero_tail && bar == kBarVFull && j == ntiles - 1) ? bar0 + 8 * kBarVLand
+                                                                                   : bar0 + 8 * (bar + s);
+        mbar_arrive_expect_tx(done, C::kKVBytes);
         for (int c = 0; c < C::kChunks; ++c)
-            tma_load_3d(sbase + off + s * C::kKVBytes + c * (BN * 128), map, bar0 + 8 * (bar + s), c * 64,
+            tma_load_3d(sbase + off + s * C::kKVBytes + c * (BN * 128), map, done, c * 64,
                         TOK ? hk : krow, TOK ? row0 + krow : kbh);
     };
     // With one tile per CTA (two CTAs per SM) the first copies go out before the CTA
@@ -296,9 +313,9 @@ __global__ void __launch_bounds__(threads_for<NT>(), 3 - NT)
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
+        int issued = 2 * nearly;  // K and V copies issued so far (kept by lane 0)
         if (lane == 0 && ntiles > 0) {
             if (kTiles == 2) load_q();
-            int issued = 2 * nearly;  // K/V copies issued at entry
             for (int j = nearly; j < ntiles; ++j) {
                 const int s = j % kStages;
                 const uint32_t n = (uint32_t)(j / kStages);
@@ -316,7 +333,28 @@ __global__ void __launch_bounds__(threads_for<NT>(), 3 - NT)
             for (int j = (nk > kStages ? nk - kStages : 0); j < nk; ++j)
                 drain_wait(bar0 + 8 * (kBarKFull + j % kStages), (uint32_t)(j / kStages) & 1, p.wc);
             for (int j = (nv > kStages ? nv - kStages : 0); j < nv; ++j)
-                drain_wait(bar0 + 8 * (kBarVFull + j % kStages), (uint32_t)(j / kStages) & 1, p.wc);
+                if (!(zero_tail && j == ntiles - 1))  // the tail tile is waited for below
+                    drain_wait(bar0 + 8 * (kBarVFull + j % kStages), (uint32_t)(j / kStages) & 1, p.wc);
+        }
+        // The tail V tile: once it has landed, the whole warp zeroes its rows [zero_lo, zero_hi)
+        // (a row is 128 bytes per 64-column chunk, whatever the swizzle does inside it), makes the
+        // stores visible to the tensor core and releases the tile to the MMA issuer.
+        if (zero_tail && __shfl_sync(0xffffffffu, issued, 0) >= 2 * ntiles) {
+            const bool landed = __all_sync(0xffffffffu, mbar_wait(bar0 + 8 * kBarVLand, 0, p.wc, abort_flag));
+            if (landed) {
+                const int s = (ntiles - 1) % kStages;
+                uint8_t* vt = smem + C::kOffV + s * C::kKVBytes;
+                const int units = (zero_hi - zero_lo) * C::kChunks * 8;  // 16-byte stores
+                for (int u = lane; u < units; u += 32) {
+                    const int r = zero_lo + u / (C::kChunks * 8), c = (u / 8) % C::kChunks, q = u & 7;
+                    *reinterpret_cast<uint4*>(vt + c * (BN * 128) + r * 128 + q * 16) = make_uint4(0u, 0u, 0u, 0u);
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar0 + 8 * (kBarVFull + s));
+            } else if (lane == 0) {
+                drain_wait(bar0 + 8 * kBarVLand, 0, p.wc);  // gave up: the copy may still be in flight
+            }
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer

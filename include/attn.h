@@ -110,9 +110,15 @@ typedef enum { ATTN_BF16 = 0, ATTN_F32 = 1, ATTN_F16 = 2 } attn_dtype;
  *
  * Ownership and lifetime.  The library keeps no pointer after the call returns,
  * and allocates no device memory.  The buffers must stay valid until the stream
- * work completes.  out must not alias q, k or v.  Key and value rows that are
- * masked out must still hold finite numbers: a masked key gets weight exactly 0,
- * but the tensor-core product 0 * V of an Inf or NaN value row is NaN.
+ * work completes.  out must not alias q, k or v.
+ *
+ * Non-finite values.  Key and value rows that no query of the call can see (rows at
+ * or past key_lens[b], and rows outside every query's mask band, e.g. cache rows
+ * past pos_offset + q_len - 1 under a causal mask) never influence out, whatever
+ * they hold: the kernels zero such value rows in shared memory before the
+ * tensor-core product, since 0 * Inf and 0 * NaN are NaN there.  A row that some
+ * query sees takes part in the products of its neighbours' rows with weight 0, so
+ * an Inf or NaN in it also reaches rows that do not see it.
  *
  * Errors.  Arguments are checked before any launch:
  *   - null pointers, negative sizes, q_heads % kv_heads != 0, a mask_mode or dtype
@@ -373,12 +379,26 @@ ATTN_API const char* attn_last_error(void);
  * attn_sync_status -- wait for cuda_stream, then read and clear the library's
  * device status word on the current device.
  *
- * Every device-side wait in the kernels is bounded.  A wait that gives up
- * records a code in this word, releases what it holds, and exits its block.
+ * Every wait of a kernel on a shared-memory barrier (data arriving, the tensor
+ * core finishing, another warp's result) is bounded: it gives up after 2 s, or
+ * after 1 ms once another block has recorded a time-out.  A wait that gives up
+ * records a code in this word, waits (again bounded) for its own copies and
+ * products in flight, releases its tensor memory and exits its block.  The
+ * hardware barriers (a block's __syncthreads, the decode kernels' cluster
+ * barrier, and the prefill kernel's barrier between the two halves of a row) are
+ * not bounded; every thread meets each of them on every path, including a path
+ * that gave up.
+ *
+ * The word is one per device, shared by every call and every stream on it; the
+ * first code recorded wins until this call clears it.  This call synchronises only
+ * cuda_stream: a caller that uses several streams should synchronise all of them
+ * (or the device) before it trusts the code, which may come from a kernel on any
+ * of them.
+ *
  * Returns:
  *   - ATTN_ERR_TIMEOUT when a wait gave up;
- *   - ATTN_ERR_INVALID_ARG when a kernel found a bad device-side pointer
- *     (attn_decode_caches);
+ *   - ATTN_ERR_INVALID_ARG when a kernel found a bad device-side argument
+ *     (a per-item cache pointer, a page-table entry, cu_seqlens or a cache length);
  *   - ATTN_ERR_CUDA when the stream reported an error;
  *   - ATTN_OK otherwise.
  * Source: ferrum-kernels Backend::sync, where sync is separate from the launch.

@@ -44,6 +44,23 @@ def assert_close(got, ref, dtype: str, what: str = ""):
     return max_abs, rel_l2
 
 
+def assert_close_per_head(got, ref, dtype: str, what: str = ""):
+    """assert_close over the whole output, then the relative-L2 bound again on every (batch,
+    head) slab [..., L, D], so that a fault confined to a few CTAs cannot hide in the norm of
+    a large tensor (max-abs is already element by element)."""
+    res = assert_close(got, ref, dtype, what)
+    g = np.asarray(got, dtype=np.float64).reshape(-1, got.shape[-2] * got.shape[-1])
+    r = np.asarray(ref, dtype=np.float64).reshape(-1, ref.shape[-2] * ref.shape[-1])
+    bound = {"f16": F16_REL_L2, "bf16": BF16_REL_L2}.get(dtype)
+    if bound is not None:
+        num = np.linalg.norm(g - r, axis=1)
+        den = np.linalg.norm(r, axis=1)
+        rel = np.where(den > 0, num / np.maximum(den, 1e-300), num)
+        worst = int(np.argmax(rel))
+        assert rel[worst] <= bound, f"{what}: slab {worst} rel-L2 {rel[worst]:.3e} > {bound}"
+    return res
+
+
 def oracle_rows(q, k, v, rows, *, key_lens=None, **kw):
     """Oracle output for flat rows (b*Hq + h)*Lq + i of a possibly huge problem.
 
