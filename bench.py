@@ -247,6 +247,72 @@ KERNEL_SOURCES = {
 SHARED_SOURCES = ("head_attention_attn_gb300/csrc/common.cuh", "head_attention_attn_gb300/csrc/kernels.h")
 
 
+def decode_forms_leg(args, world, dev, peaks, peak_src, dec_bytes):
+    """GB/s of attn_decode_caches and attn_decode_paged at the decode workload's shape: 64 items,
+    8 kv heads, 8192 cached positions each, head_dim 128, bf16, device kv_lens, with 32 query heads
+    (as the workload) and with 64.  Every launch reads the same 2.15 GB of K and V as the
+    contiguous decode, plus its Q and O."""
+    import head_attention_attn_gb300 as attn
+    c = WORKLOADS[DECODE]
+    m, Hkv, cap, D = c.B, c.Hkv, c.Lk, c.D
+    kv_bytes = 2.0 * m * Hkv * cap * D * 2
+    kv_lens = torch.full((m,), cap, dtype=torch.int32, device=dev)
+    scale = float(torch.tensor(1.0 / math.sqrt(D), dtype=torch.float32))
+    steps = max(3, min(args.steps, 300))
+    legs = []
+    torch.cuda.manual_seed(1006)
+
+    def leg(name, call, kernel, Hq):
+        nbytes = kv_bytes + 2.0 * m * Hq * D * 2
+        sec = time_device(call, steps, args.warmup, world, dev)
+        if attn.sync_status() != attn.ATTN_OK:
+            raise RuntimeError(f"device status after {name}: " + attn.last_error())
+        gbs = nbytes / sec / 1e9
+        legs.append({"workload": name, "value": round(gbs * world, 1), "unit": "GB/s", "steps": steps,
+                     "ms_per_step": round(sec * 1e3, 4),
+                     "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                  "frac": round(gbs / peaks["hbm_gbs"], 4), "peak_source": f"{peak_src} HBM copy",
+                                  "traffic": None, "kernel": kernel, "algorithmic_bytes_per_launch": nbytes},
+                     "l2": f"inputs {nbytes / 1e6:.0f} MB > {L2_BYTES / 1e6:.0f} MB L2, no flush"})
+
+    # per-item caches [Hkv, capacity, D], one allocation each, through device pointer arrays
+    ks = [torch.empty(Hkv, cap, D, dtype=torch.bfloat16, device=dev).normal_() for _ in range(m)]
+    vs = [torch.empty(Hkv, cap, D, dtype=torch.bfloat16, device=dev).normal_() for _ in range(m)]
+    kp = torch.tensor([t.data_ptr() for t in ks], dtype=torch.int64, device=dev)
+    vp = torch.tensor([t.data_ptr() for t in vs], dtype=torch.int64, device=dev)
+    for Hq, kernel in ((32, "decode_splitkv_kernel<128, G4, bf16> (per-item caches)"),
+                       (64, "decode_tc_kernel<G8, bf16, per-item caches> (row gather)")):
+        q = torch.empty(m, Hq, D, dtype=torch.bfloat16, device=dev).normal_()
+        out = torch.empty_like(q)
+        leg(f"decode_caches_bf16_{m}x{Hq}q{Hkv}kv_{cap}x{D}",
+            lambda q=q, out=out: attn.attn_decode_caches(q, kp, vp, kv_lens, out, scale=scale, kv_heads=Hkv,
+                                                         capacity=cap),
+            kernel, Hq)
+    del ks, vs, kp, vp
+    torch.cuda.empty_cache()
+
+    # paged: pools [num_pages, Hkv, page_size, D] and a shuffled page table
+    g = torch.Generator().manual_seed(1007)
+    for ps, Hq, kernel in ((16, 32, "decode_splitkv_kernel<128, G4, bf16> (paged, bulk copy per page piece)"),
+                           (16, 64, "decode_tc_kernel<G8, bf16, paged> (TMA per page)"),
+                           (128, 32, "decode_tc_kernel<G4, bf16, paged> (TMA per page)"),
+                           (1, 32, "decode_splitkv_kernel<128, G4, bf16> (paged, bulk copy per page piece)")):
+        max_pages = cap // ps
+        num_pages = m * max_pages
+        k_pool = torch.empty(num_pages, Hkv, ps, D, dtype=torch.bfloat16, device=dev).normal_()
+        v_pool = torch.empty_like(k_pool).normal_()
+        table = torch.randperm(num_pages, generator=g).to(torch.int32).view(m, max_pages).to(dev)
+        q = torch.empty(m, Hq, D, dtype=torch.bfloat16, device=dev).normal_()
+        out = torch.empty_like(q)
+        leg(f"decode_paged_bf16_{m}x{Hq}q{Hkv}kv_{cap}x{D}_page{ps}",
+            lambda q=q, out=out, k_pool=k_pool, v_pool=v_pool, table=table:
+                attn.attn_decode_paged(q, k_pool, v_pool, table, kv_lens, out, scale=scale),
+            kernel, Hq)
+        del k_pool, v_pool, table
+        torch.cuda.empty_cache()
+    return legs
+
+
 def kernel_source_hash(kernel: str = "prefill") -> str:
     """Identifies a kernel's code: its source, the shared device headers and the nvcc flags
     (comments and blank lines do not count), so a DRAM-traffic figure stays attached to the
@@ -403,6 +469,10 @@ def run_ours(args, rank, world, local):
     del host_d, devt_d
     torch.cuda.empty_cache()
 
+    # ---- per-item and paged caches at the decode workload's shape (ferrum-kernels
+    # flash_attention_batched_per_cache): the same K/V bytes, addressed by the device
+    decode_forms = decode_forms_leg(args, world, dev, peaks, peak_src, dec_bytes)
+
     # ---- attention prelude leg: split fused QKV + QK RMS norm + RoPE + head-major transpose for
     # the headline workload's 4 x 4096 tokens (32 q / 8 kv heads, head_dim 128, bf16)
     prelude = prelude_leg(args, world, dev, peaks, peak_src)
@@ -446,7 +516,7 @@ def run_ours(args, rank, world, local):
                    "l2": f"inputs {bytes_of(c) / 1e6:.0f} MB > {L2_BYTES / 1e6:.0f} MB L2, no flush",
                    "parallelism": f"replicas x{world}"},
         "roofline": roof, "e2e": e2e, "gpu_launches": args.steps, "clocks": clocks, "decode": decode,
-        "prelude": prelude, "per_config": per_config,
+        "decode_forms": decode_forms, "prelude": prelude, "per_config": per_config,
     }
     if rank == 0 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(args.cpu_seconds)

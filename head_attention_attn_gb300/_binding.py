@@ -17,8 +17,9 @@ MASK_NONE, MASK_CAUSAL, MASK_WINDOW, MASK_CAUSAL_WINDOW = 0, 1, 2, 3
 QK_COPY, QK_NORM_ROPE, QK_ROPE, QK_ROPE_INTERLEAVED = 0, 1, 2, 3
 ATTN_BF16, ATTN_F32, ATTN_F16 = 0, 1, 2
 
-EXPORTED = ("attn_fwd", "attn_fwd_out_token_major", "attn_fwd_varlen", "attn_decode_caches", "attn_decode_paged", "attn_qkv_prelude", "attn_qkv_prelude_caches", "attn_last_error", "attn_sync_status", "attn_selftest_timeout",
-            "attn_version")
+EXPORTED = ("attn_fwd", "attn_fwd_out_token_major", "attn_fwd_varlen", "attn_fwd_varlen_paged", "attn_decode_caches",
+            "attn_decode_paged", "attn_qkv_prelude", "attn_qkv_prelude_caches", "attn_last_error", "attn_sync_status",
+            "attn_selftest_timeout", "attn_version")
 
 _STATUS_NAMES = {0: "ATTN_OK", 1: "ATTN_ERR_INVALID_ARG", 2: "ATTN_ERR_UNSUPPORTED", 3: "ATTN_ERR_CUDA",
                  4: "ATTN_ERR_TIMEOUT"}
@@ -57,6 +58,9 @@ def load(path: str | None = None):
         lib.attn_fwd_out_token_major.argtypes = lib.attn_fwd.argtypes
         lib.attn_fwd_varlen.restype = ci
         lib.attn_fwd_varlen.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, ci, ci, ctypes.c_float, ci, vp]
+        lib.attn_fwd_varlen_paged.restype = ci
+        lib.attn_fwd_varlen_paged.argtypes = [vp, vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, ci, ci, ci, ci, ci,
+                                              ctypes.c_float, ci, vp]
         lib.attn_qkv_prelude.restype = ci
         lib.attn_qkv_prelude.argtypes = [vp, vp, vp, vp, vp, ci, vp, vp, vp, ci, ci, ci, ci, ci, ctypes.c_float, ci,
                                          ci, ci, ci, vp]
@@ -195,6 +199,54 @@ def attn_fwd_varlen(q, k, v, cu_seqlens, max_seqlen: int, out=None, *, mask_mode
                                     cu_seqlens.contiguous().data_ptr(), batch, total, int(max_seqlen), Hq, Hkv, D,
                                     int(mask_mode), int(window), ctypes.c_float(scale), dtype,
                                     _stream_handle(stream))
+    _check(status)
+    return out
+
+
+def attn_fwd_varlen_paged(q, k_pool, v_pool, page_table, cu_seqlens, kv_lens, max_seqlen: int, out=None, *,
+                          mask_mode: int = MASK_CAUSAL, window: int = 0, scale: float | None = None, stream=None):
+    """Packed query chunks against paged caches (see attn_fwd_varlen_paged in attn.h).
+
+    q [total_q, Hq, D] token-major bf16 or fp16; k_pool, v_pool [num_pages, Hkv, page_size, D]
+    of q's dtype; page_table int32 [batch, max_pages]; cu_seqlens int32 [batch + 1]; kv_lens
+    int32 [batch] (the cached positions, each sequence's queries being the newest of them);
+    all contiguous CUDA tensors.  Returns out [total_q, Hq, D] without synchronising.
+    """
+    import torch
+    if not q.is_cuda or not q.is_contiguous() or q.dim() != 3:
+        raise ValueError("q must be a contiguous 3-D CUDA tensor [total_q, q_heads, D]")
+    if q.dtype == torch.bfloat16:
+        dtype = ATTN_BF16
+    elif q.dtype == torch.float16:
+        dtype = ATTN_F16
+    else:
+        raise ValueError(f"unsupported dtype {q.dtype} (bf16 or fp16)")
+    total, Hq, D = q.shape
+    for name, t in (("k_pool", k_pool), ("v_pool", v_pool)):
+        if not t.is_cuda or t.dtype != q.dtype or not t.is_contiguous() or t.dim() != 4 or t.shape[3] != D:
+            raise ValueError(f"{name} must be a contiguous CUDA tensor [num_pages, Hkv, page_size, D] of q's dtype")
+    if tuple(k_pool.shape) != tuple(v_pool.shape):
+        raise ValueError("k_pool and v_pool must share a shape")
+    num_pages, Hkv, page_size, _ = (int(x) for x in k_pool.shape)
+    if cu_seqlens.dtype != torch.int32 or not cu_seqlens.is_cuda or cu_seqlens.dim() != 1 or cu_seqlens.numel() < 1 \
+            or not cu_seqlens.is_contiguous():
+        raise ValueError("cu_seqlens must be a contiguous 1-D int32 CUDA tensor [batch + 1]")
+    batch = cu_seqlens.numel() - 1
+    if page_table.dtype != torch.int32 or not page_table.is_cuda or page_table.dim() != 2 or \
+            page_table.shape[0] != batch or not page_table.is_contiguous():
+        raise ValueError("page_table must be a contiguous int32 CUDA tensor [batch, max_pages]")
+    _check_kv_lens(kv_lens, batch)
+    if out is None:
+        out = torch.empty_like(q)
+    elif tuple(out.shape) != tuple(q.shape) or out.dtype != q.dtype or not out.is_contiguous() or not out.is_cuda:
+        raise ValueError("out must be a contiguous CUDA tensor shaped and typed like q")
+    if scale is None:
+        scale = float(torch.tensor(1.0 / math.sqrt(D), dtype=torch.float32).item())
+    status = load().attn_fwd_varlen_paged(q.data_ptr(), k_pool.data_ptr(), v_pool.data_ptr(), page_table.data_ptr(),
+                                          out.data_ptr(), cu_seqlens.data_ptr(), kv_lens.data_ptr(), batch, total,
+                                          int(max_seqlen), Hq, Hkv, num_pages, page_size, int(page_table.shape[1]), D,
+                                          int(mask_mode), int(window), ctypes.c_float(scale), dtype,
+                                          _stream_handle(stream))
     _check(status)
     return out
 

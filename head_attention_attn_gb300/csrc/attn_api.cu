@@ -3,9 +3,13 @@
 //
 // Kernel choice:
 //   f32                          -> K3 (SIMT fp32, any head_dim 1..256)
-//   bf16/fp16, q_len == 1, head_dim 128, group 4/8 -> K5 (tensor-core split-KV decode)
+//   bf16/fp16, q_len == 1, head_dim 128, group 4/8 -> K5 (tensor-core split-KV decode);
+//                                   paged caches of that shape whose page size TMA can place,
+//                                   and per-item caches with group 8 (row gather)
 //   bf16/fp16, q_len == 1, group 1/2/4/8 -> K2 (split-KV decode, the other shapes)
-//   bf16/fp16 otherwise          -> K1 (tcgen05 + TMA fused prefill)
+//   bf16/fp16 otherwise          -> K1 (tcgen05 + TMA fused prefill); packed queries over
+//                                   paged caches also go to K1, whose producer then gathers
+//                                   the K/V rows through the page table
 // There is no host fallback: an unsupported shape is refused (ferrum-kernels:
 // CUDA ops fail rather than copy data through host memory).
 #include <math.h>
@@ -24,7 +28,9 @@ __device__ unsigned int g_attn_status = 0;
 namespace {
 
 constexpr int kMaxDevices = 64;
-constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s per device-side wait
+// A device-side wait gives up after 250 ms: a healthy one lasts microseconds (a copy landing, a
+// tensor-core product), and a launch whose waits fail ends after about one limit per wave of blocks.
+constexpr unsigned long long kWaitLimitNs = 250000000ull;
 
 thread_local std::string t_last_error;
 
@@ -204,6 +210,63 @@ attn_status attn_fwd_varlen(const void* q, const void* k, const void* v, void* o
     return ATTN_OK;
 }
 
+attn_status attn_fwd_varlen_paged(const void* q, const void* k_pool, const void* v_pool, const int32_t* page_table,
+                                  void* out, const int32_t* cu_seqlens_q, const int32_t* kv_lens, int batch,
+                                  int total_q, int max_seqlen_q, int q_heads, int kv_heads, int num_pages,
+                                  int page_size, int max_pages, int head_dim, int mask_mode, int window, float scale,
+                                  int dtype, void* cuda_stream) {
+    t_last_error.clear();
+    if (batch < 0 || total_q < 0 || max_seqlen_q < 0 || num_pages < 0 || max_pages < 0)
+        return fail(ATTN_ERR_INVALID_ARG, "negative size (batch=%d, total_q=%d, max_seqlen_q=%d, num_pages=%d, "
+                    "max_pages=%d)", batch, total_q, max_seqlen_q, num_pages, max_pages);
+    if (page_size < 1) return fail(ATTN_ERR_INVALID_ARG, "page_size must be at least 1, not %d", page_size);
+    if ((long long)page_size * max_pages > 0x7fffffffLL)
+        return fail(ATTN_ERR_INVALID_ARG, "max_pages * page_size exceeds 2^31-1");
+    if (q_heads <= 0 || kv_heads <= 0 || head_dim <= 0)
+        return fail(ATTN_ERR_INVALID_ARG, "q_heads, kv_heads and head_dim must be positive (%d, %d, %d)", q_heads,
+                    kv_heads, head_dim);
+    if (q_heads % kv_heads != 0)
+        return fail(ATTN_ERR_INVALID_ARG, "q_heads (%d) is not a multiple of kv_heads (%d)", q_heads, kv_heads);
+    if (mask_mode < ATTN_MASK_NONE || mask_mode > ATTN_MASK_CAUSAL_WINDOW)
+        return fail(ATTN_ERR_INVALID_ARG, "mask_mode %d out of range", mask_mode);
+    if (dtype != ATTN_BF16 && dtype != ATTN_F32 && dtype != ATTN_F16)
+        return fail(ATTN_ERR_INVALID_ARG, "dtype %d out of range", dtype);
+    if (window < 0) return fail(ATTN_ERR_INVALID_ARG, "negative window %d", window);
+    if (!isfinite(scale)) return fail(ATTN_ERR_INVALID_ARG, "scale is not finite");
+    if (dtype == ATTN_F32) return fail(ATTN_ERR_UNSUPPORTED, "paged caches support bf16 and fp16");
+    if (head_dim != 64 && head_dim != 128)
+        return fail(ATTN_ERR_UNSUPPORTED, "bf16 and fp16 support head_dim 64 and 128, not %d", head_dim);
+    if (max_seqlen_q > total_q)
+        return fail(ATTN_ERR_INVALID_ARG, "max_seqlen_q %d exceeds total_q %d", max_seqlen_q, total_q);
+    if (batch == 0 || max_seqlen_q == 0) return ATTN_OK;  // nothing to compute
+    const long long blocks = ((long long)max_seqlen_q + 255) / 128;  // upper bound on query blocks per head
+    if (blocks * batch * q_heads > 0x7fffffffLL)
+        return fail(ATTN_ERR_UNSUPPORTED, "max_seqlen_q * batch * q_heads is too large for one launch");
+    if (!q || !out || !cu_seqlens_q || !kv_lens)
+        return fail(ATTN_ERR_INVALID_ARG, "null q, out, cu_seqlens_q or kv_lens pointer");
+    if ((long long)page_size * max_pages > 0 && (!k_pool || !v_pool || !page_table))
+        return fail(ATTN_ERR_INVALID_ARG, "null k_pool, v_pool or page_table pointer");
+    if (!aligned(q, 16) || !aligned(out, 16) || !aligned(k_pool, 16) || !aligned(v_pool, 16) ||
+        !aligned(page_table, 4) || !aligned(cu_seqlens_q, 4) || !aligned(kv_lens, 4))
+        return fail(ATTN_ERR_INVALID_ARG,
+                    "q, out and the pools must be 16-byte aligned; page_table, cu_seqlens_q and kv_lens 4-byte aligned");
+
+    DeviceState* st = nullptr;
+    attn_status s = device_state(&st);
+    if (s != ATTN_OK) return s;
+    attn::WaitCtl wc{st->status, kWaitLimitNs};
+    attn::Problem p{q, k_pool, v_pool, out, batch, q_heads, kv_heads, max_seqlen_q, 0, head_dim,
+                    0, mask_mode, window, nullptr, scale, dtype == ATTN_F16, cu_seqlens_q, total_q};
+    p.page_table = page_table;
+    p.kv_lens = kv_lens;
+    p.page_size = page_size;
+    p.max_pages = max_pages;
+    p.num_pages = num_pages;
+    cudaError_t e = attn::launch_prefill_tc(p, wc, static_cast<cudaStream_t>(cuda_stream));
+    if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "prefill_tc (paged) launch: %s", cudaGetErrorString(e));
+    return ATTN_OK;
+}
+
 attn_status attn_decode_caches(const void* q, const void* const* k_caches, const void* const* v_caches, void* out,
                                int m, int q_heads, int kv_heads, int capacity, int head_dim, const int32_t* kv_lens,
                                int sliding_window, float scale, int dtype, void* cuda_stream) {
@@ -241,8 +304,14 @@ attn_status attn_decode_caches(const void* q, const void* const* k_caches, const
     attn::WaitCtl wc{st->status, kWaitLimitNs};
     attn::CachesProblem p{q, k_caches, v_caches, out, m, q_heads, kv_heads, capacity, head_dim,
                           kv_lens, sliding_window, scale, dtype == ATTN_F16};
-    cudaError_t e = attn::launch_decode_caches(p, wc, stream, st->num_sms);
-    if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "decode_caches launch: %s", cudaGetErrorString(e));
+    // Per-item caches reach the tensor-core decode only through its row gather (the host cannot
+    // encode tensor maps for addresses held on the device), which streams at ~40 % of HBM: it
+    // wins at 8 query heads per kv head, while at 4 the CUDA-core decode's bulk copies do better.
+    const bool tc = attn::decode_tc_gather_supported(q_heads, kv_heads, head_dim) && q_heads / kv_heads == 8;
+    cudaError_t e = tc ? attn::launch_decode_tc_caches(p, wc, stream, st->num_sms)
+                       : attn::launch_decode_caches(p, wc, stream, st->num_sms);
+    if (e != cudaSuccess)
+        return fail(ATTN_ERR_CUDA, "%s launch: %s", tc ? "decode_tc (caches)" : "decode_caches", cudaGetErrorString(e));
     return ATTN_OK;
 }
 
@@ -290,8 +359,18 @@ attn_status attn_decode_paged(const void* q, const void* k_pool, const void* v_p
     attn::WaitCtl wc{st->status, kWaitLimitNs};
     attn::PagedProblem p{q, k_pool, v_pool, page_table, out, m, q_heads, kv_heads, num_pages, page_size,
                          max_pages, head_dim, kv_lens, sliding_window, scale, dtype == ATTN_F16};
-    cudaError_t e = attn::launch_decode_paged(p, wc, stream, st->num_sms);
-    if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "decode_paged launch: %s", cudaGetErrorString(e));
+    // Measured on GB300 (64 items, 8 kv heads, 8192 positions, head_dim 128), GB/s of the tensor-core
+    // decode (TMA per page where it can, rows gathered otherwise) against the CUDA-core decode
+    // (bulk copy per page piece): page 16: 4184 / 5103 (4 query heads per kv head), 4094 / 2413
+    // (8); page 32: 5299 / 5124, 5171 / 2421; page 128: 6176 / 5138, 6012 / 2428; page 7:
+    // 2043 / 4637, 2001 / 2390; page 1: 1798 / 1556, 1765 / 995.
+    const bool tma_pages = attn::decode_tc_paged_tma(page_size, num_pages, kv_heads);
+    const bool tc = attn::decode_tc_gather_supported(q_heads, kv_heads, head_dim) &&
+                    (G == 4 ? (tma_pages && page_size >= 32) : (tma_pages || page_size < 4));
+    cudaError_t e = tc ? attn::launch_decode_tc_paged(p, wc, stream, st->num_sms)
+                       : attn::launch_decode_paged(p, wc, stream, st->num_sms);
+    if (e != cudaSuccess)
+        return fail(ATTN_ERR_CUDA, "%s launch: %s", tc ? "decode_tc (paged)" : "decode_paged", cudaGetErrorString(e));
     return ATTN_OK;
 }
 
@@ -408,7 +487,8 @@ attn_status attn_sync_status(void* cuda_stream) {
         if (word == attn::kStatusBadSeqlens)
             return fail(ATTN_ERR_INVALID_ARG,
                         "a device-side length is out of range: cu_seqlens not non-decreasing within total and "
-                        "max_seqlen, or a cache length outside the capacity or the rope tables");
+                        "max_seqlen, a cache length outside the capacity or the rope tables, or fewer cached "
+                        "positions than queries");
         return fail(ATTN_ERR_CUDA, "device status word %u", word);
     }
     return ATTN_OK;

@@ -70,15 +70,10 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
-// A wait that has lasted this long also gives up once any block has recorded a time-out:
-// no healthy wait lasts a millisecond, and without this every later block of a failing
-// launch would wait out its own full limit.
-constexpr unsigned long long kJoinTimeoutAfterNs = 1000000ull;
-
 // Wait until the phase with the given parity has completed.  Gives up after
-// wc.limit_ns, as soon as *abort is set by another thread of the block, or (after
-// kJoinTimeoutAfterNs) once the status word holds a time-out; on its own time-out it
-// records kStatusTimeout and sets *abort.  Returns true when the phase completed.
+// wc.limit_ns, or as soon as *abort is set by another thread of the block;
+// on its own time-out it records kStatusTimeout and sets *abort.
+// Returns true when the phase completed.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const WaitCtl& wc,
                                           volatile int* abort) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -87,13 +82,8 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const W
         if (mbar_try_wait(bar, parity)) return true;
         if ((it & 31u) == 0u) {
             if (*abort) return false;
-            const unsigned long long waited = globaltimer_ns() - t0;
-            if (waited > wc.limit_ns) {
+            if (globaltimer_ns() - t0 > wc.limit_ns) {
                 record_status(wc.status, kStatusTimeout);
-                *abort = 1;
-                return false;
-            }
-            if (waited > kJoinTimeoutAfterNs && *reinterpret_cast<volatile unsigned*>(wc.status) == kStatusTimeout) {
                 *abort = 1;
                 return false;
             }

@@ -218,43 +218,46 @@ __global__ void __launch_bounds__(kThreads, (G == 8) ? 1 : 2) decode_splitkv_ker
 
     if (warp == kWarps) {
         // ------------------------------------------------------------ producer
-        if (lane == 0) {
-            int issued = 0;
-            for (int c = 0; c < nchunks; ++c) {
-                const int st = c % kStages;
-                if (c >= kStages &&
-                    !mbar_wait(smem_u32(&s_empty[st]), (uint32_t)(c / kStages - 1) & 1, p.wc, abort_flag))
-                    break;
-                const long long k0 = kbeg + (long long)c * kChunk;
-                const int rows = (int)min((long long)kChunk, kend - k0);
-                const uint32_t bytes = (uint32_t)rows * C::kRowBytes;
-                const uint32_t dst = ring + st * C::kStageBytes;
-                const uint32_t bar = smem_u32(&s_full[st]);
-                mbar_arrive_expect_tx(bar, 2 * bytes);
-                if (pages != nullptr) {
-                    // the chunk's rows may span pages: one copy per page piece, same bytes in total
-                    uint32_t off = 0;
-                    for (long long a = k0; a < k0 + rows;) {
-                        const long long pg = a / p.page_size;
-                        const long long e = min(k0 + rows, (pg + 1) * (long long)p.page_size);
-                        const size_t src = (((size_t)__ldg(pages + pg) * p.Hkv + hk) * p.page_size +
-                                            (size_t)(a - pg * p.page_size)) * D;
-                        const uint32_t nb = (uint32_t)(e - a) * C::kRowBytes;
-                        bulk_load(dst + off, kbase + src, nb, bar);
-                        bulk_load(dst + kChunk * C::kRowBytes + off, vbase + src, nb, bar);
-                        off += nb;
-                        a = e;
-                    }
-                } else {
-                    bulk_load(dst, kbase + k0 * D, bytes, bar);
-                    bulk_load(dst + kChunk * C::kRowBytes, vbase + k0 * D, bytes, bar);
+        // Lane 0 copies a contiguous chunk; over paged caches every lane loads the page ids of
+        // its own page pieces of the chunk and issues their copies, so the page-table reads and
+        // the copies of one chunk proceed in parallel.
+        int issued = 0;  // kept by lane 0
+        for (int c = 0; c < nchunks; ++c) {
+            const int st = c % kStages;
+            if (c >= kStages &&
+                !__all_sync(0xffffffffu, mbar_wait(smem_u32(&s_empty[st]), (uint32_t)(c / kStages - 1) & 1, p.wc,
+                                                   abort_flag)))
+                break;
+            const long long k0 = kbeg + (long long)c * kChunk;
+            const int rows = (int)min((long long)kChunk, kend - k0);
+            const uint32_t bytes = (uint32_t)rows * C::kRowBytes;
+            const uint32_t dst = ring + st * C::kStageBytes;
+            const uint32_t bar = smem_u32(&s_full[st]);
+            if (lane == 0) mbar_arrive_expect_tx(bar, 2 * bytes);
+            __syncwarp();
+            if (pages != nullptr) {
+                // the chunk's rows may span pages: one copy per page piece, same bytes in total
+                const long long pg0 = k0 / p.page_size;
+                const int npieces = (int)((k0 + rows - 1) / p.page_size - pg0 + 1);
+                for (int i = lane; i < npieces; i += 32) {
+                    const long long pg = pg0 + i;
+                    const long long a = max(k0, pg * p.page_size), e = min(k0 + rows, (pg + 1) * p.page_size);
+                    const size_t src = (((size_t)__ldg(pages + pg) * p.Hkv + hk) * p.page_size +
+                                        (size_t)(a - pg * p.page_size)) * D;
+                    const uint32_t off = (uint32_t)(a - k0) * C::kRowBytes, nb = (uint32_t)(e - a) * C::kRowBytes;
+                    bulk_load(dst + off, kbase + src, nb, bar);
+                    bulk_load(dst + kChunk * C::kRowBytes + off, vbase + src, nb, bar);
                 }
-                issued = c + 1;
+            } else if (lane == 0) {
+                bulk_load(dst, kbase + k0 * D, bytes, bar);
+                bulk_load(dst + kChunk * C::kRowBytes, vbase + k0 * D, bytes, bar);
             }
-            // no copy may still be writing shared memory when the block moves on
+            issued = c + 1;
+        }
+        // no copy may still be writing shared memory when the block moves on
+        if (lane == 0)
             for (int c = (issued > kStages ? issued - kStages : 0); c < issued; ++c)
                 drain_wait(smem_u32(&s_full[c % kStages]), (uint32_t)(c / kStages) & 1, p.wc);
-        }
     } else {
         // ------------------------------------------------------------ compute warps
         const int grp = lane / LPK;            // which key row of a load instruction this lane reads

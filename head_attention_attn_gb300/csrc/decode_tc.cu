@@ -12,7 +12,11 @@
 //
 // Work unit: (batch b, kv head hk, split); the splits of one unit form a cluster and merge
 // their partial results through distributed shared memory in CTA rank 0.
-//   warp 0       TMA producer: 128-key K and V tiles through 3-stage rings.
+//   warp 0       producer: 128-key K and V tiles through 3-stage rings, either by TMA from
+//                one contiguous [B, Hkv, Lk, D] cache, or (per-item caches and paged caches,
+//                whose addresses only the device knows) by 16-byte cp.async copies that
+//                all 32 lanes issue row by row into the same swizzled layout, rows past the
+//                visible keys written as zeros.
 //   warp 1       TMEM owner and single-thread MMA issuer: QK(j) then PV(j-1).
 //   warps 2-5    one key per thread: it reads its key's 16 head scores from TMEM, the per-head
 //                block maxima come from a shuffle reduce-scatter and a 4-warp exchange,
@@ -22,7 +26,9 @@
 //                128 head dims.
 //
 // The operation is the q_len = 1 case of ferrum-kernels Backend::flash_attention (the
-// GQA decode of a KV cache at pos_offset), with the masks of attn.h.
+// GQA decode of a KV cache at pos_offset), with the masks of attn.h, and the per-cache
+// decode of Backend::flash_attention_batched_per_cache (device kv_lens, the last-w sliding
+// window) over per-item or paged caches.
 #include "kernels.h"
 
 #include <algorithm>
@@ -35,7 +41,8 @@ constexpr int D = 128;
 constexpr int BN = 128;         // keys per block
 constexpr int NH = 16;          // MMA N: the group's query heads, padded
 constexpr int kStages = 3;
-constexpr int kThreads = 192;
+constexpr int kThreads = 192;        // TMA source: producer, MMA, 4 softmax warps
+constexpr int kThreadsGather = 256;  // gather sources: + 2 producer warps (one per ring stage)
 constexpr int kMaxSplits = 8;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f;
@@ -50,7 +57,8 @@ struct L {
     static constexpr int kOffP = kOffQ + kQBytes;
     static constexpr int kOffX = kOffP + kPBytes;            // [2 parities][4 warps][16] block maxima
     static constexpr int kOffS = kOffX + 2 * 4 * NH * 4;     // [4 warps][16] row-sum parts
-    static constexpr int kOffBar = kOffS + 4 * NH * 4;
+    static constexpr int kOffRow = kOffS + 4 * NH * 4;       // [3][128] gather: byte offset of each key row
+    static constexpr int kOffBar = kOffRow + kStages * BN * 8;
     static constexpr int kSmem = kOffBar + 256 + 1024;        // + realignment slack
     // after the last P V product the K ring is free; the combine reuses it
     static constexpr int kOffCm = 0;                         // [16] log2-domain maxima
@@ -80,14 +88,38 @@ constexpr uint32_t kColS = 0;   // + 16 * buffer
 constexpr uint32_t kColO = 32;
 constexpr uint32_t kTmemCols = 64;
 
+// Where the K and V rows come from.
+enum : int {
+    kSrcTma = 0,     // one contiguous [B, Hkv, Lk, D] cache per tensor, TMA tensor maps
+    kSrcCaches = 1,  // per-item caches: device arrays of pointers to [Hkv, capacity, D]
+    kSrcPaged = 2,   // pools [num_pages, Hkv, page_size, D] and a device page table [B, max_pages]
+};
+
 struct DecodeTcParams {
     const uint16_t* q;
     uint16_t* out;
-    const int32_t* key_lens;
-    int Hq, Hkv, Lk, P, mode, window;
+    const int32_t* key_lens;  // key_lens (contiguous cache) or kv_lens (per-item and paged caches)
+    int Hq, Hkv, Lk, P, mode, window;  // Lk: the capacity of an item's cache for the gather sources
     float scale_log2;
     WaitCtl wc;
+    // gather sources: the query of item b is its newest position kv_lens[b] - 1 and sees the
+    // item's positions, or only the last `sliding` of them
+    int sliding;
+    const uint16_t* const* kc;  // per-item caches
+    const uint16_t* const* vc;
+    const uint16_t* kpool;      // paged caches
+    const uint16_t* vpool;
+    const int32_t* page_table;
+    int page_size, max_pages, num_pages;
+    int paged_tma;  // paged: the page size lets TMA copy whole pages (else the rows are gathered)
 };
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
 __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, const WaitCtl& wc) {
     const unsigned long long t0 = globaltimer_ns();
@@ -153,11 +185,12 @@ __device__ __forceinline__ int head_of_lane(int lane) {
     return 8 * ((lane >> 4) & 1) + 4 * ((lane >> 3) & 1) + 2 * ((lane >> 2) & 1) + ((lane >> 1) & 1);
 }
 
-template <int G, bool F16>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int G, bool F16, int SRC>
+__global__ void __launch_bounds__(SRC != kSrcTma ? kThreadsGather : kThreads, 1)
     decode_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                      const DecodeTcParams p) {
     static_assert(G >= 1 && G <= NH, "group size");
+    constexpr bool kGather = SRC != kSrcTma;  // an instantiation with the gather producers
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_s = smem_u32(smem_raw);
     uint8_t* smem = smem_raw + ((1024u - (raw_s & 1023u)) & 1023u);
@@ -170,29 +203,75 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int split = blockIdx.x, nsplit = gridDim.x;
     const int hk = blockIdx.y, b = blockIdx.z;
 
-    // this split's keys [kbeg, kend) of the query's visible interval, in whole blocks
+    // The query's visible interval [lo, hi); this split's share [vbeg, vend), in 128-key blocks
+    // from gbeg.  Block j's tile starts at position blk_start(j) and its keys that count are
+    // [max(vbeg, gbeg + j BN), min(vend, gbeg + (j + 1) BN)).
     const int klen = valid_keys(p.key_lens, b, p.Lk);
     long long lo, hi;
-    key_interval(p.mode, p.window, klen, p.P, p.P, &lo, &hi);
+    const uint16_t* kbase = nullptr;  // per-item caches: the item's K and V caches
+    const uint16_t* vbase = nullptr;
+    const int32_t* pages = nullptr;
+    bool tma = true;  // copies by TMA (per-item caches: the gather producers)
+    if constexpr (SRC == kSrcTma) {
+        key_interval(p.mode, p.window, klen, p.P, p.P, &lo, &hi);
+    } else {
+        lo = (p.sliding > 0 && klen > p.sliding) ? (long long)(klen - p.sliding) : 0;
+        hi = klen;
+        bool bad = false;
+        if constexpr (SRC == kSrcCaches) {
+            kbase = p.kc[b];
+            vbase = p.vc[b];
+            const uintptr_t ka = reinterpret_cast<uintptr_t>(kbase), va = reinterpret_cast<uintptr_t>(vbase);
+            bad = kbase == nullptr || vbase == nullptr || ((ka | va) & 15u) != 0;
+            tma = false;  // the host cannot encode tensor maps for addresses only the device holds
+        } else {
+            // every CTA of the cluster checks all of the item's visible page entries, so they agree
+            tma = p.paged_tma != 0;
+            kbase = static_cast<const uint16_t*>(p.kpool);
+            vbase = static_cast<const uint16_t*>(p.vpool);
+            pages = p.page_table + (size_t)b * p.max_pages;
+            if (hi > lo)
+                for (long long x = lo / p.page_size + threadIdx.x; x <= (hi - 1) / p.page_size; x += blockDim.x) {
+                    const int id = __ldg(pages + x);
+                    bad |= (id < 0 || id >= p.num_pages);
+                }
+        }
+        if (__syncthreads_or(bad)) {
+            // nothing of the item is read and its output is zeros
+            if (threadIdx.x == 0) record_status(p.wc.status, SRC == kSrcCaches ? kStatusBadPointer : kStatusBadPage);
+            lo = hi = 0;
+        }
+    }
     if (hi < lo) hi = lo;
-    long long per = (hi - lo + nsplit - 1) / nsplit;
+    // Blocks start on multiples of 128 positions (the positions before lo in the first block do
+    // not count): page pieces then land on whole 8-row groups of the swizzled tiles, and every
+    // source splits the keys the same way, so the contiguous, per-item and paged decodes of the
+    // same cache compute the same numbers in the same order.
+    const long long origin = (lo / BN) * BN;
+    long long per = (hi - origin + nsplit - 1) / nsplit;
     per = (per + BN - 1) / BN * BN;
-    const long long kbeg = lo + (long long)split * per;
-    const long long kend = min(hi, kbeg + per);
-    const int nblk = (kend > kbeg) ? (int)((kend - kbeg + BN - 1) / BN) : 0;
-
+    const long long gbeg = origin + (long long)split * per;
+    const long long vbeg = max(gbeg, lo);
+    const long long vend = min(hi, gbeg + per);
+    const int nblk = (vend > vbeg) ? (int)((vend - gbeg + BN - 1) / BN) : 0;
+    auto blk_start = [&](int j) -> long long { return gbeg + (long long)j * BN; };
+    // the same bounds as offsets from gbeg (all within [-BN, per], so 32-bit)
+    const int vb_rel = (int)(vbeg - gbeg), ve_rel = (int)(vend - gbeg);
+    const int lo_rel = (int)max(-(long long)BN, lo - gbeg), hi_rel = (int)min(per + BN, hi - gbeg);
     if (threadIdx.x == 0) {
         for (int i = 0; i < kNumBars; ++i) {
             uint32_t count = 1;
             if (i == kBarSFree || i == kBarSFree + 1 || i == kBarPFull || i == kBarXch || i == kBarXch + 1 ||
                 i == kBarSum)
                 count = 4;  // one arrival per softmax warp
+            if (kGather && !tma && ((i >= kBarKFull && i < kBarKFull + kStages) || (i >= kBarVFull && i < kBarVFull + kStages)))
+                count = 32;  // one arrival per lane of the stage's producer warp, after its copies landed
             mbar_init(bar0 + 8 * i, count);
         }
         *abort_flag = 0;
         mbar_fence_init();
     }
-    if (warp >= 2) {
+    if (warp >= 2 && warp < 6) {
         // Q of the group's heads into a 16-row K-major tile (128-byte swizzle), zero rows past G;
         // 256 16-byte units, two per thread
         const int t = threadIdx.x - 64;
@@ -211,7 +290,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_alloc(smem_u32(tmem_holder), kTmemCols);
         tmem_relinquish();
     }
-    if (warp == 0 && lane == 0) {
+    if (tma && warp == 0 && lane == 0) {
         tma_prefetch_desc(&tmK);
         tma_prefetch_desc(&tmV);
     }
@@ -226,35 +305,140 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int h = 0; h < NH; ++h) m_run[h] = -INFINITY, l_part[h] = 0.f;
     bool ok = true;
 
-    if (warp == 0) {
-        // ------------------------------------------------------------ TMA producer
-        if (lane == 0 && nblk > 0) {
-            const int kbh = b * p.Hkv + hk;
-            int issued = 0;
-            for (int j = 0; j < nblk; ++j) {
-                const int s = j % kStages;
-                const uint32_t n = (uint32_t)(j / kStages);
-                const int krow = (int)(kbeg + (long long)j * BN);
-                if (j >= kStages && !mbar_wait(bar0 + 8 * (kBarKEmpty + s), (n - 1) & 1, p.wc, abort_flag)) break;
-                mbar_arrive_expect_tx(bar0 + 8 * (kBarKFull + s), L::kKVBytes);
-                for (int c = 0; c < D / 64; ++c)
-                    tma_load_3d(sbase + L::kOffK + s * L::kKVBytes + c * (BN * 128), &tmK, bar0 + 8 * (kBarKFull + s),
-                                c * 64, krow, kbh);
-                if (j >= kStages && !mbar_wait(bar0 + 8 * (kBarVEmpty + s), (n - 1) & 1, p.wc, abort_flag)) {
-                    issued = 2 * j + 1;
-                    break;
-                }
-                mbar_arrive_expect_tx(bar0 + 8 * (kBarVFull + s), L::kKVBytes);
-                for (int c = 0; c < D / 64; ++c)
-                    tma_load_3d(sbase + L::kOffV + s * L::kKVBytes + c * (BN * 128), &tmV, bar0 + 8 * (kBarVFull + s),
-                                c * 64, krow, kbh);
-                issued = 2 * j + 2;
+    if (warp >= 6 && tma) {
+        // the two extra producer warps of a gather instantiation have nothing to copy when the
+        // block's rows come by TMA
+    } else if (kGather && !tma && (warp == 0 || warp >= 6)) {
+        // ------------------------------------------------------------ gather producers
+        // Three warps, one per ring stage (warp 0: stage 0, warps 6 and 7: stages 1 and 2), so
+        // each stage is released as soon as its own copies have landed and all three are in
+        // flight at once.  For a block the warp writes the byte offset of each of the 128 key
+        // rows (or ~0 past the visible keys) to shared memory, then copies 2 rows per
+        // instruction, 16 lanes per 256-byte row, each 16-byte unit to its swizzled place in
+        // the K or V tile (the layout TMA gives); rows past the visible keys are zeros.  K is
+        // released first (wait_group 1), then V; each lane waits for its own copies, fences
+        // them for the tensor core and arrives.
+        const int st = warp == 0 ? 0 : warp - 5;
+        unsigned long long* rowoff = reinterpret_cast<unsigned long long*>(smem + L::kOffRow) + st * BN;
+        const int half = lane >> 4, u = lane & 15, c = u >> 3, qd = u & 7;
+        const char* kb = reinterpret_cast<const char*>(kbase);
+        const char* vb = reinterpret_cast<const char*>(vbase);
+        const uint32_t kt = sbase + L::kOffK + st * L::kKVBytes, vt = sbase + L::kOffV + st * L::kKVBytes;
+        for (int j = st; j < nblk; j += kStages) {
+            const uint32_t n = (uint32_t)(j / kStages);
+            if (j >= kStages) {
+                if (!warp_wait(bar0 + 8 * (kBarKEmpty + st), (n - 1) & 1, p.wc, abort_flag)) break;
+                if (!warp_wait(bar0 + 8 * (kBarVEmpty + st), (n - 1) & 1, p.wc, abort_flag)) break;
             }
-            const int nk = (issued + 1) / 2, nv = issued / 2;
-            for (int j = (nk > kStages ? nk - kStages : 0); j < nk; ++j)
-                drain_wait(bar0 + 8 * (kBarKFull + j % kStages), (uint32_t)(j / kStages) & 1, p.wc);
-            for (int j = (nv > kStages ? nv - kStages : 0); j < nv; ++j)
-                drain_wait(bar0 + 8 * (kBarVFull + j % kStages), (uint32_t)(j / kStages) & 1, p.wc);
+            const long long krow0 = gbeg + (long long)j * BN;
+            __syncwarp();
+            for (int r = lane; r < BN; r += 32) {
+                const long long key = krow0 + r;
+                unsigned long long off = ~0ull;
+                if (key >= vbeg && key < vend) {  // the keys that count; other rows are zeros
+                    if constexpr (SRC == kSrcCaches) {
+                        off = ((unsigned long long)hk * (unsigned long long)p.Lk + (unsigned long long)key) * (D * 2);
+                    } else {
+                        const long long pg = __ldg(pages + key / p.page_size);
+                        off = (((unsigned long long)pg * p.Hkv + hk) * (unsigned long long)p.page_size +
+                               (unsigned long long)(key % p.page_size)) * (D * 2);
+                    }
+                }
+                rowoff[r] = off;
+            }
+            __syncwarp();
+#pragma unroll 2
+            for (int kind = 0; kind < 2; ++kind) {  // K, then V
+                const uint32_t tile = kind ? vt : kt;
+                const char* src = kind ? vb : kb;
+#pragma unroll 8
+                for (int i = 0; i < BN / 2; ++i) {
+                    const int r = 2 * i + half;
+                    const unsigned long long off = rowoff[r];
+                    const uint32_t dofs = c * (BN * 128) + r * 128 + ((qd ^ (r & 7)) << 4);
+                    if (off != ~0ull) cp_async16(tile + dofs, src + off + u * 16);
+                    else *reinterpret_cast<uint4*>(smem + (tile - sbase) + dofs) = make_uint4(0u, 0u, 0u, 0u);
+                }
+                cp_async_commit();
+            }
+            cp_async_wait<1>();  // this lane's K copies have landed
+            fence_proxy_async_smem();
+            mbar_arrive(bar0 + 8 * (kBarKFull + st));
+            cp_async_wait<0>();  // and its V copies
+            fence_proxy_async_smem();
+            mbar_arrive(bar0 + 8 * (kBarVFull + st));
+        }
+        cp_async_wait<0>();  // nothing stays in flight, whatever happened above
+    } else if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer
+        // contiguous cache: one box per 64-column chunk at (chunk, position, b Hkv + hk); paged:
+        // one copy per page piece that holds visible keys (whole pages of at most 128 rows, or
+        // 128 rows of a longer page), the pool map bounding every coordinate.  Lane 0 issues the
+        // copies.
+        if (nblk > 0) {
+            const int kbh = b * p.Hkv + hk;
+            auto load = [&](const CUtensorMap* map, uint32_t tile, uint32_t bar, int j) {
+                const long long s0 = blk_start(j);
+                if constexpr (SRC == kSrcTma) {
+                    mbar_arrive_expect_tx(bar, L::kKVBytes);
+                    for (int c = 0; c < D / 64; ++c) tma_load_3d(tile + c * (BN * 128), map, bar, c * 64, (int)s0, kbh);
+                } else {
+                    const int ps = p.page_size;
+                    if (ps >= BN) {  // one 128-row piece of a page
+                        const int pg = __ldg(pages + s0 / ps);
+                        mbar_arrive_expect_tx(bar, L::kKVBytes);
+                        for (int c = 0; c < D / 64; ++c)
+                            tma_load_3d(tile + c * (BN * 128), map, bar, c * 64, (int)(s0 % ps), pg * p.Hkv + hk);
+                    }
+                }
+            };
+            // paged with pages shorter than a block: whole pages of ps rows (ps divides 128, a
+            // multiple of 8), lane i reading the page id of the block's i-th page with keys and
+            // copying that page, after lane 0 has posted the bytes of them all
+            auto load_pages = [&](const CUtensorMap* map, uint32_t tile, uint32_t bar, int j) {
+                const int ps = p.page_size;
+                const long long s0 = blk_start(j);
+                const long long f = max(s0, lo) / ps, e = (min(s0 + BN, hi) - 1) / ps;  // pages with keys
+                if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)((e - f + 1) * ps * (D * 2)));
+                __syncwarp();
+                for (long long x = f + lane; x <= e; x += 32) {
+                    const int pg = __ldg(pages + x);
+                    const uint32_t row = (uint32_t)(x * ps - s0);
+                    for (int c = 0; c < D / 64; ++c)
+                        tma_load_3d(tile + c * (BN * 128) + row * 128, map, bar, c * 64, 0, pg * p.Hkv + hk);
+                }
+            };
+            const bool small_pages = SRC == kSrcPaged && p.page_size < BN;
+            // the whole warp runs the loop for small pages, lane 0 alone otherwise
+            int issued = 0;  // kept by lane 0
+            if (small_pages || lane == 0) {
+                auto wait = [&](uint32_t bar, uint32_t parity) {
+                    return small_pages ? warp_wait(bar, parity, p.wc, abort_flag)
+                                       : mbar_wait(bar, parity, p.wc, abort_flag);
+                };
+                for (int j = 0; j < nblk; ++j) {
+                    const int s = j % kStages;
+                    const uint32_t n = (uint32_t)(j / kStages);
+                    const uint32_t kt = sbase + L::kOffK + s * L::kKVBytes, vt = sbase + L::kOffV + s * L::kKVBytes;
+                    if (j >= kStages && !wait(bar0 + 8 * (kBarKEmpty + s), (n - 1) & 1)) break;
+                    if (small_pages) load_pages(&tmK, kt, bar0 + 8 * (kBarKFull + s), j);
+                    else load(&tmK, kt, bar0 + 8 * (kBarKFull + s), j);
+                    if (j >= kStages && !wait(bar0 + 8 * (kBarVEmpty + s), (n - 1) & 1)) {
+                        issued = 2 * j + 1;
+                        break;
+                    }
+                    if (small_pages) load_pages(&tmV, vt, bar0 + 8 * (kBarVFull + s), j);
+                    else load(&tmV, vt, bar0 + 8 * (kBarVFull + s), j);
+                    issued = 2 * j + 2;
+                }
+            }
+            if (lane == 0) {
+                const int nk = (issued + 1) / 2, nv = issued / 2;
+                for (int j = (nk > kStages ? nk - kStages : 0); j < nk; ++j)
+                    drain_wait(bar0 + 8 * (kBarKFull + j % kStages), (uint32_t)(j / kStages) & 1, p.wc);
+                for (int j = (nv > kStages ? nv - kStages : 0); j < nv; ++j)
+                    drain_wait(bar0 + 8 * (kBarVFull + j % kStages), (uint32_t)(j / kStages) & 1, p.wc);
+            }
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
@@ -327,8 +511,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(bar0 + 8 * (kBarSFree + par));
 
-            // scores in the log2 domain; keys outside [kend) and padding heads are -inf
-            const bool vis = kbeg + (long long)j * BN + key < kend;
+            // scores in the log2 domain; keys that do not count in this block and padding heads are -inf
+            // (offsets from gbeg: block j holds rel = j BN + key, and the split counts [vb_rel, ve_rel))
+            const int rel = j * BN + key;
+            const bool vis = rel >= vb_rel && rel < ve_rel;
             float x[NH];
 #pragma unroll
             for (int h = 0; h < NH; ++h) x[h] = (vis && h < G) ? s[h] * sl : -INFINITY;
@@ -379,7 +565,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int h = 0; h < NH; ++h) o[h] *= alpha[h];
                 tmem_st16(tmem + lane_off + kColO, reinterpret_cast<const uint32_t*>(o));
             }
-            fence_proxy_async_smem();  // P^T is read by the tensor core (async proxy)
+            // A V tile row that the query does not see gets weight 0, but the tensor core multiplies
+            // that 0 into the row, and 0 * Inf or 0 * NaN is NaN: in a block whose tile reaches
+            // outside [lo, hi) (the first or last), once the tile has landed each thread zeroes its
+            // row if it lies outside (the gather writes such rows as zeros already).
+            if (tma && (j * BN < lo_rel || (j + 1) * BN > hi_rel)) {
+                const int s = j % kStages;
+                if (!warp_wait(bar0 + 8 * (kBarVFull + s), (uint32_t)(j / kStages) & 1, p.wc, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                if (rel < lo_rel || rel >= hi_rel) {
+                    uint8_t* vrow = smem + L::kOffV + s * L::kKVBytes + key * 128;
+#pragma unroll
+                    for (int c = 0; c < D / 64; ++c)
+#pragma unroll
+                        for (int q = 0; q < 8; ++q)
+                            *reinterpret_cast<uint4*>(vrow + c * (BN * 128) + q * 16) = make_uint4(0u, 0u, 0u, 0u);
+                }
+            }
+            fence_proxy_async_smem();  // P^T (and zeroed V rows) are read by the tensor core (async proxy)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar0 + 8 * kBarPFull);
@@ -422,7 +627,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // ---------------------------------------------------------------- combine the splits in rank 0
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-    if (split == 0 && warp >= 2) {
+    if (split == 0 && warp >= 2 && warp < 6) {
         const int dim = 32 * (warp & 3) + lane;
         for (int h = 0; h < G; ++h) {
             float ms[kMaxSplits], ls[kMaxSplits], os[kMaxSplits];
@@ -483,24 +688,23 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-// [outer, L, 128] 16-bit tensor as 3-D (128, L, outer); box 64 x 128 x 1, 128-byte swizzle, zero fill.
-bool encode_kv(CUtensorMap* map, const void* base, int L, int outer, bool f16) {
+// [outer, L, 128] 16-bit tensor as 3-D (128, L, outer); box 64 x rows x 1, 128-byte swizzle, zero
+// fill for coordinates outside the tensor.
+bool encode_kv(CUtensorMap* map, const void* base, unsigned long long L, unsigned long long outer, int rows, bool f16) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
     cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)L, (cuuint64_t)outer};
     cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)L * D * 2};
-    cuuint32_t box[3] = {64, 128, 1};
+    cuuint32_t box[3] = {64, (cuuint32_t)rows, 1};
     cuuint32_t estr[3] = {1, 1, 1};
     return fn(map, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base),
               dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int G, bool F16>
-cudaError_t launch_g(const Problem& pr, const DecodeTcParams& p, int nsplit, cudaStream_t stream) {
-    CUtensorMap tk, tv;
-    if (!encode_kv(&tk, pr.k, pr.Lk, pr.B * pr.Hkv, F16) || !encode_kv(&tv, pr.v, pr.Lk, pr.B * pr.Hkv, F16))
-        return cudaErrorInvalidValue;
+template <int G, bool F16, int SRC>
+cudaError_t launch_g(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeTcParams& p, int items, int nsplit,
+                     cudaStream_t stream) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
@@ -509,14 +713,15 @@ cudaError_t launch_g(const Problem& pr, const DecodeTcParams& p, int nsplit, cud
     {
         std::lock_guard<std::mutex> g(mu);
         if (dev < 64 && !configured[dev]) {
-            e = cudaFuncSetAttribute(decode_tc_kernel<G, F16>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmem);
+            e = cudaFuncSetAttribute(decode_tc_kernel<G, F16, SRC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     L::kSmem);
             if (e != cudaSuccess) return e;
             configured[dev] = true;
         }
     }
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)nsplit, (unsigned)pr.Hkv, (unsigned)pr.B);
-    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.gridDim = dim3((unsigned)nsplit, (unsigned)p.Hkv, (unsigned)items);
+    cfg.blockDim = dim3(SRC != kSrcTma ? kThreadsGather : kThreads, 1, 1);
     cfg.dynamicSmemBytes = L::kSmem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
@@ -526,7 +731,43 @@ cudaError_t launch_g(const Problem& pr, const DecodeTcParams& p, int nsplit, cud
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, decode_tc_kernel<G, F16>, tk, tv, p);
+    return cudaLaunchKernelEx(&cfg, decode_tc_kernel<G, F16, SRC>, tk, tv, p);
+}
+
+template <int SRC>
+cudaError_t launch_src(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeTcParams& p, int G, bool f16,
+                       int items, int nsplit, cudaStream_t stream) {
+    if (G == 4) return f16 ? launch_g<4, true, SRC>(tk, tv, p, items, nsplit, stream)
+                           : launch_g<4, false, SRC>(tk, tv, p, items, nsplit, stream);
+    if (G == 8) return f16 ? launch_g<8, true, SRC>(tk, tv, p, items, nsplit, stream)
+                           : launch_g<8, false, SRC>(tk, tv, p, items, nsplit, stream);
+    return cudaErrorInvalidValue;
+}
+
+// One CTA per SM.  Measured on GB300 (batch 4-64, 2048-8192 keys): the best split count
+// reaches about 0.84 CTAs per SM (128 on 152 SMs) and no more; clusters of 8 of these
+// 200-KB CTAs schedule poorly (twice slower than 4 at batch 4), and a split should cover at
+// least 1024 keys.
+int choose_splits(long long units, long long keys, int num_sms) {
+    constexpr int kMaxUsedSplits = 4;
+    const long long target = num_sms > 0 ? (27LL * num_sms) / 32 : 128;
+    int n = 1;
+    while (n < kMaxUsedSplits && units * n < target) n *= 2;
+    return (int)std::max(1LL, std::min<long long>(n, std::max(1LL, keys / 1024)));
+}
+
+DecodeTcParams base_params(const void* q, void* out, const int32_t* lens, int Hq, int Hkv, int Lk, float scale,
+                           const WaitCtl& wc) {
+    DecodeTcParams p = {};
+    p.q = static_cast<const uint16_t*>(q);
+    p.out = static_cast<uint16_t*>(out);
+    p.key_lens = lens;
+    p.Hq = Hq;
+    p.Hkv = Hkv;
+    p.Lk = Lk;
+    p.scale_log2 = scale * kLog2e;
+    p.wc = wc;
+    return p;
 }
 
 }  // namespace
@@ -537,34 +778,70 @@ bool decode_tc_supported(const Problem& p) {
     return G == 4 || G == 8;
 }
 
+bool decode_tc_gather_supported(int Hq, int Hkv, int D) {
+    if (D != 128 || Hkv <= 0 || Hq % Hkv != 0) return false;
+    const int G = Hq / Hkv;
+    return G == 4 || G == 8;
+}
+
+bool decode_tc_paged_tma(int page_size, int num_pages, int Hkv) {
+    return ((page_size >= 8 && page_size <= BN && BN % page_size == 0) || page_size % BN == 0) &&
+           (long long)num_pages * Hkv <= 0x7fffffffLL;
+}
+
 cudaError_t launch_decode_tc(const Problem& pr, const WaitCtl& wc, cudaStream_t stream, int num_sms) {
     if (pr.Hkv > 65535 || pr.B > 65535) return cudaErrorInvalidConfiguration;
-    DecodeTcParams p;
-    p.q = static_cast<const uint16_t*>(pr.q);
-    p.out = static_cast<uint16_t*>(pr.out);
-    p.key_lens = pr.key_lens;
-    p.Hq = pr.Hq;
-    p.Hkv = pr.Hkv;
-    p.Lk = pr.Lk;
+    DecodeTcParams p = base_params(pr.q, pr.out, pr.key_lens, pr.Hq, pr.Hkv, pr.Lk, pr.scale, wc);
     p.P = pr.pos_offset;
     p.mode = pr.mode;
     p.window = pr.window;
-    p.scale_log2 = pr.scale * kLog2e;
-    p.wc = wc;
-    // One CTA per SM.  Measured on GB300 (batch 4-64, 2048-8192 keys): the best split count
-    // reaches about 0.84 CTAs per SM (128 on 152 SMs) and no more; clusters of 8 of these
-    // 200-KB CTAs schedule poorly (twice slower than 4 at batch 4), and a split should cover at
-    // least 1024 keys.
-    constexpr int kMaxUsedSplits = 4;
-    const long long units = (long long)pr.B * pr.Hkv;
-    const long long target = num_sms > 0 ? (27LL * num_sms) / 32 : 128;
-    int n = 1;
-    while (n < kMaxUsedSplits && units * n < target) n *= 2;
-    const int nsplit = (int)std::max(1LL, std::min<long long>(n, std::max(1LL, (long long)pr.Lk / 1024)));
-    const int G = pr.Hq / pr.Hkv;
-    if (G == 4) return pr.f16 ? launch_g<4, true>(pr, p, nsplit, stream) : launch_g<4, false>(pr, p, nsplit, stream);
-    if (G == 8) return pr.f16 ? launch_g<8, true>(pr, p, nsplit, stream) : launch_g<8, false>(pr, p, nsplit, stream);
-    return cudaErrorInvalidValue;
+    CUtensorMap tk, tv;
+    if (!encode_kv(&tk, pr.k, pr.Lk, (unsigned long long)pr.B * pr.Hkv, BN, pr.f16) ||
+        !encode_kv(&tv, pr.v, pr.Lk, (unsigned long long)pr.B * pr.Hkv, BN, pr.f16))
+        return cudaErrorInvalidValue;
+    const int nsplit = choose_splits((long long)pr.B * pr.Hkv, pr.Lk, num_sms);
+    return launch_src<kSrcTma>(tk, tv, p, pr.Hq / pr.Hkv, pr.f16, pr.B, nsplit, stream);
+}
+
+cudaError_t launch_decode_tc_caches(const CachesProblem& cp, const WaitCtl& wc, cudaStream_t stream, int num_sms) {
+    if (cp.Hkv > 65535 || cp.m > 65535) return cudaErrorInvalidConfiguration;
+    DecodeTcParams p = base_params(cp.q, cp.out, cp.kv_lens, cp.Hq, cp.Hkv, cp.capacity, cp.scale, wc);
+    p.sliding = cp.sliding;
+    p.kc = reinterpret_cast<const uint16_t* const*>(cp.k_caches);
+    p.vc = reinterpret_cast<const uint16_t* const*>(cp.v_caches);
+    CUtensorMap unused = {};
+    const long long span = cp.sliding > 0 ? std::min(cp.sliding, cp.capacity) : cp.capacity;
+    const int nsplit = choose_splits((long long)cp.m * cp.Hkv, span, num_sms);
+    return launch_src<kSrcCaches>(unused, unused, p, cp.Hq / cp.Hkv, cp.f16, cp.m, nsplit, stream);
+}
+
+cudaError_t launch_decode_tc_paged(const PagedProblem& pp, const WaitCtl& wc, cudaStream_t stream, int num_sms) {
+    if (pp.Hkv > 65535 || pp.m > 65535) return cudaErrorInvalidConfiguration;
+    const int cap = pp.page_size * pp.max_pages;  // an item's capacity: kv_lens clamp to it
+    DecodeTcParams p = base_params(pp.q, pp.out, pp.kv_lens, pp.Hq, pp.Hkv, cap, pp.scale, wc);
+    p.sliding = pp.sliding;
+    p.kpool = static_cast<const uint16_t*>(pp.k_pool);
+    p.vpool = static_cast<const uint16_t*>(pp.v_pool);
+    p.page_table = pp.page_table;
+    p.page_size = pp.page_size;
+    p.max_pages = pp.max_pages;
+    p.num_pages = pp.num_pages;
+    // TMA copies whole pages of 8 to 128 rows that divide a 128-key block, or 128-row pieces of
+    // pages that are multiples of 128 rows, through the pools seen as [num_pages * Hkv,
+    // page_size, 128]; other page sizes are gathered row by row
+    const int ps = pp.page_size;
+    p.paged_tma = (((ps >= 8 && ps <= BN && BN % ps == 0) || ps % BN == 0) &&
+                   (long long)pp.num_pages * pp.Hkv <= 0x7fffffffLL) ? 1 : 0;
+    CUtensorMap tk = {}, tv = {};
+    if (p.paged_tma) {
+        const int rows = std::min(ps, BN);
+        if (!encode_kv(&tk, pp.k_pool, ps, (unsigned long long)pp.num_pages * pp.Hkv, rows, pp.f16) ||
+            !encode_kv(&tv, pp.v_pool, ps, (unsigned long long)pp.num_pages * pp.Hkv, rows, pp.f16))
+            return cudaErrorInvalidValue;
+    }
+    const long long span = pp.sliding > 0 ? std::min(pp.sliding, cap) : cap;
+    const int nsplit = choose_splits((long long)pp.m * pp.Hkv, span + BN, num_sms);
+    return launch_src<kSrcPaged>(tk, tv, p, pp.Hq / pp.Hkv, pp.f16, pp.m, nsplit, stream);
 }
 
 }  // namespace attn

@@ -1,5 +1,6 @@
 // kernels.h -- internal (non-exported) launch interface between the C ABI layer
-// and the three attention kernels.
+// and the kernels: the tensor-core prefill (K1), the split-KV decode (K2), the fp32 path
+// (K3), the attention prelude (K4) and the tensor-core decode (K5).
 #pragma once
 
 #include <cuda_runtime.h>
@@ -31,6 +32,13 @@ struct Problem {
     int total;
     // Head-major batch only: out is token-major [B, Lq, Hq, D] instead of [B, Hq, Lq, D].
     bool out_tok = false;
+    // Paged K/V (K1 only, with packed q/out): k and v are pools [num_pages, Hkv, page_size, D];
+    // sequence b's position j is row j % page_size of pool page page_table[b * max_pages +
+    // j / page_size]; kv_lens[b] positions are cached and the sequence's queries are the newest
+    // of them.  Null when K/V are not paged.
+    const int32_t* page_table = nullptr;
+    const int32_t* kv_lens = nullptr;
+    int page_size = 0, max_pages = 0, num_pages = 0;
 };
 
 // Visible key interval [lo, hi) for queries at positions [qpos_lo, qpos_hi]
@@ -63,7 +71,8 @@ __device__ __forceinline__ int valid_keys(const int32_t* key_lens, int b, int Lk
     return n < 0 ? 0 : (n > Lk ? Lk : n);
 }
 
-// K1: tcgen05 + TMA fused prefill, bf16 or fp16, head_dim 64 or 128.
+// K1: tcgen05 + TMA fused prefill, bf16 or fp16, head_dim 64 or 128; head-major, packed, or
+// packed queries over paged K/V.
 cudaError_t launch_prefill_tc(const Problem& p, const WaitCtl& wc, cudaStream_t stream);
 
 // K2: split-KV decode for q_len == 1, bf16 or fp16, head_dim 64 or 128, group size 1/2/4/8.
@@ -73,6 +82,14 @@ cudaError_t launch_decode_splitkv(const Problem& p, const WaitCtl& wc, cudaStrea
 // K5: tensor-core decode for q_len == 1, head_dim 128, 4 or 8 query heads per kv head.
 bool decode_tc_supported(const Problem& p);
 cudaError_t launch_decode_tc(const Problem& p, const WaitCtl& wc, cudaStream_t stream, int num_sms);
+// K5 over per-item caches (rows gathered by the device) or paged caches (TMA per page piece where
+// the page size allows it, rows gathered otherwise), the same shapes.
+bool decode_tc_gather_supported(int Hq, int Hkv, int D);
+bool decode_tc_paged_tma(int page_size, int num_pages, int Hkv);
+struct CachesProblem;
+struct PagedProblem;
+cudaError_t launch_decode_tc_caches(const CachesProblem& p, const WaitCtl& wc, cudaStream_t stream, int num_sms);
+cudaError_t launch_decode_tc_paged(const PagedProblem& p, const WaitCtl& wc, cudaStream_t stream, int num_sms);
 
 // K2 over per-item caches: one single-query decode step for m items, item i reading its
 // own [Hkv, capacity, D] K and V caches through device pointer arrays.

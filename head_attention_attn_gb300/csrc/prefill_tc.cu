@@ -38,6 +38,7 @@
 // realizar cached/attention.rs causal softmax (a fully masked row gives zeros).
 #include "kernels.h"
 
+#include <algorithm>
 #include <mutex>
 
 namespace attn {
@@ -63,7 +64,8 @@ struct Cfg {
     static constexpr int kOffV = kOffK + kStages * kKVBytes;
     static constexpr int kOffX = kOffV + kStages * kKVBytes;          // row-extreme exchange
     static constexpr int kOffL = kOffX + kTiles * 2 * BM * 4;         // row-sum exchange
-    static constexpr int kOffBar = kOffL + kTiles * 2 * BM * 4;
+    static constexpr int kOffRow = kOffL + kTiles * 2 * BM * 4;        // paged: byte offset of each key row
+    static constexpr int kOffBar = kOffRow + BN * 8;
     static constexpr int kSmem = kOffBar + 256 + 1024;
     static constexpr uint32_t kTmemCols = NT == 2 ? 512 : 256;
     static constexpr uint32_t kColS = 0;    // + 128 * tile
@@ -86,6 +88,13 @@ enum : int {
 };
 static_assert(kNumBars * 8 <= 240, "barrier area");
 
+// Where Q, K, V and out live.
+enum : int {
+    kHeadMajor = 0,  // q/out [B, Hq, Lq, D], k/v [B, Hkv, Lk, D]: TMA
+    kPacked = 1,     // packed sequences, token-major q/out [total, Hq, D] and k/v [total, Hkv, D]: TMA
+    kPaged = 2,      // packed token-major q/out, K/V in paged pools: Q by TMA, K/V rows gathered
+};
+
 struct PrefillParams {
     __nv_bfloat16* out;
     const int32_t* key_lens;
@@ -96,7 +105,22 @@ struct PrefillParams {
     int out_tok;        // head-major batch: out is [B, Lq, Hq, D] instead of [B, Hq, Lq, D]
     float scale_log2;
     WaitCtl wc;
+    // kPaged: pools [num_pages, Hkv, page_size, D]; sequence b's position j is row j % page_size of
+    // pool page page_table[b * max_pages + j / page_size]; kv_lens[b] positions are cached and the
+    // sequence's queries are its newest positions
+    const uint8_t* kpool;
+    const uint8_t* vpool;
+    const int32_t* page_table;
+    const int32_t* kv_lens;
+    int page_size, max_pages, num_pages;
 };
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
 __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, const WaitCtl& wc) {
     const unsigned long long t0 = globaltimer_ns();
@@ -162,7 +186,9 @@ __device__ __forceinline__ void tile_bar_sync(int t) {
 // PAIR (two tiles, even group size): the tiles are two query heads of one kv group over the
 // same 128 query rows, so both visit exactly the same key tiles.  Otherwise the tiles are two
 // consecutive 128-row blocks of one query head.
-template <int D, int NT, bool F16, bool TOK, bool PAIR>
+// ZT: some query block may need rows of its last V tile zeroed (the host clears it when it can show
+// that none does; the code is then left out, which the heaviest workloads measurably prefer).
+template <int D, int NT, bool F16, int LAYOUT, bool PAIR, bool ZT>
 __global__ void __launch_bounds__(threads_for<NT>(), 3 - NT)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV, const PrefillParams p) {
@@ -178,6 +204,8 @@ __global__ void __launch_bounds__(threads_for<NT>(), 3 - NT)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    constexpr bool TOK = LAYOUT != kHeadMajor;  // packed token-major q/out
+    constexpr bool PAGED = LAYOUT == kPaged;
 
     int idx = blockIdx.x;
     const int nh = PAIR ? p.Hq / 2 : p.Hq;
@@ -206,7 +234,20 @@ __global__ void __launch_bounds__(threads_for<NT>(), 3 - NT)
         Lq = Lk = s1 - s0;
     }
     if (q0 >= Lq) return;  // a packed sequence shorter than this query block (uniform exit)
-    const int klen = valid_keys(p.key_lens, b, Lk);
+    int P = p.P;
+    int klen;
+    bool bad_item = false;
+    if constexpr (PAGED) {
+        // the sequence's Lq queries are the newest of its kv_lens[b] cached positions
+        const long long cap = (long long)p.page_size * p.max_pages;
+        long long n = __ldg(p.kv_lens + b);
+        n = n < 0 ? 0 : (n > cap ? cap : n);
+        klen = (int)n;
+        P = klen - Lq;
+        bad_item = P < 0;
+    } else {
+        klen = valid_keys(p.key_lens, b, Lk);
+    }
 
     // Visible key interval of each query tile, and the shared key-tile grid.
     long long tlo[kTiles], thi[kTiles];
@@ -220,8 +261,28 @@ __global__ void __launch_bounds__(threads_for<NT>(), 3 - NT)
             continue;
         }
         const int qb = min(qa + BM, Lq) - 1;
-        key_interval(p.mode, p.window, klen, (long long)p.P + qa, (long long)p.P + qb, &tlo[t], &thi[t]);
+        key_interval(p.mode, p.window, klen, (long long)P + qa, (long long)P + qb, &tlo[t], &thi[t]);
         if (thi[t] > tlo[t] && (kv0 < 0 || tlo[t] < kv0)) kv0 = tlo[t];
+    }
+    if constexpr (PAGED) {
+        // Every CTA of the sequence checks the page entries of all the keys its queries can
+        // see, so they agree: a sequence with an entry outside the pool, or with fewer cached
+        // positions than queries, reads nothing and its rows are zeros.
+        long long slo, shi;
+        key_interval(p.mode, p.window, klen, (long long)P, (long long)P + Lq - 1, &slo, &shi);
+        bool bad = false;
+        if (!bad_item && shi > slo) {
+            const int32_t* pages = p.page_table + (size_t)b * p.max_pages;
+            for (long long x = slo / p.page_size + threadIdx.x; x <= (shi - 1) / p.page_size; x += blockDim.x) {
+                const int id = __ldg(pages + x);
+                bad |= (id < 0 || id >= p.num_pages);
+            }
+        }
+        const bool bad_pages = __syncthreads_or(bad);
+        if (bad_item || bad_pages) {
+            if (threadIdx.x == 0) record_status(p.wc.status, bad_pages ? kStatusBadPage : kStatusBadSeqlens);
+            kv0 = -1;
+        }
     }
     TileRange rng[kTiles];
     int ntiles = 0;
@@ -236,20 +297,23 @@ __global__ void __launch_bounds__(threads_for<NT>(), 3 - NT)
         }
     }
     if (kv0 < 0) kv0 = 0;
-    // Rows of the last key tile past every visible key of this CTA's queries get weight 0, and
-    // the tensor core multiplies that 0 into the V row: an Inf or NaN there would still make
-    // the product NaN.  Such rows of the tail V tile are zeroed in shared memory before its P V
-    // products (rows past the tensor already read as zeros from the copy).
-    long long hi_all = 0;
-#pragma unroll
-    for (int t = 0; t < kTiles; ++t)
-        if (thi[t] > tlo[t] && thi[t] > hi_all) hi_all = thi[t];
-    const long long tail_row = kv0 + (long long)(ntiles - 1) * BN;
-    const long long row_limit = TOK ? (long long)p.total - row0 : (long long)Lk;
-    const int zero_lo = (int)(hi_all - tail_row);
-    const int zero_hi = (int)min((long long)BN, row_limit - tail_row);
-    const bool zero_tail = ntiles > 0 && zero_hi > zero_lo;
-
+    // Rows of the last key tile that no query of the sequence sees (past the end of the union of
+    // its queries' bands: key padding, cache rows past the newest query) get weight 0, and the
+    // tensor core multiplies that 0 into the V row: an Inf or NaN there would still make the
+    // product NaN.  Such rows [zero_lo, zero_hi) of the tail V tile are zeroed in shared memory
+    // before its P V products (rows past the tensor already read as zeros from the copy; the
+    // paged gather writes every row past this CTA's keys as zeros).  A row that some query of
+    // the sequence sees is finite for its output to be, so it needs nothing.  Only the producer
+    // computes this.
+    auto tail_rows = [&](int* zlo, int* zhi) -> bool {
+        long long slo, shi;
+        key_interval(p.mode, p.window, klen, (long long)P, (long long)P + Lq - 1, &slo, &shi);
+        const long long tail_row = kv0 + (long long)(ntiles - 1) * BN;
+        const long long row_limit = TOK ? (long long)p.total - row0 : (long long)Lk;
+        *zlo = (int)max(0LL, shi - tail_row);
+        *zhi = (int)min((long long)BN, row_limit - tail_row);
+        return ZT && !PAGED && ntiles > 0 && *zhi > *zlo;
+    };
     const int kbh = b * p.Hkv + hk;
     auto load_q = [&]() {
         mbar_arrive_expect_tx(bar0 + 8 * kBarQFull, kTiles * C::kQBytes);
@@ -262,12 +326,12 @@ __global__ void __launch_bounds__(threads_for<NT>(), 3 - NT)
                     tma_load_3d(sbase + C::kOffQ + t * C::kQBytes + c * (BM * 128), &tmQ, bar0 + 8 * kBarQFull,
                                 c * 64, q0 + tile_dq(t), b * p.Hq + hq + tile_dh(t));
     };
-    auto load_kv = [&](const CUtensorMap* map, int off, int bar, int j) {
+    // (the tail V tile lands on its own barrier, land_tail, when some of its rows must be zeroed first)
+    auto load_kv = [&](const CUtensorMap* map, int off, int bar, int j, bool land_tail) {
         const int s = j % kStages;
         const int krow = (int)kv0 + j * BN;
-        // the tail V tile lands on its own barrier when some of its rows must be zeroed first
-        const uint32_t done = (zero_tail && bar == kBarVFull && j == ntiles - 1) ? bar0 + 8 * kBarVLand
-                                                                                   : bar0 + 8 * (bar + s);
+        const uint32_t done = (land_tail && bar == kBarVFull && j == ntiles - 1) ? bar0 + 8 * kBarVLand
+                                                                                 : bar0 + 8 * (bar + s);
         mbar_arrive_expect_tx(done, C::kKVBytes);
         for (int c = 0; c < C::kChunks; ++c)
             tma_load_3d(sbase + off + s * C::kKVBytes + c * (BN * 128), map, done, c * 64,
@@ -276,24 +340,28 @@ __global__ void __launch_bounds__(threads_for<NT>(), 3 - NT)
     // With one tile per CTA (two CTAs per SM) the first copies go out before the CTA
     // synchronises; with two tiles (one CTA per SM) that delays the CTA's start more than
     // the copies gain, so the producer starts them after the barrier.
-    const int nearly = kTiles == 1 ? min(kStages, ntiles) : 0;  // K/V tiles loaded at entry
+    const int nearly = (kTiles == 1 && !PAGED) ? min(kStages, ntiles) : 0;  // K/V tiles loaded at entry
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kNumBars; ++i) {
             uint32_t count = 1;
             if (i >= kBarPFull && i < kBarPFull + kTiles)
                 count = 8;  // one arrival per softmax warp of the tile
+            if (PAGED && ((i >= kBarKFull && i < kBarKFull + kStages) || (i >= kBarVFull && i < kBarVFull + kStages)))
+                count = 32;  // one arrival per producer lane, after its copies have landed
             mbar_init(bar0 + 8 * i, count);
         }
         *abort_flag = 0;
         mbar_fence_init();
         // Thread 0 is the producer: its first copies start now and land while TMEM is
         // allocated and the CTA synchronises.
-        if (kTiles == 1 && ntiles > 0) {
+        if (kTiles == 1 && !PAGED && ntiles > 0) {
+            int zlo, zhi;
+            const bool zt = tail_rows(&zlo, &zhi);
             load_q();
             for (int j = 0; j < nearly; ++j) {
-                load_kv(&tmK, C::kOffK, kBarKFull, j);
-                load_kv(&tmV, C::kOffV, kBarVFull, j);
+                load_kv(&tmK, C::kOffK, kBarKFull, j, false);
+                load_kv(&tmV, C::kOffV, kBarVFull, j, zt);
             }
         }
     }
@@ -303,29 +371,107 @@ __global__ void __launch_bounds__(threads_for<NT>(), 3 - NT)
     }
     if (kTiles == 2 && warp == 0 && lane == 0) {
         tma_prefetch_desc(&tmQ);
-        tma_prefetch_desc(&tmK);
-        tma_prefetch_desc(&tmV);
+        if (!PAGED) {
+            tma_prefetch_desc(&tmK);
+            tma_prefetch_desc(&tmV);
+        }
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
 
-    if (warp == 0) {
+    if (PAGED && warp == 0) {
+        // ------------------------------------------------------------ gather producer (paged K/V)
+        // Q comes by TMA.  For every key tile the lanes write the byte offset of each of its
+        // 128 rows in the pools (or ~0 past the visible keys) to shared memory, then copy whole
+        // rows, 16 bytes per lane, each unit to its swizzled place (the layout TMA would give).
+        // The copies of K(j) and V(j) are separate items in that order; an item is released to
+        // the MMA issuer once the next one has been issued and its own copies have landed and
+        // are fenced for the tensor core.  One item of lag never waits on itself: K(j) is
+        // released before V(j) needs the V slot freed by PV(j - 2), and V(j) before K(j + 1)
+        // needs the K slot freed by QK(j - 1), while the issuer runs PV(j - 1) before QK(j).
+        if (lane == 0 && ntiles > 0) load_q();
+        if (ntiles > 0) {
+            long long hi_all = 0;  // rows from here on are zeros
+#pragma unroll
+            for (int t = 0; t < kTiles; ++t)
+                if (thi[t] > tlo[t] && thi[t] > hi_all) hi_all = thi[t];
+            unsigned long long* rowoff = reinterpret_cast<unsigned long long*>(smem + C::kOffRow);
+            constexpr int kUnits = C::kChunks * 8;  // 16-byte units of one row
+            constexpr int kRowsPerStep = 32 / kUnits;
+            const int rsub = lane / kUnits, u = lane % kUnits, c = u >> 3, qd = u & 7;
+            const int32_t* pages = p.page_table + (size_t)b * p.max_pages;
+            int items = 0;
+            bool ok = true;
+            for (int j = 0; ok && j < ntiles; ++j) {
+                const int s = j % kStages;
+                const uint32_t n = (uint32_t)(j / kStages);
+                const long long krow0 = kv0 + (long long)j * BN;
+                __syncwarp();
+                for (int r = lane; r < BN; r += 32) {
+                    const long long key = krow0 + r;
+                    unsigned long long off = ~0ull;
+                    if (key < hi_all) {
+                        const long long pg = __ldg(pages + key / p.page_size);
+                        off = (((unsigned long long)pg * p.Hkv + hk) * (unsigned long long)p.page_size +
+                               (unsigned long long)(key % p.page_size)) * (D * 2);
+                    }
+                    rowoff[r] = off;
+                }
+                __syncwarp();
+                for (int kind = 0; kind < 2; ++kind) {  // K(j), then V(j)
+                    const int empty = kind ? kBarVEmpty : kBarKEmpty;
+                    if (j >= kStages &&
+                        !__all_sync(0xffffffffu, mbar_wait(bar0 + 8 * (empty + s), (n - 1) & 1, p.wc, abort_flag))) {
+                        ok = false;
+                        break;
+                    }
+                    const int off_tile = (kind ? C::kOffV : C::kOffK) + s * C::kKVBytes;
+                    const uint8_t* src = kind ? p.vpool : p.kpool;
+#pragma unroll 4
+                    for (int i = 0; i < BN / kRowsPerStep; ++i) {
+                        const int r = kRowsPerStep * i + rsub;
+                        const unsigned long long off = rowoff[r];
+                        const uint32_t dofs = off_tile + c * (BN * 128) + r * 128 + ((qd ^ (r & 7)) << 4);
+                        if (off != ~0ull) cp_async16(sbase + dofs, src + off + u * 16);
+                        else *reinterpret_cast<uint4*>(smem + dofs) = make_uint4(0u, 0u, 0u, 0u);
+                    }
+                    cp_async_commit();
+                    ++items;
+                    if (items >= 2) {  // the item before this one has landed: release it
+                        const int x = items - 2;
+                        cp_async_wait<1>();
+                        fence_proxy_async_smem();
+                        mbar_arrive(bar0 + 8 * (((x & 1) ? kBarVFull : kBarKFull) + (x >> 1) % kStages));
+                    }
+                }
+            }
+            cp_async_wait<0>();  // nothing stays in flight, whatever happened above
+            if (ok) {
+                const int x = items - 1;
+                fence_proxy_async_smem();
+                mbar_arrive(bar0 + 8 * (((x & 1) ? kBarVFull : kBarKFull) + (x >> 1) % kStages));
+            }
+            if (lane == 0) drain_wait(bar0 + 8 * kBarQFull, 0, p.wc);
+        }
+    } else if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
         int issued = 2 * nearly;  // K and V copies issued so far (kept by lane 0)
+        int zero_lo, zero_hi;
+        const bool zero_tail = tail_rows(&zero_lo, &zero_hi);
         if (lane == 0 && ntiles > 0) {
             if (kTiles == 2) load_q();
             for (int j = nearly; j < ntiles; ++j) {
                 const int s = j % kStages;
                 const uint32_t n = (uint32_t)(j / kStages);
                 if (j >= kStages && !mbar_wait(bar0 + 8 * (kBarKEmpty + s), (n - 1) & 1, p.wc, abort_flag)) break;
-                load_kv(&tmK, C::kOffK, kBarKFull, j);
+                load_kv(&tmK, C::kOffK, kBarKFull, j, false);
                 if (j >= kStages && !mbar_wait(bar0 + 8 * (kBarVEmpty + s), (n - 1) & 1, p.wc, abort_flag)) {
                     issued = 2 * j + 1;
                     break;
                 }
-                load_kv(&tmV, C::kOffV, kBarVFull, j);
+                load_kv(&tmV, C::kOffV, kBarVFull, j, zero_tail);
                 issued = 2 * j + 2;
             }
             drain_wait(bar0 + 8 * kBarQFull, 0, p.wc);
@@ -429,7 +575,7 @@ __global__ void __launch_bounds__(threads_for<NT>(), 3 - NT)
         const int row = wq * 32 + lane;
         const int qi = q0 + tile_dq(t) + row;
         const int hqt = hq + tile_dh(t);
-        const long long qpos = (long long)p.P + qi;
+        const long long qpos = (long long)P + qi;
         long long rlo, rhi;
         key_interval(p.mode, p.window, klen, qpos, qpos, &rlo, &rhi);
         const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
@@ -662,12 +808,17 @@ bool encode_16bit_3d_tok(CUtensorMap* map, const void* base, int D, int H, int t
     return r == CUDA_SUCCESS;
 }
 
-template <int D, int NT, bool F16, bool TOK, bool PAIR = false>
+template <int D, int NT, bool F16, int LAYOUT, bool PAIR, bool ZT>
 cudaError_t launch_impl(const Problem& pr, const WaitCtl& wc, cudaStream_t stream) {
     using C = Cfg<D, NT>;
     constexpr int kTiles = NT;
     CUtensorMap tq, tk, tv;
-    if (TOK) {
+    if (LAYOUT == kPaged) {
+        // only Q is copied by TMA; the K and V rows are gathered through the page table
+        if (!encode_16bit_3d_tok(&tq, pr.q, D, pr.Hq, pr.total, F16)) return cudaErrorInvalidValue;
+        tk = tq;
+        tv = tq;
+    } else if (LAYOUT == kPacked) {
         if (!encode_16bit_3d_tok(&tq, pr.q, D, pr.Hq, pr.total, F16) ||
             !encode_16bit_3d_tok(&tk, pr.k, D, pr.Hkv, pr.total, F16) ||
             !encode_16bit_3d_tok(&tv, pr.v, D, pr.Hkv, pr.total, F16))
@@ -685,12 +836,13 @@ cudaError_t launch_impl(const Problem& pr, const WaitCtl& wc, cudaStream_t strea
     {
         std::lock_guard<std::mutex> g(mu);
         if (dev < 64 && !configured[dev]) {
-            e = cudaFuncSetAttribute(prefill_tc_kernel<D, NT, F16, TOK, PAIR>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+            e = cudaFuncSetAttribute(prefill_tc_kernel<D, NT, F16, LAYOUT, PAIR, ZT>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
             if (e != cudaSuccess) return e;
             configured[dev] = true;
         }
     }
-    PrefillParams p;
+    PrefillParams p = {};
     p.out = reinterpret_cast<__nv_bfloat16*>(pr.out);
     p.key_lens = pr.key_lens;
     p.B = pr.B;
@@ -708,35 +860,64 @@ cudaError_t launch_impl(const Problem& pr, const WaitCtl& wc, cudaStream_t strea
     p.out_tok = pr.out_tok ? 1 : 0;
     p.scale_log2 = pr.scale * kLog2e;
     p.wc = wc;
+    if (LAYOUT == kPaged) {
+        p.kpool = static_cast<const uint8_t*>(pr.k);
+        p.vpool = static_cast<const uint8_t*>(pr.v);
+        p.page_table = pr.page_table;
+        p.kv_lens = pr.kv_lens;
+        p.page_size = pr.page_size;
+        p.max_pages = pr.max_pages;
+        p.num_pages = pr.num_pages;
+    }
     const long long grid = (long long)p.num_m * pr.B * (PAIR ? pr.Hq / 2 : pr.Hq);
     if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    prefill_tc_kernel<D, NT, F16, TOK, PAIR><<<(unsigned)grid, threads_for<NT>(), C::kSmem, stream>>>(tq, tk, tv, p);
+    prefill_tc_kernel<D, NT, F16, LAYOUT, PAIR, ZT><<<(unsigned)grid, threads_for<NT>(), C::kSmem, stream>>>(tq, tk, tv, p);
     return cudaGetLastError();
+}
+
+// Whether the tail zeroing can matter for a head-major call: only key padding, or a mask whose
+// band (the union over all queries) ends before kv_len, leaves rows inside the tensor that no
+// query sees.
+bool tail_zero_needed(const Problem& p) {
+    if (p.key_lens != nullptr || p.cu_seqlens != nullptr) return true;
+    long long slo, shi;
+    key_interval(p.mode, p.window, p.Lk, (long long)p.pos_offset, (long long)p.pos_offset + p.Lq - 1, &slo, &shi);
+    return shi < p.Lk;
+}
+
+template <int D, int NT, bool F16, int LAYOUT, bool PAIR>
+cudaError_t launch_zt(const Problem& p, const WaitCtl& wc, cudaStream_t stream) {
+    if constexpr (LAYOUT == kHeadMajor) {
+        if (!tail_zero_needed(p)) return launch_impl<D, NT, F16, LAYOUT, PAIR, false>(p, wc, stream);
+    }
+    return launch_impl<D, NT, F16, LAYOUT, PAIR, LAYOUT != kPaged>(p, wc, stream);
+}
+
+template <int LAYOUT>
+cudaError_t launch_layout(const Problem& p, const WaitCtl& wc, cudaStream_t stream) {
+    // head_dim 64: one query tile per CTA, so two CTAs share an SM (256 TMEM columns and
+    // about 83 KB of shared memory each) and hide each other's set-up and epilogue.
+    // head_dim 128: two tiles per CTA (512 TMEM columns, one CTA per SM), ping-pong inside;
+    // an even group size pairs two query heads of one kv group over the same rows.
+    if (p.D == 64)
+        return p.f16 ? launch_zt<64, 1, true, LAYOUT, false>(p, wc, stream)
+                     : launch_zt<64, 1, false, LAYOUT, false>(p, wc, stream);
+    if (p.D == 128) {
+        if ((p.Hq / p.Hkv) % 2 == 0)
+            return p.f16 ? launch_zt<128, 2, true, LAYOUT, true>(p, wc, stream)
+                         : launch_zt<128, 2, false, LAYOUT, true>(p, wc, stream);
+        return p.f16 ? launch_zt<128, 2, true, LAYOUT, false>(p, wc, stream)
+                     : launch_zt<128, 2, false, LAYOUT, false>(p, wc, stream);
+    }
+    return cudaErrorInvalidValue;
 }
 
 }  // namespace
 
 cudaError_t launch_prefill_tc(const Problem& p, const WaitCtl& wc, cudaStream_t stream) {
-    // head_dim 64: one query tile per CTA, so two CTAs share an SM (256 TMEM columns and
-    // about 83 KB of shared memory each) and hide each other's set-up and epilogue.
-    // head_dim 128: two tiles per CTA (512 TMEM columns, one CTA per SM), ping-pong inside.
-    const bool tok = p.cu_seqlens != nullptr;
-    if (p.D == 64) {
-        if (tok) return p.f16 ? launch_impl<64, 1, true, true>(p, wc, stream) : launch_impl<64, 1, false, true>(p, wc, stream);
-        return p.f16 ? launch_impl<64, 1, true, false>(p, wc, stream) : launch_impl<64, 1, false, false>(p, wc, stream);
-    }
-    if (p.D == 128) {
-        // an even group size pairs two query heads of one kv group over the same rows
-        if ((p.Hq / p.Hkv) % 2 == 0) {
-            if (tok) return p.f16 ? launch_impl<128, 2, true, true, true>(p, wc, stream)
-                                  : launch_impl<128, 2, false, true, true>(p, wc, stream);
-            return p.f16 ? launch_impl<128, 2, true, false, true>(p, wc, stream)
-                         : launch_impl<128, 2, false, false, true>(p, wc, stream);
-        }
-        if (tok) return p.f16 ? launch_impl<128, 2, true, true>(p, wc, stream) : launch_impl<128, 2, false, true>(p, wc, stream);
-        return p.f16 ? launch_impl<128, 2, true, false>(p, wc, stream) : launch_impl<128, 2, false, false>(p, wc, stream);
-    }
-    return cudaErrorInvalidValue;
+    if (p.page_table != nullptr) return launch_layout<kPaged>(p, wc, stream);
+    if (p.cu_seqlens != nullptr) return launch_layout<kPacked>(p, wc, stream);
+    return launch_layout<kHeadMajor>(p, wc, stream);
 }
 
 }  // namespace attn

@@ -287,6 +287,64 @@ ATTN_API attn_status attn_qkv_prelude_caches(const void* qkv, const float* q_nor
                                              void* cuda_stream);
 
 /*
+ * attn_fwd_varlen_paged -- attention of packed multi-token query chunks against paged KV
+ * caches: chunked prefill and multi-token verification over the caches of attn_decode_paged.
+ *
+ * Source: ferrum-kernels Backend::transpose_token_to_head names the CUDA paged-KV path,
+ * paged_varlen_attention, whose output is token-major, and paged_decode_attention built on
+ * it; the pages give no layout.  The reading taken here: the queries are packed as in
+ * attn_fwd_varlen (ripvec-core Driver::prepare_batch_unpadded, cu_seqlens), the caches are
+ * the pages of attn_decode_paged, and a sequence's queries are the newest positions of its
+ * cache (its tokens were appended before the call, as ferrum-kernels
+ * Backend::split_qkv_norm_rope_into_cache does).
+ *
+ * Layout (caller-owned device memory, contiguous):
+ *   q, out        [total_q, q_heads, head_dim], token-major; sequence b's queries are rows
+ *                 [cu_seqlens_q[b], cu_seqlens_q[b+1]).
+ *   k_pool, v_pool
+ *                 [num_pages, kv_heads, page_size, head_dim]; sequence b's cached position j is
+ *                 row j % page_size of pool page page_table[b][j / page_size].
+ *   page_table    device int32 [batch, max_pages].  Pages may be shared.
+ *   cu_seqlens_q  device int32 [batch + 1].
+ *   kv_lens       device int32 [batch]: the cached positions of sequence b, clamped to
+ *                 [0, max_pages * page_size], its len_b = cu_seqlens_q[b+1] - cu_seqlens_q[b]
+ *                 queries included.
+ *
+ * Query i of sequence b sits at position kv_lens[b] - len_b + i and sees the cached
+ * positions that mask_mode and window allow at that position (attn_mask_mode): causal for
+ * chunked prefill, the causal window for a sliding-window model.  Query head h reads kv head
+ * h / (q_heads / kv_heads).  Rows of out outside every sequence are not written.
+ *
+ * Arguments: batch (sequences), total_q (rows of q and out), max_seqlen_q (an upper bound on
+ * every len_b; it sizes the launch), num_pages, page_size (>= 1), max_pages, mask_mode,
+ * window, scale, dtype (ATTN_BF16 or ATTN_F16), cuda_stream as for attn_fwd.
+ *
+ * Supported: head_dim 64 or 128; otherwise ATTN_ERR_UNSUPPORTED.  batch 0 or max_seqlen_q 0
+ * launches nothing.  Key rows no query sees never reach out, whatever they hold.
+ *
+ * Errors: host-visible arguments are checked before the launch (ATTN_ERR_INVALID_ARG for
+ * negative sizes, page_size < 1, max_pages * page_size above 2^31-1, max_seqlen_q >
+ * total_q, null or misaligned pointers: 16 bytes for q, out and the pools, 4 bytes for the
+ * int32 arrays).  Device-side values are checked on the device and reported by
+ * attn_sync_status() as ATTN_ERR_INVALID_ARG:
+ *   - a sequence whose cu_seqlens_q bounds are not inside [0, total_q], run backwards or
+ *     exceed max_seqlen_q is not read and its rows are not written;
+ *   - a sequence with fewer cached positions than queries, or with a page-table entry
+ *     outside [0, num_pages) among the positions its queries see, reads nothing and its rows
+ *     are written as zeros.
+ *
+ * The result equals attn_fwd per sequence over the gathered cache (q_len len_b, pos_offset
+ * kv_lens[b] - len_b, key_lens kv_lens[b]), bit for bit where both run the prefill kernel.
+ * The library allocates nothing and keeps no pointer after the call.
+ */
+ATTN_API attn_status attn_fwd_varlen_paged(const void* q, const void* k_pool, const void* v_pool,
+                                           const int32_t* page_table, void* out, const int32_t* cu_seqlens_q,
+                                           const int32_t* kv_lens, int batch, int total_q, int max_seqlen_q,
+                                           int q_heads, int kv_heads, int num_pages, int page_size,
+                                           int max_pages, int head_dim, int mask_mode, int window, float scale,
+                                           int dtype, void* cuda_stream);
+
+/*
  * attn_decode_caches -- one decode step for m items, each against its own KV cache, in
  * one launch.
  *
@@ -380,8 +438,9 @@ ATTN_API const char* attn_last_error(void);
  * device status word on the current device.
  *
  * Every wait of a kernel on a shared-memory barrier (data arriving, the tensor
- * core finishing, another warp's result) is bounded: it gives up after 2 s, or
- * after 1 ms once another block has recorded a time-out.  A wait that gives up
+ * core finishing, another warp's result) is bounded: it gives up after 250 ms (a
+ * healthy wait lasts microseconds), so a launch whose waits fail ends after about
+ * that long per wave of blocks.  A wait that gives up
  * records a code in this word, waits (again bounded) for its own copies and
  * products in flight, releases its tensor memory and exits its block.  The
  * hardware barriers (a block's __syncthreads, the decode kernels' cluster

@@ -54,13 +54,14 @@ def test_decode_caches_match_oracle(D, G, window):
     assert_close(out.double().cpu().numpy(), ref, "bf16", f"decode caches D={D} G={G} w={window}")
 
 
-@pytest.mark.parametrize("Hq", [4, 8])
-def test_decode_caches_agree_with_contiguous_decode(Hq):
-    """Per-item caches all at full length against attn_fwd over one contiguous cache: with
-    group 1 or 2 both run the same CUDA-core kernel and agree bit for bit; with group 4 attn_fwd
-    runs the tensor-core decode, so both are checked against the oracle instead."""
-    m, Hkv, cap, D = 4, 2, 900, 128
-    q, ks, vs, _ = _case(m, Hq, Hkv, cap, D, [cap] * m, seed=3)
+@pytest.mark.parametrize("Hq,cap,m", [(4, 900, 4), (8, 900, 4), (16, 900, 4), (8, 5000, 2), (16, 3000, 1)])
+def test_decode_caches_agree_with_contiguous_decode(Hq, cap, m):
+    """Per-item caches all at full length against attn_fwd over one contiguous cache: with 1, 2
+    or 8 query heads per kv head both run the same kernel with the same split of the keys (the
+    CUDA-core decode, or the tensor-core decode, which then gathers the rows itself instead of
+    using TMA), so they agree bit for bit; everything is also checked against the oracle."""
+    Hkv, D = 2, 128
+    q, ks, vs, _ = _case(m, Hq, Hkv, cap, D, [cap] * m, seed=3 + Hq + cap)
     kl = torch.full((m,), cap, dtype=torch.int32, device=DEV)
     a = attn.attn_decode_caches(q.to(DEV), [k.to(DEV) for k in ks], [v.to(DEV) for v in vs], kl)
     k4 = torch.stack(ks).to(DEV)
@@ -68,13 +69,11 @@ def test_decode_caches_agree_with_contiguous_decode(Hq):
     b = attn.attn_fwd(q.to(DEV)[:, :, None, :].contiguous(), k4, v4, pos_offset=cap - 1, mask_mode=MASK_CAUSAL)
     torch.cuda.synchronize()
     assert attn.sync_status() == attn.ATTN_OK, attn.last_error()
-    if Hq // Hkv <= 2:
+    if Hq // Hkv != 4:  # group 4: per-item caches run the CUDA-core decode, attn_fwd the tensor-core one
         assert torch.equal(a, b[:, :, 0, :])
-    else:
-        ref = oracle.attention(q[:, :, None, :], torch.stack(ks), torch.stack(vs), pos_offset=cap - 1,
-                               mask_mode=MASK_CAUSAL, scale=float(torch.tensor(1.0 / D ** 0.5, dtype=torch.float32)))
-        assert_close(a.double().cpu().numpy(), ref[:, :, 0, :], "bf16", "caches")
-        assert_close(b[:, :, 0, :].double().cpu().numpy(), ref[:, :, 0, :], "bf16", "contiguous")
+    ref = oracle.attention(q[:, :, None, :], torch.stack(ks), torch.stack(vs), pos_offset=cap - 1,
+                           mask_mode=MASK_CAUSAL, scale=float(torch.tensor(1.0 / D ** 0.5, dtype=torch.float32)))
+    assert_close(a.double().cpu().numpy(), ref[:, :, 0, :], "bf16", "caches")
 
 
 def test_decode_caches_bad_pointer_is_reported_not_read():
@@ -93,3 +92,41 @@ def test_decode_caches_bad_pointer_is_reported_not_read():
     assert "misaligned" in attn.last_error() or "aligned" in attn.last_error()
     assert torch.all(out[1] == 0)
     assert attn.sync_status() == attn.ATTN_OK
+
+
+@pytest.mark.parametrize("cap,offset,m", [(900, 16, 3), (3000, 48, 2), (100, 0, 3), (1000, 0, 3), (5000, 0, 1)])
+@pytest.mark.parametrize("window", [0, 333])
+def test_tensor_core_caches_gather(cap, offset, m, window):
+    """Per-item caches at 8 query heads per kv head run the tensor-core decode, whose producer
+    warps gather every row (16 bytes per lane) into the tiles TMA would give, whatever the
+    caches' alignment beyond 16 bytes, their capacity or the lengths.  Without a window the result
+    equals attn_fwd over one contiguous cache with the same lengths (the same kernel and split of
+    the keys) bit for bit; every case is also checked against the oracle."""
+    Hq, Hkv, D = 16, 2, 128
+    g = torch.Generator().manual_seed(cap + offset + window)
+    q = torch.randn(m, Hq, D, generator=g).bfloat16()
+    k4 = torch.randn(m, Hkv, cap, D, generator=g).bfloat16()
+    v4 = torch.randn(m, Hkv, cap, D, generator=g).bfloat16()
+    lens = [cap, max(1, cap // 3), max(1, cap - 7)][:m]
+    kd, vd, keep = [], [], []  # each item's cache `offset` bytes into its own allocation
+    for i in range(m):
+        for src, dst in ((k4[i], kd), (v4[i], vd)):
+            buf = torch.empty(src.numel() * 2 + 1024, dtype=torch.uint8, device=DEV)
+            view = buf[offset:offset + src.numel() * 2].view(torch.bfloat16).view(Hkv, cap, D)
+            view.copy_(src.to(DEV))
+            dst.append(view)
+            keep.append(buf)
+    kl = torch.tensor(lens, dtype=torch.int32, device=DEV)
+    sc = float(torch.tensor(1.0 / D ** 0.5, dtype=torch.float32))
+    a = attn.attn_decode_caches(q.to(DEV), kd, vd, kl, sliding_window=window, scale=sc)
+    torch.cuda.synchronize()
+    assert attn.sync_status() == attn.ATTN_OK, attn.last_error()
+    ref = _reference(q, list(k4), list(v4), kl.cpu(), window, sc)
+    assert_close(a.double().cpu().numpy(), ref, "bf16", f"caches cap={cap} offset={offset} w={window}")
+    if window == 0:
+        # item i's query at position lens[i] - 1 sees positions 0 .. lens[i] - 1: the contiguous
+        # decode at pos_offset cap - 1 with key_lens = lens sees the same
+        b = attn.attn_fwd(q.to(DEV)[:, :, None, :].contiguous(), k4.to(DEV), v4.to(DEV), key_lens=kl,
+                          pos_offset=cap - 1, mask_mode=MASK_CAUSAL, scale=sc)
+        torch.cuda.synchronize()
+        assert torch.equal(a, b[:, :, 0, :])

@@ -71,8 +71,33 @@ def run_both(q, k_pool, v_pool, table, kl, window):
     return paged, cont, kc.cpu(), vc.cpu(), scale
 
 
-@pytest.mark.parametrize("D,G", [(128, 4), (128, 1), (64, 8), (64, 2)])
-@pytest.mark.parametrize("page_size,window", [(16, 0), (48, 300), (100, 0), (1, 0), (2048, 64)])
+def tma_page(page_size):
+    """Page sizes the tensor-core decode copies by TMA: whole pages of 8 to 128 rows dividing 128,
+    or multiples of 128 rows."""
+    return (8 <= page_size <= 128 and 128 % page_size == 0) or page_size % 128 == 0
+
+
+def paged_on_tensor_cores(G, page_size):
+    """The faster kernel for paged caches at head_dim 128, as measured: the tensor-core decode at
+    4 query heads per kv head when TMA copies pages of 32 rows or more, at 8 when TMA can copy the
+    pages or they are shorter than 4 rows (gathered); the CUDA-core decode otherwise."""
+    if G == 4:
+        return tma_page(page_size) and page_size >= 32
+    return G == 8 and (tma_page(page_size) or page_size < 4)
+
+
+def same_kernel(D, G, page_size):
+    """Paged and per-item caches run the same kernel, and then agree bit for bit: the CUDA-core
+    decode for both, or the tensor-core decode for both (per-item caches at group 8, gathered row
+    by row into the tiles TMA gives the paged pages)."""
+    if D != 128 or G in (1, 2):
+        return True
+    caches_tc = G == 8
+    return caches_tc == paged_on_tensor_cores(G, page_size)
+
+
+@pytest.mark.parametrize("D,G", [(128, 4), (128, 8), (128, 1), (64, 8), (64, 2)])
+@pytest.mark.parametrize("page_size,window", [(16, 0), (48, 300), (100, 0), (1, 0), (2048, 64), (32, 0), (8, 77)])
 def test_paged_equals_gathered_caches(D, G, page_size, window):
     Hkv, m = 2, 4
     max_pages = max(1, 1500 // page_size) if page_size > 1 else 300
@@ -81,24 +106,28 @@ def test_paged_equals_gathered_caches(D, G, page_size, window):
     q, kp, vp, table, kl = paged_case(m, G * Hkv, Hkv, D, page_size, max_pages, 2 * max_pages + 3, lens,
                                       seed=31 * D + G + page_size + window)
     paged, cont, kc, vc, scale = run_both(q, kp, vp, table, kl, window)
-    assert torch.equal(paged, cont)
+    if same_kernel(D, G, page_size):
+        assert torch.equal(paged, cont)
     ref = reference(q, kc, vc, kl, window, scale)
     assert_close(paged.double().cpu().numpy(), ref, "bf16", f"paged D={D} G={G} ps={page_size} w={window}")
+    assert_close(cont.double().cpu().numpy(), ref, "bf16", f"gathered D={D} G={G} ps={page_size} w={window}")
 
 
-def test_paged_f16_against_oracle():
+@pytest.mark.parametrize("window", [0, 200])
+def test_paged_f16_against_oracle(window):
     q, kp, vp, table, kl = paged_case(3, 8, 2, 128, 64, 20, 50, [1000, 17, 1280], seed=77, dtype=torch.float16)
-    paged, cont, kc, vc, scale = run_both(q, kp, vp, table, kl, 0)
-    assert torch.equal(paged, cont)
-    ref = reference(q, kc, vc, kl, 0, scale)
+    paged, cont, kc, vc, scale = run_both(q, kp, vp, table, kl, window)
+    ref = reference(q, kc, vc, kl, window, scale)
     assert_close(paged.double().cpu().numpy(), ref, "f16", "paged f16")
+    assert_close(cont.double().cpu().numpy(), ref, "f16", "gathered f16")
 
 
-def test_bad_page_entry_is_reported_and_that_item_zeroed():
-    q, kp, vp, table, kl = paged_case(3, 4, 2, 64, 32, 8, 10, [200, 200, 200], seed=78)
+@pytest.mark.parametrize("Hq,D", [(4, 64), (8, 128)])  # the CUDA-core and the tensor-core decode
+def test_bad_page_entry_is_reported_and_that_item_zeroed(Hq, D):
+    q, kp, vp, table, kl = paged_case(3, Hq, 2, D, 32, 8, 10, [200, 200, 200], seed=78)
     table[1, 3] = 10  # one past the pool: item 1 sees positions up to 199, page 3 is visible
     table[2, 7] = -1  # outside item 2's visible positions (pages 0..6): never read, no error
-    scale = float(torch.tensor(1.0 / 8.0, dtype=torch.float32))
+    scale = float(torch.tensor(1.0 / D ** 0.5, dtype=torch.float32))
     out = attn.attn_decode_paged(q.to(DEV), kp.to(DEV), vp.to(DEV), table.to(DEV), kl.to(DEV), scale=scale)
     torch.cuda.synchronize()
     assert attn.sync_status() == attn.ATTN_ERR_INVALID_ARG
@@ -129,3 +158,21 @@ def test_zero_capacity_zero_fills():
     torch.cuda.synchronize()
     assert attn.sync_status() == attn.ATTN_OK, attn.last_error()
     assert torch.all(out == 0)
+
+
+@pytest.mark.parametrize("G", [4, 8])
+@pytest.mark.parametrize("page_size", [16, 8, 32, 128, 256, 2])
+def test_tensor_core_paged_decode_splits(G, page_size):
+    """Few items with long caches: the tensor-core decode splits each item's keys over a
+    cluster; paged and gathered caches still agree bit for bit and match the oracle."""
+    Hkv, m, D = 2, 2, 128
+    max_pages = 6000 // page_size
+    cap = max_pages * page_size
+    q, kp, vp, table, kl = paged_case(m, G * Hkv, Hkv, D, page_size, max_pages, max_pages + 7, [cap, cap - 1234],
+                                      seed=90 + G + page_size)
+    paged, cont, kc, vc, scale = run_both(q, kp, vp, table, kl, 0)
+    if same_kernel(D, G, page_size):
+        assert torch.equal(paged, cont)
+    ref = reference(q, kc, vc, kl, 0, scale)
+    assert_close(paged.double().cpu().numpy(), ref, "bf16", f"paged splits G={G} ps={page_size}")
+    assert_close(cont.double().cpu().numpy(), ref, "bf16", f"gathered splits G={G} ps={page_size}")

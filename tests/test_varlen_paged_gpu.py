@@ -1,0 +1,182 @@
+"""Packed multi-token query chunks against paged KV caches (attn_fwd_varlen_paged).
+
+Sequence b has len_b packed queries, the newest of its kv_lens[b] cached positions (chunked
+prefill, multi-token verification); its cache lives in pages of two pools addressed by
+page_table[b].  Gathering the pages back into one [Hkv, capacity, D] cache and calling attn_fwd
+per sequence (q_len len_b, pos_offset kv_lens[b] - len_b, key_lens kv_lens[b]) runs the same
+prefill kernel on the same shared-memory tiles, so the two agree bit for bit; both are checked
+against the fp64 oracle.  Pool rows outside every sequence's cached positions hold NaN, which
+must never reach the output.
+"""
+import numpy as np
+import pytest
+import torch
+
+import head_attention_attn_gb300 as attn
+import oracle
+from head_attention_attn_gb300.inputs import MASK_CAUSAL, MASK_CAUSAL_WINDOW, MASK_NONE, MASK_WINDOW
+from parity_util import assert_close, to_numpy_f64
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _library():
+    from head_attention_attn_gb300 import build
+    build.build_library()
+    attn.load()
+    yield
+    assert attn.sync_status() == attn.ATTN_OK, attn.last_error()
+
+
+def scale_of(D):
+    return float(torch.tensor(1.0 / D ** 0.5, dtype=torch.float32))
+
+
+def paged_chunks(q_lens, kv_lens, Hq, Hkv, D, page_size, seed, dtype=torch.bfloat16, spare_pages=5):
+    """Packed queries, per-sequence caches scattered over shuffled pool pages (unused rows NaN)."""
+    g = torch.Generator().manual_seed(seed)
+    B = len(q_lens)
+    max_pages = max(1, -(-max(kv_lens) // page_size))
+    cap = max_pages * page_size
+    total = int(sum(q_lens))
+    q = torch.randn(total, Hq, D, generator=g).to(dtype)
+    caches_k = torch.randn(B, Hkv, cap, D, generator=g).to(dtype)
+    caches_v = torch.randn(B, Hkv, cap, D, generator=g).to(dtype)
+    for b in range(B):  # positions past kv_lens[b] hold NaN in the gathered view too
+        caches_k[b, :, kv_lens[b]:] = float("nan")
+        caches_v[b, :, kv_lens[b]:] = float("nan")
+    num_pages = B * max_pages + spare_pages
+    perm = torch.randperm(num_pages, generator=g)[: B * max_pages]
+    table = perm.view(B, max_pages).to(torch.int32)
+    k_pool = torch.full((num_pages, Hkv, page_size, D), float("nan"), dtype=dtype)
+    v_pool = torch.full_like(k_pool, float("nan"))
+    for b in range(B):
+        for j in range(max_pages):
+            k_pool[table[b, j]] = caches_k[b, :, j * page_size:(j + 1) * page_size]
+            v_pool[table[b, j]] = caches_v[b, :, j * page_size:(j + 1) * page_size]
+    cu = torch.tensor(np.concatenate([[0], np.cumsum(q_lens)]), dtype=torch.int32)
+    return q, k_pool, v_pool, table, cu, torch.tensor(kv_lens, dtype=torch.int32), caches_k, caches_v
+
+
+def run_paged(q, k_pool, v_pool, table, cu, kl, mode, window, sc, out=None):
+    out = attn.attn_fwd_varlen_paged(q.to(DEV), k_pool.to(DEV), v_pool.to(DEV), table.to(DEV), cu.to(DEV),
+                                     kl.to(DEV), int((cu[1:] - cu[:-1]).max()), out=out, mask_mode=mode,
+                                     window=window, scale=sc)
+    torch.cuda.synchronize()
+    return out
+
+
+CASES = [
+    # q_lens, kv_lens: chunks that straddle pages, a whole prefill, one-token and empty chunks
+    ([100, 300, 1, 0, 129, 64], [137, 300, 1000, 50, 700, 64]),
+]
+
+
+@pytest.mark.parametrize("D,Hq,Hkv", [(64, 4, 2), (128, 4, 2), (128, 3, 1), (128, 8, 1)])
+@pytest.mark.parametrize("page_size", [16, 7, 1, 256])
+@pytest.mark.parametrize("mode,window", [(MASK_CAUSAL, 0), (MASK_CAUSAL_WINDOW, 150)])
+def test_paged_chunks_equal_gathered_prefill(D, Hq, Hkv, page_size, mode, window):
+    q_lens, kv_lens = CASES[0]
+    q, kp, vp, table, cu, kl, ck, cv = paged_chunks(q_lens, kv_lens, Hq, Hkv, D, page_size,
+                                                    seed=D + Hq * 10 + page_size + mode)
+    sc = scale_of(D)
+    out = run_paged(q, kp, vp, table, cu, kl, mode, window, sc)
+    assert attn.sync_status() == attn.ATTN_OK, attn.last_error()
+    got = to_numpy_f64(out)
+    for b, (n, klen) in enumerate(zip(q_lens, kv_lens)):
+        if n == 0:
+            continue
+        s0 = int(cu[b])
+        qb = q[s0:s0 + n].permute(1, 0, 2)[None].contiguous()        # [1, Hq, n, D]
+        kb, vb = ck[b:b + 1], cv[b:b + 1]                           # [1, Hkv, cap, D]
+        P = klen - n
+        ref = oracle.attention(qb, kb, vb, pos_offset=P, mask_mode=mode, window=window, key_lens=[klen], scale=sc)
+        assert_close(got[s0:s0 + n], ref[0].transpose(1, 0, 2), "bf16", f"seq {b} (len {n}, kv {klen})")
+        if n > 1:  # the same prefill kernel through attn_fwd over the gathered cache: bit for bit
+            fwd = attn.attn_fwd(qb.to(DEV), kb.to(DEV), vb.to(DEV), key_lens=torch.tensor([klen], dtype=torch.int32,
+                                device=DEV), pos_offset=P, mask_mode=mode, window=window, scale=sc)
+            torch.cuda.synchronize()
+            assert torch.equal(fwd[0].transpose(0, 1).cpu(), out[s0:s0 + n].cpu()), f"seq {b}"
+    assert attn.sync_status() == attn.ATTN_OK, attn.last_error()
+
+
+@pytest.mark.parametrize("mode,window", [(MASK_NONE, 0), (MASK_WINDOW, 64)])
+def test_paged_chunks_other_masks_against_oracle(mode, window):
+    q_lens, kv_lens = [50, 200, 7], [90, 200, 400]
+    D, Hq, Hkv = 128, 4, 2
+    q, kp, vp, table, cu, kl, ck, cv = paged_chunks(q_lens, kv_lens, Hq, Hkv, D, 32, seed=11 + mode)
+    sc = scale_of(D)
+    got = to_numpy_f64(run_paged(q, kp, vp, table, cu, kl, mode, window, sc))
+    assert attn.sync_status() == attn.ATTN_OK, attn.last_error()
+    for b, (n, klen) in enumerate(zip(q_lens, kv_lens)):
+        s0 = int(cu[b])
+        ref = oracle.attention(q[s0:s0 + n].permute(1, 0, 2)[None], ck[b:b + 1], cv[b:b + 1], pos_offset=klen - n,
+                               mask_mode=mode, window=window, key_lens=[klen], scale=sc)
+        assert_close(got[s0:s0 + n], ref[0].transpose(1, 0, 2), "bf16", f"seq {b}")
+
+
+def test_paged_chunks_f16():
+    q_lens, kv_lens = [130, 5], [500, 5]
+    q, kp, vp, table, cu, kl, ck, cv = paged_chunks(q_lens, kv_lens, 8, 2, 128, 16, seed=12, dtype=torch.float16)
+    sc = scale_of(128)
+    out = run_paged(q, kp, vp, table, cu, kl, MASK_CAUSAL, 0, sc)
+    assert attn.sync_status() == attn.ATTN_OK, attn.last_error()
+    assert out.dtype == torch.float16
+    got = to_numpy_f64(out)
+    for b, (n, klen) in enumerate(zip(q_lens, kv_lens)):
+        s0 = int(cu[b])
+        ref = oracle.attention(q[s0:s0 + n].permute(1, 0, 2)[None], ck[b:b + 1], cv[b:b + 1], pos_offset=klen - n,
+                               mask_mode=MASK_CAUSAL, key_lens=[klen], scale=sc)
+        assert_close(got[s0:s0 + n], ref[0].transpose(1, 0, 2), "f16", f"seq {b}")
+
+
+def test_bad_page_entry_zeroes_only_that_sequence():
+    q_lens, kv_lens = [40, 60, 30], [300, 200, 100]
+    q, kp, vp, table, cu, kl, ck, cv = paged_chunks(q_lens, kv_lens, 4, 2, 64, 32, seed=13)
+    table[1, 2] = table.max() + 100       # inside sequence 1's cached positions: reported, rows zeroed
+    table[2, 5] = -7                      # past sequence 2's 100 positions (pages 0..3): never read
+    sc = scale_of(64)
+    out = torch.full((q.shape[0], 4, 64), 5.0, dtype=torch.bfloat16, device=DEV)
+    run_paged(q, kp, vp, table, cu, kl, MASK_CAUSAL, 0, sc, out=out)
+    assert attn.sync_status() == attn.ATTN_ERR_INVALID_ARG
+    assert "page" in attn.last_error()
+    assert attn.sync_status() == attn.ATTN_OK
+    got = to_numpy_f64(out)
+    assert np.all(got[40:100] == 0)
+    for b in (0, 2):
+        s0, n, klen = int(cu[b]), q_lens[b], kv_lens[b]
+        ref = oracle.attention(q[s0:s0 + n].permute(1, 0, 2)[None], ck[b:b + 1], cv[b:b + 1], pos_offset=klen - n,
+                               mask_mode=MASK_CAUSAL, key_lens=[klen], scale=sc)
+        assert_close(got[s0:s0 + n], ref[0].transpose(1, 0, 2), "bf16", f"seq {b}")
+
+
+def test_fewer_cached_positions_than_queries_is_reported():
+    q_lens, kv_lens = [50, 20], [40, 100]  # sequence 0 has 50 queries but only 40 cached positions
+    q, kp, vp, table, cu, kl, ck, cv = paged_chunks(q_lens, kv_lens, 4, 4, 128, 16, seed=14)
+    sc = scale_of(128)
+    out = torch.full((q.shape[0], 4, 128), 5.0, dtype=torch.bfloat16, device=DEV)
+    run_paged(q, kp, vp, table, cu, kl, MASK_CAUSAL, 0, sc, out=out)
+    assert attn.sync_status() == attn.ATTN_ERR_INVALID_ARG
+    assert attn.sync_status() == attn.ATTN_OK
+    got = to_numpy_f64(out)
+    assert np.all(got[:50] == 0)
+    ref = oracle.attention(q[50:70].permute(1, 0, 2)[None], ck[1:2], cv[1:2], pos_offset=80, mask_mode=MASK_CAUSAL,
+                           key_lens=[100], scale=sc)
+    assert_close(got[50:70], ref[0].transpose(1, 0, 2), "bf16", "seq 1")
+
+
+def test_bad_cu_seqlens_is_reported_and_not_written():
+    q_lens, kv_lens = [30, 30], [30, 60]
+    q, kp, vp, table, cu, kl, ck, cv = paged_chunks(q_lens, kv_lens, 4, 2, 64, 16, seed=15)
+    cu_bad = cu.clone()
+    cu_bad[2] = 61  # past total_q = 60
+    out = torch.full((q.shape[0], 4, 64), 5.0, dtype=torch.bfloat16, device=DEV)
+    attn.attn_fwd_varlen_paged(q.to(DEV), kp.to(DEV), vp.to(DEV), table.to(DEV), cu_bad.to(DEV), kl.to(DEV), 31,
+                               out=out, scale=0.125)
+    torch.cuda.synchronize()
+    assert attn.sync_status() == attn.ATTN_ERR_INVALID_ARG
+    assert attn.sync_status() == attn.ATTN_OK
+    assert torch.all(out[30:] == 5.0)                     # sequence 1 is not written
+    assert torch.isfinite(out[:30].float()).all() and not torch.all(out[:30] == 5.0)
