@@ -75,6 +75,10 @@ __device__ __forceinline__ int valid_keys(const int32_t* key_lens, int b, int Lk
 // packed queries over paged K/V.
 cudaError_t launch_prefill_tc(const Problem& p, const WaitCtl& wc, cudaStream_t stream);
 
+// K6: the head_dim 64 prefill with 64-key blocks and four CTAs per SM (head-major or packed).
+bool prefill_narrow_supported(const Problem& p);
+cudaError_t launch_prefill_narrow(const Problem& p, const WaitCtl& wc, cudaStream_t stream);
+
 // K2: split-KV decode for q_len == 1, bf16 or fp16, head_dim 64 or 128, group size 1/2/4/8.
 bool decode_supported(const Problem& p);
 cudaError_t launch_decode_splitkv(const Problem& p, const WaitCtl& wc, cudaStream_t stream, int num_sms);

@@ -899,9 +899,12 @@ cudaError_t launch_layout(const Problem& p, const WaitCtl& wc, cudaStream_t stre
     // about 83 KB of shared memory each) and hide each other's set-up and epilogue.
     // head_dim 128: two tiles per CTA (512 TMEM columns, one CTA per SM), ping-pong inside;
     // an even group size pairs two query heads of one kv group over the same rows.
-    if (p.D == 64)
-        return p.f16 ? launch_zt<64, 1, true, LAYOUT, false>(p, wc, stream)
-                     : launch_zt<64, 1, false, LAYOUT, false>(p, wc, stream);
+    if (p.D == 64) {  // head-major and packed layouts take the narrow-block kernel
+        if constexpr (LAYOUT == kPaged)
+            return p.f16 ? launch_zt<64, 1, true, LAYOUT, false>(p, wc, stream)
+                         : launch_zt<64, 1, false, LAYOUT, false>(p, wc, stream);
+        return cudaErrorInvalidValue;
+    }
     if (p.D == 128) {
         if ((p.Hq / p.Hkv) % 2 == 0)
             return p.f16 ? launch_zt<128, 2, true, LAYOUT, true>(p, wc, stream)
@@ -915,6 +918,7 @@ cudaError_t launch_layout(const Problem& p, const WaitCtl& wc, cudaStream_t stre
 }  // namespace
 
 cudaError_t launch_prefill_tc(const Problem& p, const WaitCtl& wc, cudaStream_t stream) {
+    if (prefill_narrow_supported(p)) return launch_prefill_narrow(p, wc, stream);
     if (p.page_table != nullptr) return launch_layout<kPaged>(p, wc, stream);
     if (p.cu_seqlens != nullptr) return launch_layout<kPacked>(p, wc, stream);
     return launch_layout<kHeadMajor>(p, wc, stream);

@@ -334,7 +334,8 @@ ATTN_API attn_status attn_qkv_prelude_caches(const void* qkv, const float* q_nor
  *     are written as zeros.
  *
  * The result equals attn_fwd per sequence over the gathered cache (q_len len_b, pos_offset
- * kv_lens[b] - len_b, key_lens kv_lens[b]), bit for bit where both run the prefill kernel.
+ * kv_lens[b] - len_b, key_lens kv_lens[b]); at head_dim 128, where both run the same prefill
+ * kernel on the same tiles, bit for bit.
  * The library allocates nothing and keeps no pointer after the call.
  */
 ATTN_API attn_status attn_fwd_varlen_paged(const void* q, const void* k_pool, const void* v_pool,

@@ -4,8 +4,8 @@ Sequence b has len_b packed queries, the newest of its kv_lens[b] cached positio
 prefill, multi-token verification); its cache lives in pages of two pools addressed by
 page_table[b].  Gathering the pages back into one [Hkv, capacity, D] cache and calling attn_fwd
 per sequence (q_len len_b, pos_offset kv_lens[b] - len_b, key_lens kv_lens[b]) runs the same
-prefill kernel on the same shared-memory tiles, so the two agree bit for bit; both are checked
-against the fp64 oracle.  Pool rows outside every sequence's cached positions hold NaN, which
+prefill kernel on the same shared-memory tiles at head_dim 128, so the two agree bit for bit; both
+are checked against the fp64 oracle.  Pool rows outside every sequence's cached positions hold NaN, which
 must never reach the output.
 """
 import numpy as np
@@ -94,7 +94,8 @@ def test_paged_chunks_equal_gathered_prefill(D, Hq, Hkv, page_size, mode, window
         P = klen - n
         ref = oracle.attention(qb, kb, vb, pos_offset=P, mask_mode=mode, window=window, key_lens=[klen], scale=sc)
         assert_close(got[s0:s0 + n], ref[0].transpose(1, 0, 2), "bf16", f"seq {b} (len {n}, kv {klen})")
-        if n > 1:  # the same prefill kernel through attn_fwd over the gathered cache: bit for bit
+        if n > 1 and D == 128:  # the same prefill kernel through attn_fwd over the gathered cache: bit for bit
+            # (at head_dim 64 attn_fwd runs the 64-key-block kernel, a different summation order)
             fwd = attn.attn_fwd(qb.to(DEV), kb.to(DEV), vb.to(DEV), key_lens=torch.tensor([klen], dtype=torch.int32,
                                 device=DEV), pos_offset=P, mask_mode=mode, window=window, scale=sc)
             torch.cuda.synchronize()
