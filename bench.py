@@ -40,14 +40,21 @@ from head_attention_attn_gb300.inputs import WORKLOADS, make_inputs  # noqa: E40
 METRIC = "attention TFLOP/s (prefill) and KV GB/s (decode) on 1 GB300, % of roofline"
 HEADLINE = "causal_gqa_bf16_4x32q8kv_4096x128"
 DECODE = "decode_bf16_64x32q8kv_8192x128"
-EXTRA_PREFILL = ["bidir_keypad_bf16_8x12x512x64", "window128_bf16_4x12x8192x64"]
+EXTRA_PREFILL = ["causal_mha_f32_1x4x64x32", "bidir_keypad_bf16_8x12x512x64", "window128_bf16_4x12x8192x64"]
+KEYPAD = "bidir_keypad_bf16_8x12x512x64"
 PRELUDE = "qkv_prelude_bf16_16384x32q8kv_128_normrope"
 L2_BYTES = 129 * 1024 * 1024
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 # DRAM bytes per launch measured by ncu (dram__bytes_read.sum + dram__bytes_write.sum) for a
-# kernel source state; the entry stops applying as soon as the kernel source changes.
-NCU_TRAFFIC = {"07f11fa938f9": 460976896.0}  # prefill_tc_kernel<128, 2, bf16, paired heads>: 357.80 MB read + 103.18 MB written
+# kernel's code state (its hash); the entry stops applying as soon as the kernel's code changes.
+NCU_TRAFFIC = {
+    # prefill_tc_kernel<128, 2, bf16, paired heads>, causal GQA: 355.24 MB read + 102.99 MB written
+    ("prefill", "b7fe52fc2293"): 458225920.0,
+    # decode_tc_kernel<G4, bf16>: 537.09 MB read + 3.62 MB written at batch 16, scaled by the units
+    # (items) to the bench's batch 64
+    ("decode_tc", "4b4a0f4709ce"): 4 * 540707328.0,
+}
 
 
 # ----------------------------------------------------------------------------- distributed plumbing
@@ -242,6 +249,7 @@ def prelude_leg(args, world, dev, peaks, peak_src):
 
 KERNEL_SOURCES = {
     "prefill": ("head_attention_attn_gb300/csrc/prefill_tc.cu",),
+    "prefill_narrow": ("head_attention_attn_gb300/csrc/prefill_narrow.cu",),
     "decode_tc": ("head_attention_attn_gb300/csrc/decode_tc.cu",),
 }
 SHARED_SOURCES = ("head_attention_attn_gb300/csrc/common.cuh", "head_attention_attn_gb300/csrc/kernels.h")
@@ -385,7 +393,7 @@ def run_ours(args, rank, world, local):
     value = tflops * world  # replicas: every rank processes one full workload per step
     roof = {"bound": "tensor", "achieved": round(tflops, 2), "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
             "frac": round(tflops / peaks["bf16_tflops"], 4), "peak_source": f"{peak_src} bf16 dense (burst)",
-            "traffic": NCU_TRAFFIC.get(kernel_source_hash("prefill")), "kernel": "prefill_tc_kernel<128, 2 tiles, bf16>",
+            "traffic": NCU_TRAFFIC.get(("prefill", kernel_source_hash("prefill"))), "kernel": "prefill_tc_kernel<128, 2 tiles, bf16>",
             "algorithmic_flops_per_launch": flops}
 
     # ---- end to end through the public call with pinned host buffers: every step copies its
@@ -463,7 +471,8 @@ def run_ours(args, rank, world, local):
               "ms_per_step": round(dsec * 1e3, 4),
               "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                            "frac": round(gbs / peaks["hbm_gbs"], 4), "peak_source": f"{peak_src} HBM copy",
-                           "traffic": None, "kernel": "decode_tc_kernel<G4, bf16>",
+                           "traffic": NCU_TRAFFIC.get(("decode_tc", kernel_source_hash("decode_tc"))),
+                           "kernel": "decode_tc_kernel<G4, bf16>",
                            "algorithmic_bytes_per_launch": dec_bytes},
               "l2": f"inputs {dec_bytes / 1e6:.0f} MB > {L2_BYTES / 1e6:.0f} MB L2, no flush"}
     del host_d, devt_d
@@ -477,15 +486,11 @@ def run_ours(args, rank, world, local):
     # the headline workload's 4 x 4096 tokens (32 q / 8 kv heads, head_dim 128, bf16)
     prelude = prelude_leg(args, world, dev, peaks, peak_src)
 
-    # ---- the other prefill workloads (smaller; context)
-    per_config = []
-    for name in EXTRA_PREFILL:
-        c_x, host_x, devt_x, call_x = setup(name)
-        kl_x = host_x[3]
-        f_x, b_x = flops_of(c_x, kl_x), bytes_of(c_x, kl_x)
-        # flush L2 between iterations only where the inputs fit in it
-        flush = None
-        if b_x < 2 * L2_BYTES:
+    # ---- the other workloads (smaller; context)
+    def timed(call_x, nbytes):
+        """Seconds per call; L2 is flushed between calls where the inputs fit in it (the flush time
+        is measured alone and subtracted)."""
+        if nbytes < 2 * L2_BYTES:
             flush = torch.empty(int(2 * L2_BYTES), dtype=torch.uint8, device=dev)
 
             def call_xf(cx=call_x):
@@ -493,15 +498,58 @@ def run_ours(args, rank, world, local):
                 cx()
             tsec_with = time_device(call_xf, min(args.steps, 200), args.warmup, world, dev)
             tsec_flush = time_device(lambda: flush.zero_(), min(args.steps, 200), args.warmup, world, dev)
-            xs = max(tsec_with - tsec_flush, 1e-9)
-        else:
-            xs = time_device(call_x, min(args.steps, 200), args.warmup, world, dev)
-        per_config.append({"workload": name, "ms_per_step": round(xs * 1e3, 4),
-                           "tflops": round(f_x / xs / 1e12, 2), "gbs": round(b_x / xs / 1e9, 1),
-                           "frac_hbm": round(b_x / xs / 1e9 / peaks["hbm_gbs"], 4),
-                           "frac_tensor": round(f_x / xs / 1e12 / peaks["bf16_tflops"], 4),
-                           "l2": "flushed (2x L2 write between calls)" if flush is not None else "inputs > L2"})
-        del host_x, devt_x, flush
+            del flush
+            return max(tsec_with - tsec_flush, 1e-9), "flushed (2x L2 write between calls)"
+        return time_device(call_x, min(args.steps, 200), args.warmup, world, dev), "inputs > L2"
+
+    per_config = []
+    outputs = {}  # one output per workload, for the oracle comparison of the CPU leg
+    for name in EXTRA_PREFILL:
+        c_x, host_x, devt_x, call_x = setup(name)
+        kl_x = host_x[3]
+        f_x, b_x = flops_of(c_x, kl_x), bytes_of(c_x, kl_x)
+        xs, l2 = timed(call_x, b_x)
+        call_x()
+        outputs[name] = devt_x[4].float().cpu()
+        entry = {"workload": name, "ms_per_step": round(xs * 1e3, 4),
+                 "tflops": round(f_x / xs / 1e12, 3), "gbs": round(b_x / xs / 1e9, 1),
+                 "frac_hbm": round(b_x / xs / 1e9 / peaks["hbm_gbs"], 4),
+                 "frac_tensor": round(f_x / xs / 1e12 / peaks["bf16_tflops"], 4), "l2": l2}
+        if c_x.dtype == "f32":
+            entry["bound"] = "launch latency (1.06 MFLOP); TFLOP/s for the record only"
+        per_config.append(entry)
+        if name == KEYPAD:
+            # the same valid rows through attn_fwd_varlen: the sequences packed, no padded query rows
+            # (ripvec-core Driver::prepare_batch_unpadded), against the padded call above
+            q, k, v, kl = host_x
+            lens = [int(x) for x in kl]
+            cu = torch.tensor(np.concatenate([[0], np.cumsum(lens)]), dtype=torch.int32, device=dev)
+            qp = torch.cat([q[b, :, :lens[b]].transpose(0, 1) for b in range(c_x.B)]).contiguous().to(dev)
+            kp = torch.cat([k[b, :, :lens[b]].transpose(0, 1) for b in range(c_x.B)]).contiguous().to(dev)
+            vp = torch.cat([v[b, :, :lens[b]].transpose(0, 1) for b in range(c_x.B)]).contiguous().to(dev)
+            op = torch.empty_like(qp)
+            scale_x = float(torch.tensor(1.0 / math.sqrt(c_x.D), dtype=torch.float32))
+
+            def call_p():
+                attn.attn_fwd_varlen(qp, kp, vp, cu, max(lens), op, mask_mode=c_x.mask_mode, scale=scale_x)
+            useful = 4.0 * c_x.D * c_x.Hq * sum(n * n for n in lens)  # valid query rows x valid keys
+            bp = 2.0 * (qp.numel() + kp.numel()) * 2
+            ps, l2p = timed(call_p, bp)
+            call_p()
+            outputs[name + ":packed"] = (op.float().cpu(), lens)
+            entry["useful_tflops"] = round(useful / xs / 1e12, 3)
+            per_config.append({"workload": name + " packed (attn_fwd_varlen)", "ms_per_step": round(ps * 1e3, 4),
+                               "useful_tflops": round(useful / ps / 1e12, 3), "gbs": round(bp / ps / 1e9, 1),
+                               "frac_hbm": round(bp / ps / 1e9 / peaks["hbm_gbs"], 4),
+                               "speedup_vs_padded": round(xs / ps, 3), "l2": l2p})
+            del qp, kp, vp, op, cu
+        del host_x, devt_x
+        torch.cuda.empty_cache()
+    for name in (HEADLINE, DECODE):  # the outputs of the two legs above, for the comparison
+        c_x, host_x, devt_x, call_x = setup(name)
+        call_x()
+        outputs[name] = devt_x[4].float().cpu()
+        del host_x, devt_x
         torch.cuda.empty_cache()
 
     if attn.sync_status() != attn.ATTN_OK:
@@ -520,6 +568,7 @@ def run_ours(args, rank, world, local):
     }
     if rank == 0 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
+        result["cpu_baseline"]["per_config"] = oracle_per_config(outputs)
     return result
 
 
@@ -554,6 +603,47 @@ def cpu_baseline(target_seconds: float):
     return {"value": round(total_flops / total_sec / 1e12, 6), "unit": "TFLOP/s", "cores": cores,
             "kind": "oracle",
             "sample": f"{total_rows} random query rows of {HEADLINE} (fp64 C oracle, {total_sec:.1f} s)"}
+
+
+def oracle_per_config(outputs):
+    """The oracle as it stands on every workload in full: its wall time on all host cores (and on
+    one thread for the two smallest), and the max-abs and relative-L2 error of the GPU output
+    measured above against it."""
+    import oracle
+    cores = len(os.sched_getaffinity(0))
+    rows = []
+    for name in [n for n in WORKLOADS if n in outputs]:
+        c = WORKLOADS[name]
+        q, k, v, kl = make_inputs(c)
+        scale = float(torch.tensor(1.0 / math.sqrt(c.D), dtype=torch.float32))
+        kw = dict(key_lens=kl, pos_offset=c.pos_offset, mask_mode=c.mask_mode, window=c.window, scale=scale)
+        t0 = time.perf_counter()
+        ref = oracle.attention(q, k, v, nthreads=cores, **kw)
+        sec = time.perf_counter() - t0
+        got = outputs[name].double().numpy()
+        diff = got - ref
+        entry = {"workload": name, "oracle_s": round(sec, 3), "cores": cores,
+                 "max_abs": float(np.max(np.abs(diff))),
+                 "rel_l2": float(np.linalg.norm(diff) / max(np.linalg.norm(ref), 1e-300))}
+        if c.B * c.Hq * c.Lq * c.Lk <= 8 * 12 * 512 * 512:  # the fp32 and key-padding workloads
+            t0 = time.perf_counter()
+            oracle.attention(q, k, v, nthreads=1, **kw)
+            entry["oracle_single_thread_s"] = round(time.perf_counter() - t0, 3)
+        if name + ":packed" in outputs:  # the packed call: each sequence's valid rows
+            got_p, lens = outputs[name + ":packed"]
+            off, worst, num, den = 0, 0.0, 0.0, 0.0
+            for b, n in enumerate(lens):
+                r = ref[b, :, :n].transpose(1, 0, 2)
+                d = got_p[off:off + n].double().numpy() - r
+                worst = max(worst, float(np.max(np.abs(d))))
+                num += float(np.sum(d * d))
+                den += float(np.sum(r * r))
+                off += n
+            entry["packed_max_abs"] = worst
+            entry["packed_rel_l2"] = float(np.sqrt(num / den))
+        rows.append(entry)
+        del ref, got, diff
+    return rows
 
 
 def run_reference(args, rank, world):
