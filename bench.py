@@ -288,8 +288,8 @@ def decode_forms_leg(args, world, dev, peaks, peak_src, dec_bytes):
     vs = [torch.empty(Hkv, cap, D, dtype=torch.bfloat16, device=dev).normal_() for _ in range(m)]
     kp = torch.tensor([t.data_ptr() for t in ks], dtype=torch.int64, device=dev)
     vp = torch.tensor([t.data_ptr() for t in vs], dtype=torch.int64, device=dev)
-    for Hq, kernel in ((32, "decode_splitkv_kernel<128, G4, bf16> (per-item caches)"),
-                       (64, "decode_tc_kernel<G8, bf16, per-item caches> (row gather)")):
+    for Hq, kernel in ((32, "decode_tc_kernel<G4, bf16, per-item caches> (TMA, tensor maps built on the device)"),
+                       (64, "decode_tc_kernel<G8, bf16, per-item caches> (TMA, tensor maps built on the device)")):
         q = torch.empty(m, Hq, D, dtype=torch.bfloat16, device=dev).normal_()
         out = torch.empty_like(q)
         leg(f"decode_caches_bf16_{m}x{Hq}q{Hkv}kv_{cap}x{D}",

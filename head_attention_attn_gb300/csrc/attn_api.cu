@@ -304,10 +304,10 @@ attn_status attn_decode_caches(const void* q, const void* const* k_caches, const
     attn::WaitCtl wc{st->status, kWaitLimitNs};
     attn::CachesProblem p{q, k_caches, v_caches, out, m, q_heads, kv_heads, capacity, head_dim,
                           kv_lens, sliding_window, scale, dtype == ATTN_F16};
-    // Per-item caches reach the tensor-core decode only through its row gather (the host cannot
-    // encode tensor maps for addresses held on the device), which streams at ~40 % of HBM: it
-    // wins at 8 query heads per kv head, while at 4 the CUDA-core decode's bulk copies do better.
-    const bool tc = attn::decode_tc_gather_supported(q_heads, kv_heads, head_dim) && q_heads / kv_heads == 8;
+    // At 4 and 8 query heads per kv head (head_dim 128) the tensor-core decode streams the
+    // per-item caches by TMA through tensor maps it builds on the device; other shapes take the
+    // CUDA-core decode.
+    const bool tc = attn::decode_tc_items_supported(q_heads, kv_heads, head_dim);
     cudaError_t e = tc ? attn::launch_decode_tc_caches(p, wc, stream, st->num_sms)
                        : attn::launch_decode_caches(p, wc, stream, st->num_sms);
     if (e != cudaSuccess)
@@ -365,7 +365,7 @@ attn_status attn_decode_paged(const void* q, const void* k_pool, const void* v_p
     // (8); page 32: 5299 / 5124, 5171 / 2421; page 128: 6176 / 5138, 6012 / 2428; page 7:
     // 2043 / 4637, 2001 / 2390; page 1: 1798 / 1556, 1765 / 995.
     const bool tma_pages = attn::decode_tc_paged_tma(page_size, num_pages, kv_heads);
-    const bool tc = attn::decode_tc_gather_supported(q_heads, kv_heads, head_dim) &&
+    const bool tc = attn::decode_tc_items_supported(q_heads, kv_heads, head_dim) &&
                     (G == 4 ? (tma_pages && page_size >= 32) : (tma_pages || page_size < 4));
     cudaError_t e = tc ? attn::launch_decode_tc_paged(p, wc, stream, st->num_sms)
                        : attn::launch_decode_paged(p, wc, stream, st->num_sms);

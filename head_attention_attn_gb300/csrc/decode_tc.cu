@@ -12,11 +12,13 @@
 //
 // Work unit: (batch b, kv head hk, split); the splits of one unit form a cluster and merge
 // their partial results through distributed shared memory in CTA rank 0.
-//   warp 0       producer: 128-key K and V tiles through 3-stage rings, either by TMA from
-//                one contiguous [B, Hkv, Lk, D] cache, or (per-item caches and paged caches,
-//                whose addresses only the device knows) by 16-byte cp.async copies that
-//                all 32 lanes issue row by row into the same swizzled layout, rows past the
-//                visible keys written as zeros.
+//   warp 0       producer: 128-key K and V tiles through 3-stage rings by TMA, from one
+//                contiguous [B, Hkv, Lk, D] cache, from per-item caches through tensor maps
+//                built on the device (a small kernel patches each item's cache address into a
+//                host-encoded template), or from paged caches one copy per page piece; or, for
+//                page sizes TMA cannot copy whole, by 16-byte cp.async copies that all 32 lanes
+//                issue row by row into the same swizzled layout, rows past the visible keys
+//                written as zeros.
 //   warp 1       TMEM owner and single-thread MMA issuer: QK(j) then PV(j-1).
 //   warps 2-5    one key per thread: it reads its key's 16 head scores from TMEM, the per-head
 //                block maxima come from a shuffle reduce-scatter and a 4-warp exchange,
@@ -91,7 +93,8 @@ constexpr uint32_t kTmemCols = 64;
 // Where the K and V rows come from.
 enum : int {
     kSrcTma = 0,     // one contiguous [B, Hkv, Lk, D] cache per tensor, TMA tensor maps
-    kSrcCaches = 1,  // per-item caches: device arrays of pointers to [Hkv, capacity, D]
+    kSrcCaches = 1,  // per-item caches [Hkv, capacity, D] through device arrays of pointers, by TMA
+                     // through a K and a V tensor map per item built on the device
     kSrcPaged = 2,   // pools [num_pages, Hkv, page_size, D] and a device page table [B, max_pages]
 };
 
@@ -99,11 +102,11 @@ struct DecodeTcParams {
     const uint16_t* q;
     uint16_t* out;
     const int32_t* key_lens;  // key_lens (contiguous cache) or kv_lens (per-item and paged caches)
-    int Hq, Hkv, Lk, P, mode, window;  // Lk: the capacity of an item's cache for the gather sources
+    int Hq, Hkv, Lk, P, mode, window;  // Lk: the capacity of an item's cache (per-item and paged caches)
     float scale_log2;
     WaitCtl wc;
-    // gather sources: the query of item b is its newest position kv_lens[b] - 1 and sees the
-    // item's positions, or only the last `sliding` of them
+    // per-item and paged caches: the query of item b is its newest position kv_lens[b] - 1 and
+    // sees the item's positions, or only the last `sliding` of them
     int sliding;
     const uint16_t* const* kc;  // per-item caches
     const uint16_t* const* vc;
@@ -112,6 +115,7 @@ struct DecodeTcParams {
     const int32_t* page_table;
     int page_size, max_pages, num_pages;
     int paged_tma;  // paged: the page size lets TMA copy whole pages (else the rows are gathered)
+    const CUtensorMap* item_maps;  // per-item caches: [items][2] (K, V) in global memory
 };
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
@@ -185,12 +189,53 @@ __device__ __forceinline__ int head_of_lane(int lane) {
     return 8 * ((lane >> 4) & 1) + 4 * ((lane >> 3) & 1) + 2 * ((lane >> 2) & 1) + ((lane >> 1) & 1);
 }
 
+template <int SRC>
+__host__ __device__ constexpr bool has_gather() { return SRC == kSrcPaged; }
+
+// Make a tensor map written through the generic proxy (by another kernel) visible to this
+// thread's tensor-map-proxy reads.
+__device__ __forceinline__ void tensormap_acquire(const CUtensorMap* map) {
+    asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(reinterpret_cast<uint64_t>(map))
+                 : "memory");
+}
+
+// One warp per map: map w is item w / 2's K (w even) or V (w odd) cache.  The warp stages the
+// host-encoded template in shared memory, lane 0 patches the cache's address into it
+// (tensormap.replace), and the warp copies it to global memory with a release of the
+// tensor-map proxy.  A null or misaligned cache keeps the template's address: the decode reads
+// nothing of such an item.
+__global__ void __launch_bounds__(128) build_item_maps_kernel(const __grid_constant__ CUtensorMap tmpl,
+                                                             const uint16_t* const* kc, const uint16_t* const* vc,
+                                                             CUtensorMap* maps, int m) {
+    __shared__ __align__(128) CUtensorMap staged[4];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int w = blockIdx.x * 4 + warp;
+    if (w >= 2 * m) return;  // whole warps
+    CUtensorMap* sm = staged + warp;
+    const uint32_t sa = smem_u32(sm);
+    if (lane < 16) reinterpret_cast<uint64_t*>(sm)[lane] = reinterpret_cast<const uint64_t*>(&tmpl)[lane];
+    __syncwarp();
+    if (lane == 0) {
+        const uint16_t* base = (w & 1) ? vc[w >> 1] : kc[w >> 1];
+        if (base != nullptr && (reinterpret_cast<uintptr_t>(base) & 15u) == 0)
+            asm volatile("tensormap.replace.tile.global_address.shared::cta.b1024.b64 [%0], %1;" ::"r"(sa),
+                         "l"(reinterpret_cast<uint64_t>(base))
+                         : "memory");
+    }
+    __syncwarp();
+    asm volatile(
+        "tensormap.cp_fenceproxy.global.shared::cta.tensormap::generic.release.gpu.sync.aligned [%0], [%1], 128;" ::"l"(
+            reinterpret_cast<uint64_t>(maps + w)),
+        "r"(sa)
+        : "memory");
+}
+
 template <int G, bool F16, int SRC>
-__global__ void __launch_bounds__(SRC != kSrcTma ? kThreadsGather : kThreads, 1)
+__global__ void __launch_bounds__(has_gather<SRC>() ? kThreadsGather : kThreads, 1)
     decode_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                      const DecodeTcParams p) {
     static_assert(G >= 1 && G <= NH, "group size");
-    constexpr bool kGather = SRC != kSrcTma;  // an instantiation with the gather producers
+    constexpr bool kGather = has_gather<SRC>();  // an instantiation with the gather producers
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_s = smem_u32(smem_raw);
     uint8_t* smem = smem_raw + ((1024u - (raw_s & 1023u)) & 1023u);
@@ -211,7 +256,7 @@ __global__ void __launch_bounds__(SRC != kSrcTma ? kThreadsGather : kThreads, 1)
     const uint16_t* kbase = nullptr;  // per-item caches: the item's K and V caches
     const uint16_t* vbase = nullptr;
     const int32_t* pages = nullptr;
-    bool tma = true;  // copies by TMA (per-item caches: the gather producers)
+    bool tma = true;  // copies by TMA (else, for page sizes TMA cannot copy, the gather producers)
     if constexpr (SRC == kSrcTma) {
         key_interval(p.mode, p.window, klen, p.P, p.P, &lo, &hi);
     } else {
@@ -223,7 +268,6 @@ __global__ void __launch_bounds__(SRC != kSrcTma ? kThreadsGather : kThreads, 1)
             vbase = p.vc[b];
             const uintptr_t ka = reinterpret_cast<uintptr_t>(kbase), va = reinterpret_cast<uintptr_t>(vbase);
             bad = kbase == nullptr || vbase == nullptr || ((ka | va) & 15u) != 0;
-            tma = false;  // the host cannot encode tensor maps for addresses only the device holds
         } else {
             // every CTA of the cluster checks all of the item's visible page entries, so they agree
             tma = p.paged_tma != 0;
@@ -238,7 +282,7 @@ __global__ void __launch_bounds__(SRC != kSrcTma ? kThreadsGather : kThreads, 1)
         }
         if (__syncthreads_or(bad)) {
             // nothing of the item is read and its output is zeros
-            if (threadIdx.x == 0) record_status(p.wc.status, SRC == kSrcCaches ? kStatusBadPointer : kStatusBadPage);
+            if (threadIdx.x == 0) record_status(p.wc.status, SRC == kSrcPaged ? kStatusBadPage : kStatusBadPointer);
             lo = hi = 0;
         }
     }
@@ -291,8 +335,18 @@ __global__ void __launch_bounds__(SRC != kSrcTma ? kThreadsGather : kThreads, 1)
         tmem_relinquish();
     }
     if (tma && warp == 0 && lane == 0) {
-        tma_prefetch_desc(&tmK);
-        tma_prefetch_desc(&tmV);
+        if constexpr (SRC == kSrcCaches) {
+            // the item's maps were written by an earlier kernel through the generic proxy: acquire
+            // them for the tensor-map proxy before the first copy reads them
+            const CUtensorMap* maps = p.item_maps + 2 * b;
+            tensormap_acquire(maps);
+            tensormap_acquire(maps + 1);
+            tma_prefetch_desc(maps);
+            tma_prefetch_desc(maps + 1);
+        } else {
+            tma_prefetch_desc(&tmK);
+            tma_prefetch_desc(&tmV);
+        }
     }
     tc_fence_before();
     __syncthreads();
@@ -336,13 +390,9 @@ __global__ void __launch_bounds__(SRC != kSrcTma ? kThreadsGather : kThreads, 1)
                 const long long key = krow0 + r;
                 unsigned long long off = ~0ull;
                 if (key >= vbeg && key < vend) {  // the keys that count; other rows are zeros
-                    if constexpr (SRC == kSrcCaches) {
-                        off = ((unsigned long long)hk * (unsigned long long)p.Lk + (unsigned long long)key) * (D * 2);
-                    } else {
-                        const long long pg = __ldg(pages + key / p.page_size);
-                        off = (((unsigned long long)pg * p.Hkv + hk) * (unsigned long long)p.page_size +
-                               (unsigned long long)(key % p.page_size)) * (D * 2);
-                    }
+                    const long long pg = __ldg(pages + key / p.page_size);
+                    off = (((unsigned long long)pg * p.Hkv + hk) * (unsigned long long)p.page_size +
+                           (unsigned long long)(key % p.page_size)) * (D * 2);
                 }
                 rowoff[r] = off;
             }
@@ -371,15 +421,18 @@ __global__ void __launch_bounds__(SRC != kSrcTma ? kThreadsGather : kThreads, 1)
         cp_async_wait<0>();  // nothing stays in flight, whatever happened above
     } else if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
-        // contiguous cache: one box per 64-column chunk at (chunk, position, b Hkv + hk); paged:
+        // contiguous cache: one box per 64-column chunk at (chunk, position, b Hkv + hk); per-item
+        // caches: the same boxes at (chunk, position, hk) through the item's own maps; paged:
         // one copy per page piece that holds visible keys (whole pages of at most 128 rows, or
         // 128 rows of a longer page), the pool map bounding every coordinate.  Lane 0 issues the
         // copies.
         if (nblk > 0) {
-            const int kbh = b * p.Hkv + hk;
+            const int kbh = SRC == kSrcTma ? b * p.Hkv + hk : hk;
+            const CUtensorMap* map_k = SRC == kSrcCaches ? p.item_maps + 2 * b : &tmK;
+            const CUtensorMap* map_v = SRC == kSrcCaches ? p.item_maps + 2 * b + 1 : &tmV;
             auto load = [&](const CUtensorMap* map, uint32_t tile, uint32_t bar, int j) {
                 const long long s0 = blk_start(j);
-                if constexpr (SRC == kSrcTma) {
+                if constexpr (SRC == kSrcTma || SRC == kSrcCaches) {
                     mbar_arrive_expect_tx(bar, L::kKVBytes);
                     for (int c = 0; c < D / 64; ++c) tma_load_3d(tile + c * (BN * 128), map, bar, c * 64, (int)s0, kbh);
                 } else {
@@ -422,13 +475,13 @@ __global__ void __launch_bounds__(SRC != kSrcTma ? kThreadsGather : kThreads, 1)
                     const uint32_t kt = sbase + L::kOffK + s * L::kKVBytes, vt = sbase + L::kOffV + s * L::kKVBytes;
                     if (j >= kStages && !wait(bar0 + 8 * (kBarKEmpty + s), (n - 1) & 1)) break;
                     if (small_pages) load_pages(&tmK, kt, bar0 + 8 * (kBarKFull + s), j);
-                    else load(&tmK, kt, bar0 + 8 * (kBarKFull + s), j);
+                    else load(map_k, kt, bar0 + 8 * (kBarKFull + s), j);
                     if (j >= kStages && !wait(bar0 + 8 * (kBarVEmpty + s), (n - 1) & 1)) {
                         issued = 2 * j + 1;
                         break;
                     }
                     if (small_pages) load_pages(&tmV, vt, bar0 + 8 * (kBarVFull + s), j);
-                    else load(&tmV, vt, bar0 + 8 * (kBarVFull + s), j);
+                    else load(map_v, vt, bar0 + 8 * (kBarVFull + s), j);
                     issued = 2 * j + 2;
                 }
             }
@@ -721,7 +774,7 @@ cudaError_t launch_g(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeT
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)nsplit, (unsigned)p.Hkv, (unsigned)items);
-    cfg.blockDim = dim3(SRC != kSrcTma ? kThreadsGather : kThreads, 1, 1);
+    cfg.blockDim = dim3(has_gather<SRC>() ? kThreadsGather : kThreads, 1, 1);
     cfg.dynamicSmemBytes = L::kSmem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
@@ -778,7 +831,7 @@ bool decode_tc_supported(const Problem& p) {
     return G == 4 || G == 8;
 }
 
-bool decode_tc_gather_supported(int Hq, int Hkv, int D) {
+bool decode_tc_items_supported(int Hq, int Hkv, int D) {
     if (D != 128 || Hkv <= 0 || Hq % Hkv != 0) return false;
     const int G = Hq / Hkv;
     return G == 4 || G == 8;
@@ -809,10 +862,30 @@ cudaError_t launch_decode_tc_caches(const CachesProblem& cp, const WaitCtl& wc, 
     p.sliding = cp.sliding;
     p.kc = reinterpret_cast<const uint16_t* const*>(cp.k_caches);
     p.vc = reinterpret_cast<const uint16_t* const*>(cp.v_caches);
-    CUtensorMap unused = {};
     const long long span = cp.sliding > 0 ? std::min(cp.sliding, cp.capacity) : cp.capacity;
     const int nsplit = choose_splits((long long)cp.m * cp.Hkv, span, num_sms);
-    return launch_src<kSrcCaches>(unused, unused, p, cp.Hq / cp.Hkv, cp.f16, cp.m, nsplit, stream);
+    // The caches' addresses are known only on the device, so a template map of one item's
+    // [Hkv, capacity, 128] cache is encoded here (its address a placeholder: q, 16-byte aligned)
+    // and a kernel writes each item's K and V maps, with the real addresses, into a stream-ordered
+    // workspace that is freed, in stream order, after the decode.
+    CUtensorMap tmpl;
+    if (!encode_kv(&tmpl, cp.q, cp.capacity, cp.Hkv, BN, cp.f16)) return cudaErrorInvalidValue;
+    void* ws = nullptr;
+    cudaError_t e = cudaMallocAsync(&ws, (size_t)cp.m * 2 * sizeof(CUtensorMap), stream);
+    if (e != cudaSuccess) return e;
+    if ((reinterpret_cast<uintptr_t>(ws) & 127u) != 0) {  // a tensor map in global memory is 128-byte aligned
+        cudaFreeAsync(ws, stream);
+        return cudaErrorMisalignedAddress;
+    }
+    build_item_maps_kernel<<<(unsigned)((2 * cp.m + 3) / 4), 128, 0, stream>>>(
+        tmpl, p.kc, p.vc, static_cast<CUtensorMap*>(ws), cp.m);
+    e = cudaGetLastError();
+    if (e == cudaSuccess) {
+        p.item_maps = static_cast<const CUtensorMap*>(ws);
+        e = launch_src<kSrcCaches>(tmpl, tmpl, p, cp.Hq / cp.Hkv, cp.f16, cp.m, nsplit, stream);
+    }
+    const cudaError_t ef = cudaFreeAsync(ws, stream);
+    return e != cudaSuccess ? e : ef;
 }
 
 cudaError_t launch_decode_tc_paged(const PagedProblem& pp, const WaitCtl& wc, cudaStream_t stream, int num_sms) {

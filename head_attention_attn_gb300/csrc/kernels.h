@@ -86,9 +86,10 @@ cudaError_t launch_decode_splitkv(const Problem& p, const WaitCtl& wc, cudaStrea
 // K5: tensor-core decode for q_len == 1, head_dim 128, 4 or 8 query heads per kv head.
 bool decode_tc_supported(const Problem& p);
 cudaError_t launch_decode_tc(const Problem& p, const WaitCtl& wc, cudaStream_t stream, int num_sms);
-// K5 over per-item caches (rows gathered by the device) or paged caches (TMA per page piece where
-// the page size allows it, rows gathered otherwise), the same shapes.
-bool decode_tc_gather_supported(int Hq, int Hkv, int D);
+// K5 over per-item caches (TMA through a K and a V tensor map per item, written on the device
+// into a stream-ordered workspace) or paged caches (TMA per page piece where the page size
+// allows it, rows gathered otherwise), the same shapes.
+bool decode_tc_items_supported(int Hq, int Hkv, int D);
 bool decode_tc_paged_tma(int page_size, int num_pages, int Hkv);
 struct CachesProblem;
 struct PagedProblem;

@@ -377,7 +377,12 @@ ATTN_API attn_status attn_fwd_varlen_paged(const void* q, const void* k_pool, co
  * pointer inside the device arrays is found on the device: that item is not read,
  * its output is zeros, and attn_sync_status() reports ATTN_ERR_INVALID_ARG.
  *
- * The library allocates nothing and keeps no pointer after the call.
+ * Workspace: at head_dim 128 with 4 or 8 query heads per kv head the caches are copied by
+ * TMA through one K and one V tensor map per item, which a kernel writes on the device
+ * (only the device holds the caches' addresses).  The call takes m * 256 bytes for them
+ * with cudaMallocAsync on cuda_stream and gives them back with cudaFreeAsync on the same
+ * stream after the launch; an allocation failure returns ATTN_ERR_CUDA.  Other shapes
+ * allocate nothing.  The library keeps no pointer after the call.
  */
 ATTN_API attn_status attn_decode_caches(const void* q, const void* const* k_caches, const void* const* v_caches,
                                         void* out, int m, int q_heads, int kv_heads, int capacity, int head_dim,

@@ -56,10 +56,11 @@ def test_decode_caches_match_oracle(D, G, window):
 
 @pytest.mark.parametrize("Hq,cap,m", [(4, 900, 4), (8, 900, 4), (16, 900, 4), (8, 5000, 2), (16, 3000, 1)])
 def test_decode_caches_agree_with_contiguous_decode(Hq, cap, m):
-    """Per-item caches all at full length against attn_fwd over one contiguous cache: with 1, 2
-    or 8 query heads per kv head both run the same kernel with the same split of the keys (the
-    CUDA-core decode, or the tensor-core decode, which then gathers the rows itself instead of
-    using TMA), so they agree bit for bit; everything is also checked against the oracle."""
+    """Per-item caches all at full length against attn_fwd over one contiguous cache: both run
+    the same kernel with the same split of the keys (the CUDA-core decode at 1 or 2 query heads
+    per kv head, the tensor-core decode at 4 and 8, there through one tensor map per item cache
+    instead of one over the whole cache), so they agree bit for bit; everything is also checked
+    against the oracle."""
     Hkv, D = 2, 128
     q, ks, vs, _ = _case(m, Hq, Hkv, cap, D, [cap] * m, seed=3 + Hq + cap)
     kl = torch.full((m,), cap, dtype=torch.int32, device=DEV)
@@ -69,8 +70,7 @@ def test_decode_caches_agree_with_contiguous_decode(Hq, cap, m):
     b = attn.attn_fwd(q.to(DEV)[:, :, None, :].contiguous(), k4, v4, pos_offset=cap - 1, mask_mode=MASK_CAUSAL)
     torch.cuda.synchronize()
     assert attn.sync_status() == attn.ATTN_OK, attn.last_error()
-    if Hq // Hkv != 4:  # group 4: per-item caches run the CUDA-core decode, attn_fwd the tensor-core one
-        assert torch.equal(a, b[:, :, 0, :])
+    assert torch.equal(a, b[:, :, 0, :])
     ref = oracle.attention(q[:, :, None, :], torch.stack(ks), torch.stack(vs), pos_offset=cap - 1,
                            mask_mode=MASK_CAUSAL, scale=float(torch.tensor(1.0 / D ** 0.5, dtype=torch.float32)))
     assert_close(a.double().cpu().numpy(), ref[:, :, 0, :], "bf16", "caches")
@@ -96,14 +96,16 @@ def test_decode_caches_bad_pointer_is_reported_not_read():
 
 @pytest.mark.parametrize("cap,offset,m", [(900, 16, 3), (3000, 48, 2), (100, 0, 3), (1000, 0, 3), (5000, 0, 1)])
 @pytest.mark.parametrize("window", [0, 333])
-def test_tensor_core_caches_gather(cap, offset, m, window):
-    """Per-item caches at 8 query heads per kv head run the tensor-core decode, whose producer
-    warps gather every row (16 bytes per lane) into the tiles TMA would give, whatever the
-    caches' alignment beyond 16 bytes, their capacity or the lengths.  Without a window the result
-    equals attn_fwd over one contiguous cache with the same lengths (the same kernel and split of
-    the keys) bit for bit; every case is also checked against the oracle."""
-    Hq, Hkv, D = 16, 2, 128
-    g = torch.Generator().manual_seed(cap + offset + window)
+@pytest.mark.parametrize("G", [4, 8])
+def test_tensor_core_caches_tma(cap, offset, m, window, G):
+    """Per-item caches at 4 and 8 query heads per kv head run the tensor-core decode, which
+    copies each item's rows by TMA through a K and a V tensor map written on the device for that
+    item's address, whatever the caches' alignment beyond 16 bytes, their capacity or the
+    lengths.  Without a window the result equals attn_fwd over one contiguous cache with the same
+    lengths (the same kernel and split of the keys) bit for bit; every case is also checked
+    against the oracle."""
+    Hq, Hkv, D = 2 * G, 2, 128
+    g = torch.Generator().manual_seed(cap + offset + window + G)
     q = torch.randn(m, Hq, D, generator=g).bfloat16()
     k4 = torch.randn(m, Hkv, cap, D, generator=g).bfloat16()
     v4 = torch.randn(m, Hkv, cap, D, generator=g).bfloat16()
@@ -130,3 +132,25 @@ def test_tensor_core_caches_gather(cap, offset, m, window):
                           pos_offset=cap - 1, mask_mode=MASK_CAUSAL, scale=sc)
         torch.cuda.synchronize()
         assert torch.equal(a, b[:, :, 0, :])
+
+
+@pytest.mark.parametrize("G", [4, 8])
+def test_tensor_core_caches_many_items(G):
+    """Several hundred items, each with its own K and V maps, ragged lengths including 0 and
+    1, fp16, checked against the oracle row by row."""
+    m, Hkv, D, cap = 300, 1, 128, 260
+    Hq = G * Hkv
+    g = torch.Generator().manual_seed(40 + G)
+    q = torch.randn(m, Hq, D, generator=g).half()
+    ks = [torch.randn(Hkv, cap, D, generator=g).half() for _ in range(m)]
+    vs = [torch.randn(Hkv, cap, D, generator=g).half() for _ in range(m)]
+    lens = torch.randint(0, cap + 1, (m,), generator=g, dtype=torch.int64).to(torch.int32)
+    lens[0], lens[1] = 0, 1
+    sc = float(torch.tensor(1.0 / D ** 0.5, dtype=torch.float32))
+    out = attn.attn_decode_caches(q.to(DEV), [k.to(DEV) for k in ks], [v.to(DEV) for v in vs], lens.to(DEV),
+                                  scale=sc)
+    torch.cuda.synchronize()
+    assert attn.sync_status() == attn.ATTN_OK, attn.last_error()
+    assert out.dtype == torch.float16
+    ref = _reference(q, ks, vs, lens, 0, sc)
+    assert_close(out.double().cpu().numpy(), ref, "f16", f"many items G={G}")

@@ -88,11 +88,11 @@ def paged_on_tensor_cores(G, page_size):
 
 def same_kernel(D, G, page_size):
     """Paged and per-item caches run the same kernel, and then agree bit for bit: the CUDA-core
-    decode for both, or the tensor-core decode for both (per-item caches at group 8, gathered row
-    by row into the tiles TMA gives the paged pages)."""
+    decode for both, or the tensor-core decode for both (per-item caches at groups 4 and 8, by TMA
+    through a tensor map per item cache, into the same tiles as the paged pages)."""
     if D != 128 or G in (1, 2):
         return True
-    caches_tc = G == 8
+    caches_tc = G in (4, 8)
     return caches_tc == paged_on_tensor_cores(G, page_size)
 
 
