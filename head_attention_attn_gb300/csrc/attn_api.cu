@@ -4,8 +4,9 @@
 // Kernel choice:
 //   f32                          -> K3 (SIMT fp32, any head_dim 1..256)
 //   bf16/fp16, q_len == 1, head_dim 128, group 4/8 -> K5 (tensor-core split-KV decode);
-//                                   paged caches of that shape whose page size TMA can place,
-//                                   and per-item caches with group 8 (row gather)
+//                                   per-item caches of that shape (TMA through tensor maps
+//                                   written on the device), and paged caches of that shape
+//                                   where the measured routing table prefers it
 //   bf16/fp16, q_len == 1, group 1/2/4/8 -> K2 (split-KV decode, the other shapes)
 //   bf16/fp16 otherwise          -> K1 (tcgen05 + TMA fused prefill); packed queries over
 //                                   paged caches also go to K1, whose producer then gathers
