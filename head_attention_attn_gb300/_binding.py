@@ -18,7 +18,7 @@ QK_COPY, QK_NORM_ROPE, QK_ROPE, QK_ROPE_INTERLEAVED = 0, 1, 2, 3
 ATTN_BF16, ATTN_F32, ATTN_F16 = 0, 1, 2
 
 EXPORTED = ("attn_fwd", "attn_fwd_out_token_major", "attn_fwd_varlen", "attn_fwd_varlen_paged", "attn_decode_caches",
-            "attn_decode_paged", "attn_qkv_prelude", "attn_qkv_prelude_caches", "attn_last_error", "attn_sync_status",
+            "attn_decode_caches_noalloc", "attn_decode_paged", "attn_qkv_prelude", "attn_qkv_prelude_caches", "attn_last_error", "attn_sync_status",
             "attn_selftest_timeout", "attn_version")
 
 _STATUS_NAMES = {0: "ATTN_OK", 1: "ATTN_ERR_INVALID_ARG", 2: "ATTN_ERR_UNSUPPORTED", 3: "ATTN_ERR_CUDA",
@@ -69,6 +69,8 @@ def load(path: str | None = None):
                                                 ctypes.c_float, ci, ci, vp]
         lib.attn_decode_caches.restype = ci
         lib.attn_decode_caches.argtypes = [vp, vp, vp, vp, ci, ci, ci, ci, ci, vp, ci, ctypes.c_float, ci, vp]
+        lib.attn_decode_caches_noalloc.restype = ci
+        lib.attn_decode_caches_noalloc.argtypes = lib.attn_decode_caches.argtypes
         lib.attn_decode_paged.restype = ci
         lib.attn_decode_paged.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, ci, vp, ci, ctypes.c_float,
                                           ci, vp]
@@ -398,8 +400,9 @@ def _decode_out(q, out):
 
 def attn_decode_caches(q, k_caches, v_caches, kv_lens, out=None, *, sliding_window: int = 0,
                        scale: float | None = None, stream=None, kv_heads: int | None = None,
-                       capacity: int | None = None):
-    """One decode step for m items against per-item caches (see attn_decode_caches in attn.h).
+                       capacity: int | None = None, noalloc: bool = False):
+    """One decode step for m items against per-item caches (see attn_decode_caches in attn.h;
+    noalloc=True calls attn_decode_caches_noalloc instead).
 
     q: [m, Hq, D] bf16 or fp16 CUDA tensor; k_caches, v_caches: sequences of m
     [Hkv, capacity, D] CUDA tensors of q's dtype, or int64 CUDA tensors of m device
@@ -444,12 +447,19 @@ def attn_decode_caches(q, k_caches, v_caches, kv_lens, out=None, *, sliding_wind
     out = _decode_out(q, out)
     if scale is None:
         scale = float(torch.tensor(1.0 / math.sqrt(D), dtype=torch.float32).item())
-    status = load().attn_decode_caches(q.data_ptr(), kp.data_ptr(), vp_.data_ptr(), out.data_ptr(), m, Hq, Hkv,
-                                       cap, D, kv_lens.data_ptr(), int(sliding_window), ctypes.c_float(scale),
-                                       dtype, _stream_handle(stream))
+    lib = load()
+    entry = lib.attn_decode_caches_noalloc if noalloc else lib.attn_decode_caches
+    status = entry(q.data_ptr(), kp.data_ptr(), vp_.data_ptr(), out.data_ptr(), m, Hq, Hkv, cap, D,
+                   kv_lens.data_ptr(), int(sliding_window), ctypes.c_float(scale), dtype, _stream_handle(stream))
     _check(status)
     out._attn_keepalive = (kp, vp_)  # the pointer arrays must outlive the queued launch
     return out
+
+
+def attn_decode_caches_noalloc(q, k_caches, v_caches, kv_lens, out=None, **kw):
+    """attn_decode_caches through the entry point that allocates nothing (its tensor maps go to a
+    fixed device table of ATTN_NOALLOC_MAX_ITEMS items; calls that overlap on the GPU race)."""
+    return attn_decode_caches(q, k_caches, v_caches, kv_lens, out, noalloc=True, **kw)
 
 
 def attn_decode_paged(q, k_pool, v_pool, page_table, kv_lens, out=None, *, sliding_window: int = 0,

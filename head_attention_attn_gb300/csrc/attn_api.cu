@@ -150,6 +150,57 @@ attn_status fwd(const void* q, const void* k, const void* v, void* out, int batc
     return ATTN_OK;
 }
 
+// attn_decode_caches and attn_decode_caches_noalloc: the same checks and kernels; `fixed_maps`
+// puts the per-item tensor maps of the tensor-core decode in the fixed device table instead of a
+// stream-ordered workspace.
+attn_status decode_caches(const void* q, const void* const* k_caches, const void* const* v_caches, void* out, int m,
+                          int q_heads, int kv_heads, int capacity, int head_dim, const int32_t* kv_lens,
+                          int sliding_window, float scale, int dtype, void* cuda_stream, bool fixed_maps) {
+    if (m < 0 || capacity < 0) return fail(ATTN_ERR_INVALID_ARG, "negative size (m=%d, capacity=%d)", m, capacity);
+    if (q_heads <= 0 || kv_heads <= 0 || head_dim <= 0)
+        return fail(ATTN_ERR_INVALID_ARG, "q_heads, kv_heads and head_dim must be positive (%d, %d, %d)", q_heads,
+                    kv_heads, head_dim);
+    if (q_heads % kv_heads != 0)
+        return fail(ATTN_ERR_INVALID_ARG, "q_heads (%d) is not a multiple of kv_heads (%d)", q_heads, kv_heads);
+    if (sliding_window < 0) return fail(ATTN_ERR_INVALID_ARG, "negative sliding_window %d", sliding_window);
+    if (!isfinite(scale)) return fail(ATTN_ERR_INVALID_ARG, "scale is not finite");
+    if (dtype != ATTN_BF16 && dtype != ATTN_F16)
+        return fail(ATTN_ERR_UNSUPPORTED, "per-item caches support bf16 and fp16 only");
+    if (head_dim != 64 && head_dim != 128)
+        return fail(ATTN_ERR_UNSUPPORTED, "bf16 and fp16 support head_dim 64 and 128, not %d", head_dim);
+    const int G = q_heads / kv_heads;
+    if (G != 1 && G != 2 && G != 4 && G != 8)
+        return fail(ATTN_ERR_UNSUPPORTED, "per-item caches support 1, 2, 4 or 8 query heads per kv head, not %d", G);
+    if (m > 65535 || kv_heads > 65535) return fail(ATTN_ERR_UNSUPPORTED, "m and kv_heads are limited to 65535");
+    if (m == 0) return ATTN_OK;
+    if (!q || !out || !k_caches || !v_caches || !kv_lens)
+        return fail(ATTN_ERR_INVALID_ARG, "null q, out, k_caches, v_caches or kv_lens pointer");
+    if (!aligned(q, 16) || !aligned(out, 16) || !aligned(k_caches, 8) || !aligned(v_caches, 8) || !aligned(kv_lens, 4))
+        return fail(ATTN_ERR_INVALID_ARG, "q/out must be 16-byte, pointer arrays 8-byte, kv_lens 4-byte aligned");
+    cudaStream_t stream = static_cast<cudaStream_t>(cuda_stream);
+    if (capacity == 0) {
+        cudaError_t e = cudaMemsetAsync(out, 0, (size_t)m * q_heads * head_dim * 2, stream);
+        if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "cudaMemsetAsync: %s", cudaGetErrorString(e));
+        return ATTN_OK;
+    }
+    DeviceState* st = nullptr;
+    attn_status s = device_state(&st);
+    if (s != ATTN_OK) return s;
+    attn::WaitCtl wc{st->status, kWaitLimitNs};
+    attn::CachesProblem p{q, k_caches, v_caches, out, m, q_heads, kv_heads, capacity, head_dim,
+                          kv_lens, sliding_window, scale, dtype == ATTN_F16};
+    // At 4 and 8 query heads per kv head (head_dim 128) the tensor-core decode streams the
+    // per-item caches by TMA through tensor maps it builds on the device; other shapes take the
+    // CUDA-core decode.
+    const bool tc = attn::decode_tc_items_supported(q_heads, kv_heads, head_dim);
+    cudaError_t e = !tc        ? attn::launch_decode_caches(p, wc, stream, st->num_sms)
+                    : fixed_maps ? attn::launch_decode_tc_caches_static(p, wc, stream, st->num_sms)
+                                 : attn::launch_decode_tc_caches(p, wc, stream, st->num_sms);
+    if (e != cudaSuccess)
+        return fail(ATTN_ERR_CUDA, "%s launch: %s", tc ? "decode_tc (caches)" : "decode_caches", cudaGetErrorString(e));
+    return ATTN_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -272,48 +323,20 @@ attn_status attn_decode_caches(const void* q, const void* const* k_caches, const
                                int m, int q_heads, int kv_heads, int capacity, int head_dim, const int32_t* kv_lens,
                                int sliding_window, float scale, int dtype, void* cuda_stream) {
     t_last_error.clear();
-    if (m < 0 || capacity < 0) return fail(ATTN_ERR_INVALID_ARG, "negative size (m=%d, capacity=%d)", m, capacity);
-    if (q_heads <= 0 || kv_heads <= 0 || head_dim <= 0)
-        return fail(ATTN_ERR_INVALID_ARG, "q_heads, kv_heads and head_dim must be positive (%d, %d, %d)", q_heads,
-                    kv_heads, head_dim);
-    if (q_heads % kv_heads != 0)
-        return fail(ATTN_ERR_INVALID_ARG, "q_heads (%d) is not a multiple of kv_heads (%d)", q_heads, kv_heads);
-    if (sliding_window < 0) return fail(ATTN_ERR_INVALID_ARG, "negative sliding_window %d", sliding_window);
-    if (!isfinite(scale)) return fail(ATTN_ERR_INVALID_ARG, "scale is not finite");
-    if (dtype != ATTN_BF16 && dtype != ATTN_F16)
-        return fail(ATTN_ERR_UNSUPPORTED, "per-item caches support bf16 and fp16 only");
-    if (head_dim != 64 && head_dim != 128)
-        return fail(ATTN_ERR_UNSUPPORTED, "bf16 and fp16 support head_dim 64 and 128, not %d", head_dim);
-    const int G = q_heads / kv_heads;
-    if (G != 1 && G != 2 && G != 4 && G != 8)
-        return fail(ATTN_ERR_UNSUPPORTED, "per-item caches support 1, 2, 4 or 8 query heads per kv head, not %d", G);
-    if (m > 65535 || kv_heads > 65535) return fail(ATTN_ERR_UNSUPPORTED, "m and kv_heads are limited to 65535");
-    if (m == 0) return ATTN_OK;
-    if (!q || !out || !k_caches || !v_caches || !kv_lens)
-        return fail(ATTN_ERR_INVALID_ARG, "null q, out, k_caches, v_caches or kv_lens pointer");
-    if (!aligned(q, 16) || !aligned(out, 16) || !aligned(k_caches, 8) || !aligned(v_caches, 8) || !aligned(kv_lens, 4))
-        return fail(ATTN_ERR_INVALID_ARG, "q/out must be 16-byte, pointer arrays 8-byte, kv_lens 4-byte aligned");
-    cudaStream_t stream = static_cast<cudaStream_t>(cuda_stream);
-    if (capacity == 0) {
-        cudaError_t e = cudaMemsetAsync(out, 0, (size_t)m * q_heads * head_dim * 2, stream);
-        if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "cudaMemsetAsync: %s", cudaGetErrorString(e));
-        return ATTN_OK;
-    }
-    DeviceState* st = nullptr;
-    attn_status s = device_state(&st);
-    if (s != ATTN_OK) return s;
-    attn::WaitCtl wc{st->status, kWaitLimitNs};
-    attn::CachesProblem p{q, k_caches, v_caches, out, m, q_heads, kv_heads, capacity, head_dim,
-                          kv_lens, sliding_window, scale, dtype == ATTN_F16};
-    // At 4 and 8 query heads per kv head (head_dim 128) the tensor-core decode streams the
-    // per-item caches by TMA through tensor maps it builds on the device; other shapes take the
-    // CUDA-core decode.
-    const bool tc = attn::decode_tc_items_supported(q_heads, kv_heads, head_dim);
-    cudaError_t e = tc ? attn::launch_decode_tc_caches(p, wc, stream, st->num_sms)
-                       : attn::launch_decode_caches(p, wc, stream, st->num_sms);
-    if (e != cudaSuccess)
-        return fail(ATTN_ERR_CUDA, "%s launch: %s", tc ? "decode_tc (caches)" : "decode_caches", cudaGetErrorString(e));
-    return ATTN_OK;
+    return decode_caches(q, k_caches, v_caches, out, m, q_heads, kv_heads, capacity, head_dim, kv_lens,
+                         sliding_window, scale, dtype, cuda_stream, false);
+}
+
+attn_status attn_decode_caches_noalloc(const void* q, const void* const* k_caches, const void* const* v_caches,
+                                       void* out, int m, int q_heads, int kv_heads, int capacity, int head_dim,
+                                       const int32_t* kv_lens, int sliding_window, float scale, int dtype,
+                                       void* cuda_stream) {
+    t_last_error.clear();
+    if (m > attn::kStaticMapItems)
+        return fail(ATTN_ERR_INVALID_ARG, "m (%d) exceeds the %d items of the fixed map table", m,
+                    attn::kStaticMapItems);
+    return decode_caches(q, k_caches, v_caches, out, m, q_heads, kv_heads, capacity, head_dim, kv_lens,
+                         sliding_window, scale, dtype, cuda_stream, true);
 }
 
 attn_status attn_decode_paged(const void* q, const void* k_pool, const void* v_pool, const int32_t* page_table,

@@ -856,20 +856,38 @@ cudaError_t launch_decode_tc(const Problem& pr, const WaitCtl& wc, cudaStream_t 
     return launch_src<kSrcTma>(tk, tv, p, pr.Hq / pr.Hkv, pr.f16, pr.B, nsplit, stream);
 }
 
-cudaError_t launch_decode_tc_caches(const CachesProblem& cp, const WaitCtl& wc, cudaStream_t stream, int num_sms) {
-    if (cp.Hkv > 65535 || cp.m > 65535) return cudaErrorInvalidConfiguration;
+namespace {
+
+// The caches' addresses are known only on the device, so a template map of one item's
+// [Hkv, capacity, 128] cache is encoded on the host (its address a placeholder: q, 16-byte
+// aligned) and a kernel writes each item's K and V maps, with the real addresses, into `maps`
+// ([m][2], 128-byte aligned) before the decode reads them.
+cudaError_t decode_caches_with_maps(const CachesProblem& cp, const WaitCtl& wc, cudaStream_t stream, int num_sms,
+                                    const CUtensorMap& tmpl, CUtensorMap* maps) {
     DecodeTcParams p = base_params(cp.q, cp.out, cp.kv_lens, cp.Hq, cp.Hkv, cp.capacity, cp.scale, wc);
     p.sliding = cp.sliding;
     p.kc = reinterpret_cast<const uint16_t* const*>(cp.k_caches);
     p.vc = reinterpret_cast<const uint16_t* const*>(cp.v_caches);
     const long long span = cp.sliding > 0 ? std::min(cp.sliding, cp.capacity) : cp.capacity;
     const int nsplit = choose_splits((long long)cp.m * cp.Hkv, span, num_sms);
-    // The caches' addresses are known only on the device, so a template map of one item's
-    // [Hkv, capacity, 128] cache is encoded here (its address a placeholder: q, 16-byte aligned)
-    // and a kernel writes each item's K and V maps, with the real addresses, into a stream-ordered
-    // workspace that is freed, in stream order, after the decode.
+    build_item_maps_kernel<<<(unsigned)((2 * cp.m + 3) / 4), 128, 0, stream>>>(tmpl, p.kc, p.vc, maps, cp.m);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    p.item_maps = maps;
+    return launch_src<kSrcCaches>(tmpl, tmpl, p, cp.Hq / cp.Hkv, cp.f16, cp.m, nsplit, stream);
+}
+
+}  // namespace
+
+// The fixed map table of attn_decode_caches_noalloc: room for kStaticMapItems items (1 MB).
+// Calls that overlap on the GPU share it, so they race.
+static __device__ __align__(256) CUtensorMap g_static_item_maps[2 * kStaticMapItems];
+
+cudaError_t launch_decode_tc_caches(const CachesProblem& cp, const WaitCtl& wc, cudaStream_t stream, int num_sms) {
+    if (cp.Hkv > 65535 || cp.m > 65535) return cudaErrorInvalidConfiguration;
     CUtensorMap tmpl;
     if (!encode_kv(&tmpl, cp.q, cp.capacity, cp.Hkv, BN, cp.f16)) return cudaErrorInvalidValue;
+    // the maps live in a stream-ordered workspace, freed in stream order after the decode
     void* ws = nullptr;
     cudaError_t e = cudaMallocAsync(&ws, (size_t)cp.m * 2 * sizeof(CUtensorMap), stream);
     if (e != cudaSuccess) return e;
@@ -877,15 +895,38 @@ cudaError_t launch_decode_tc_caches(const CachesProblem& cp, const WaitCtl& wc, 
         cudaFreeAsync(ws, stream);
         return cudaErrorMisalignedAddress;
     }
-    build_item_maps_kernel<<<(unsigned)((2 * cp.m + 3) / 4), 128, 0, stream>>>(
-        tmpl, p.kc, p.vc, static_cast<CUtensorMap*>(ws), cp.m);
-    e = cudaGetLastError();
-    if (e == cudaSuccess) {
-        p.item_maps = static_cast<const CUtensorMap*>(ws);
-        e = launch_src<kSrcCaches>(tmpl, tmpl, p, cp.Hq / cp.Hkv, cp.f16, cp.m, nsplit, stream);
-    }
+    e = decode_caches_with_maps(cp, wc, stream, num_sms, tmpl, static_cast<CUtensorMap*>(ws));
     const cudaError_t ef = cudaFreeAsync(ws, stream);
     return e != cudaSuccess ? e : ef;
+}
+
+cudaError_t launch_decode_tc_caches_static(const CachesProblem& cp, const WaitCtl& wc, cudaStream_t stream,
+                                           int num_sms) {
+    if (cp.Hkv > 65535 || cp.m > kStaticMapItems) return cudaErrorInvalidConfiguration;
+    CUtensorMap tmpl;
+    if (!encode_kv(&tmpl, cp.q, cp.capacity, cp.Hkv, BN, cp.f16)) return cudaErrorInvalidValue;
+    // the table's address, looked up once per device
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    static std::mutex mu;
+    static CUtensorMap* table[64] = {};
+    CUtensorMap* maps = nullptr;
+    {
+        std::lock_guard<std::mutex> g(mu);
+        if (table[dev] == nullptr) {
+            void* a = nullptr;
+            e = cudaGetSymbolAddress(&a, g_static_item_maps);
+            if (e != cudaSuccess) return e;
+            if ((reinterpret_cast<uintptr_t>(a) & 127u) != 0) return cudaErrorMisalignedAddress;
+            table[dev] = static_cast<CUtensorMap*>(a);
+        }
+        maps = table[dev];
+    }
+    // nothing in the table has to start at zero: the kernel writes every map an item uses
+    // before the decode reads it
+    return decode_caches_with_maps(cp, wc, stream, num_sms, tmpl, maps);
 }
 
 cudaError_t launch_decode_tc_paged(const PagedProblem& pp, const WaitCtl& wc, cudaStream_t stream, int num_sms) {

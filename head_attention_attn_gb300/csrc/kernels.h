@@ -6,6 +6,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "attn.h"
 #include "common.cuh"
 
 namespace attn {
@@ -94,6 +95,11 @@ bool decode_tc_paged_tma(int page_size, int num_pages, int Hkv);
 struct CachesProblem;
 struct PagedProblem;
 cudaError_t launch_decode_tc_caches(const CachesProblem& p, const WaitCtl& wc, cudaStream_t stream, int num_sms);
+// The same, with the maps in a fixed device table of kStaticMapItems items instead of a per-call
+// workspace (allocates nothing; calls that overlap on the GPU race on the table).
+constexpr int kStaticMapItems = ATTN_NOALLOC_MAX_ITEMS;
+cudaError_t launch_decode_tc_caches_static(const CachesProblem& p, const WaitCtl& wc, cudaStream_t stream,
+                                           int num_sms);
 cudaError_t launch_decode_tc_paged(const PagedProblem& p, const WaitCtl& wc, cudaStream_t stream, int num_sms);
 
 // K2 over per-item caches: one single-query decode step for m items, item i reading its

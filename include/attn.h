@@ -390,6 +390,30 @@ ATTN_API attn_status attn_decode_caches(const void* q, const void* const* k_cach
                                         void* cuda_stream);
 
 /*
+ * attn_decode_caches_noalloc -- attn_decode_caches without any allocation.
+ *
+ * Source: none.  The pages have no counterpart; this is a deployment variant of
+ * attn_decode_caches (same arguments, same results bit for bit).
+ *
+ * Where attn_decode_caches takes a stream-ordered workspace for the per-item tensor maps
+ * (head_dim 128, 4 or 8 query heads per kv head), this call writes them into a fixed table
+ * in the library's device memory, room for ATTN_NOALLOC_MAX_ITEMS items (1 MB).  It calls no
+ * allocation routine.  The table's address is looked up once per device
+ * (cudaGetSymbolAddress; a failure returns ATTN_ERR_CUDA).  Nothing in it has to start at
+ * zero: every map an item uses is written, on cuda_stream, before the decode reads it.
+ *
+ * Calls whose launches overlap on the GPU (different streams, or devices' work not ordered
+ * by the caller) share the table and race: order them, for example on one stream.
+ *
+ * Errors: as attn_decode_caches, and ATTN_ERR_INVALID_ARG for m > ATTN_NOALLOC_MAX_ITEMS.
+ */
+#define ATTN_NOALLOC_MAX_ITEMS 4096
+ATTN_API attn_status attn_decode_caches_noalloc(const void* q, const void* const* k_caches,
+                                                const void* const* v_caches, void* out, int m, int q_heads,
+                                                int kv_heads, int capacity, int head_dim, const int32_t* kv_lens,
+                                                int sliding_window, float scale, int dtype, void* cuda_stream);
+
+/*
  * attn_decode_paged -- attn_decode_caches over paged KV caches: every item's cache lives in
  * fixed-size pages of two shared pools, addressed through a per-item page table.
  *

@@ -165,13 +165,13 @@ def test_library_has_no_host_fallback_symbols(lib):
     assert isinstance(ctypes.CDLL(attn.library_path()), ctypes.CDLL)
 
 
-def _caches_call(lib, **kw):
+def _caches_call(lib, noalloc=False, **kw):
     args = dict(q=16, kc=16, vc=16, out=16, m=2, hq=8, hkv=2, cap=64, d=128, lens=16, win=0, scale=0.1,
                 dtype=attn.ATTN_BF16, stream=None)
     args.update(kw)
-    return lib.attn_decode_caches(args["q"], args["kc"], args["vc"], args["out"], args["m"], args["hq"], args["hkv"],
-                                  args["cap"], args["d"], args["lens"], args["win"], ctypes.c_float(args["scale"]),
-                                  args["dtype"], args["stream"])
+    entry = lib.attn_decode_caches_noalloc if noalloc else lib.attn_decode_caches
+    return entry(args["q"], args["kc"], args["vc"], args["out"], args["m"], args["hq"], args["hkv"], args["cap"],
+                 args["d"], args["lens"], args["win"], ctypes.c_float(args["scale"]), args["dtype"], args["stream"])
 
 
 @pytest.mark.parametrize("change,status", [
@@ -191,8 +191,15 @@ def _caches_call(lib, **kw):
     (dict(hq=6, hkv=2), attn.ATTN_ERR_UNSUPPORTED),
     (dict(m=0), attn.ATTN_OK),
 ])
-def test_decode_caches_arguments(lib, change, status):
-    assert _caches_call(lib, **change) == status
+@pytest.mark.parametrize("noalloc", [False, True])
+def test_decode_caches_arguments(lib, change, status, noalloc):
+    assert _caches_call(lib, noalloc=noalloc, **change) == status
+
+
+def test_decode_caches_noalloc_refuses_more_items_than_its_table(lib):
+    # ATTN_NOALLOC_MAX_ITEMS is 4096: the call is refused before anything is read or launched
+    assert _caches_call(lib, noalloc=True, m=4097) == attn.ATTN_ERR_INVALID_ARG
+    assert "fixed map table" in attn.last_error()
 
 
 def _varlen_call(lib, **kw):
