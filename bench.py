@@ -240,7 +240,7 @@ def prelude_leg(args, world, dev, peaks, peak_src):
     nbytes = 2.0 * qkv.numel() * 2 + cos.numel() * 4 * 2 + 2 * hd * 4  # qkv in, q/k/v out, tables, weights
     gbs = nbytes / sec / 1e9
     return {"workload": PRELUDE, "value": round(gbs * world, 1), "unit": "GB/s",
-            "steps": steps, "ms_per_step": round(sec * 1e3, 4),
+            "steps": steps, "ms_per_step": round(sec * 1e3, 4), "launch_ms": LAUNCH_STATS.get(call),
             "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                          "frac": round(gbs / peaks["hbm_gbs"], 4), "peak_source": f"{peak_src} HBM copy",
                          "traffic": None, "kernel": "prelude_kernel<128, bf16>", "algorithmic_bytes_per_launch": nbytes},
@@ -277,7 +277,7 @@ def decode_forms_leg(args, world, dev, peaks, peak_src, dec_bytes):
             raise RuntimeError(f"device status after {name}: " + attn.last_error())
         gbs = nbytes / sec / 1e9
         legs.append({"workload": name, "value": round(gbs * world, 1), "unit": "GB/s", "steps": steps,
-                     "ms_per_step": round(sec * 1e3, 4),
+                     "ms_per_step": round(sec * 1e3, 4), "launch_ms": LAUNCH_STATS.get(call),
                      "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                                   "frac": round(gbs / peaks["hbm_gbs"], 4), "peak_source": f"{peak_src} HBM copy",
                                   "traffic": None, "kernel": kernel, "algorithmic_bytes_per_launch": nbytes},
@@ -337,21 +337,31 @@ def kernel_source_hash(kernel: str = "prefill") -> str:
     return h.hexdigest()[:12]
 
 
+LAUNCH_STATS = {}  # fn -> per-launch statistics of its last time_device run
+
+
 def time_device(fn, steps: int, warmup: int, world: int, device) -> float:
-    """Seconds per call: CUDA events on the launching stream, synced on both sides, max over ranks."""
+    """Seconds per call: CUDA events on the launching stream, synced on both sides, max over ranks.
+
+    The returned mean is the whole timed region over `steps`.  An event also sits between
+    consecutive launches (recorded on the stream, no synchronisation), so LAUNCH_STATS[fn] holds
+    the median, 10th and 90th percentile of the per-launch durations on this rank."""
     for _ in range(warmup):
         fn()
     torch.cuda.synchronize()
     barrier(world)
     stream = torch.cuda.current_stream()
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    start.record(stream)
-    for _ in range(steps):
+    events = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+    events[0].record(stream)
+    for i in range(steps):
         fn()
-    end.record(stream)
+        events[i + 1].record(stream)
     torch.cuda.synchronize()
     barrier(world)
-    sec = start.elapsed_time(end) / 1e3 / steps
+    sec = events[0].elapsed_time(events[-1]) / 1e3 / steps
+    per = sorted(events[i].elapsed_time(events[i + 1]) for i in range(steps))
+    LAUNCH_STATS[fn] = {"median_ms": round(per[len(per) // 2], 4), "p10_ms": round(per[len(per) // 10], 4),
+                        "p90_ms": round(per[(9 * len(per)) // 10], 4), "launches": steps}
     return max_over_ranks(sec, world, device)
 
 
@@ -468,7 +478,7 @@ def run_ours(args, rank, world, local):
     dsec = time_device(call_d, dec_steps, args.warmup, world, dev)
     gbs = dec_bytes / dsec / 1e9
     decode = {"workload": DECODE, "value": round(gbs * world, 1), "unit": "GB/s", "steps": dec_steps,
-              "ms_per_step": round(dsec * 1e3, 4),
+              "ms_per_step": round(dsec * 1e3, 4), "launch_ms": LAUNCH_STATS.get(call_d),
               "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                            "frac": round(gbs / peaks["hbm_gbs"], 4), "peak_source": f"{peak_src} HBM copy",
                            "traffic": NCU_TRAFFIC.get(("decode_tc", kernel_source_hash("decode_tc"))),
@@ -512,6 +522,7 @@ def run_ours(args, rank, world, local):
         call_x()
         outputs[name] = devt_x[4].float().cpu()
         entry = {"workload": name, "ms_per_step": round(xs * 1e3, 4),
+                 "launch_ms": LAUNCH_STATS.get(call_x) if l2 == "inputs > L2" else None,
                  "tflops": round(f_x / xs / 1e12, 3), "gbs": round(b_x / xs / 1e9, 1),
                  "frac_hbm": round(b_x / xs / 1e9 / peaks["hbm_gbs"], 4),
                  "frac_tensor": round(f_x / xs / 1e12 / peaks["bf16_tflops"], 4), "l2": l2}
@@ -563,6 +574,7 @@ def run_ours(args, rank, world, local):
                    "head_dim": c.D, "mask": "causal", "pos_offset": c.pos_offset,
                    "l2": f"inputs {bytes_of(c) / 1e6:.0f} MB > {L2_BYTES / 1e6:.0f} MB L2, no flush",
                    "parallelism": f"replicas x{world}"},
+        "launch_ms": LAUNCH_STATS.get(call),
         "roofline": roof, "e2e": e2e, "gpu_launches": args.steps, "clocks": clocks, "decode": decode,
         "decode_forms": decode_forms, "prelude": prelude, "per_config": per_config,
     }
