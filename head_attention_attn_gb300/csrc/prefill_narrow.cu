@@ -126,7 +126,9 @@ __device__ __forceinline__ float row_min64(const float* s) {
 
 // TOK: packed token-major sequences.  ZT: some sequence may have key rows inside the tensor
 // that none of its queries sees (the host clears it when it can show that none does).
-template <bool F16, bool TOK, bool ZT>
+// POS: the scale is positive (known on the host), so the minimum path for negative scales and the
+// explicit zeroing for scale 0 are left out of the softmax.
+template <bool F16, bool TOK, bool ZT, bool POS>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     prefill_narrow_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                           const __grid_constant__ CUtensorMap tmV, const NarrowParams p) {
@@ -350,7 +352,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                 tmem_ld_wait32(reinterpret_cast<uint32_t*>(s));
                 tmem_ld_wait32(reinterpret_cast<uint32_t*>(s) + 32);
                 float ext;
-                if (sl >= 0.f) {
+                if (POS || sl >= 0.f) {
                     if (!full) {
 #pragma unroll
                         for (int c = 0; c < 64; ++c) s[c] = (c >= c_lo && c < c_hi) ? s[c] : -INFINITY;
@@ -363,7 +365,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                     }
                     ext = row_min64(s);
                 }
-                const bool seen = (sl >= 0.f) ? (ext != -INFINITY) : (ext != INFINITY);
+                const bool seen = (POS || sl >= 0.f) ? (ext != -INFINITY) : (ext != INFINITY);
                 if (seen) {
                     const float ms = ext * sl;
                     if (m_run == -INFINITY) {
@@ -389,7 +391,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                         // masked scores hold -inf (+inf with a negative scale), so their
                         // 2^(s*scale*log2e - m) is already 0; only scale 0 turns them into NaN
                         // (inf * 0) and needs the explicit zero
-                        if (!full && sl == 0.f) {
+                        if (!POS && !full && sl == 0.f) {
                             p0 = (c >= c_lo && c < c_hi) ? p0 : 0.f;
                             p1 = (c + 1 >= c_lo && c + 1 < c_hi) ? p1 : 0.f;
                         }
@@ -499,7 +501,7 @@ bool encode(CUtensorMap* map, const void* base, unsigned long long dim1, unsigne
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <bool F16, bool TOK, bool ZT>
+template <bool F16, bool TOK, bool ZT, bool POS>
 cudaError_t launch_impl(const Problem& pr, const WaitCtl& wc, cudaStream_t stream) {
     CUtensorMap tq, tk, tv;
     const unsigned long long row = D * 2;
@@ -522,7 +524,7 @@ cudaError_t launch_impl(const Problem& pr, const WaitCtl& wc, cudaStream_t strea
     {
         std::lock_guard<std::mutex> g(mu);
         if (dev < 64 && !configured[dev]) {
-            e = cudaFuncSetAttribute(prefill_narrow_kernel<F16, TOK, ZT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+            e = cudaFuncSetAttribute(prefill_narrow_kernel<F16, TOK, ZT, POS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      kSmem);
             if (e != cudaSuccess) return e;
             configured[dev] = true;
@@ -547,7 +549,7 @@ cudaError_t launch_impl(const Problem& pr, const WaitCtl& wc, cudaStream_t strea
     p.wc = wc;
     const long long grid = (long long)p.num_m * pr.B * pr.Hq;
     if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    prefill_narrow_kernel<F16, TOK, ZT><<<(unsigned)grid, kThreads, kSmem, stream>>>(tq, tk, tv, p);
+    prefill_narrow_kernel<F16, TOK, ZT, POS><<<(unsigned)grid, kThreads, kSmem, stream>>>(tq, tk, tv, p);
     return cudaGetLastError();
 }
 
@@ -560,11 +562,16 @@ bool tail_zero_needed(const Problem& p) {
     return shi < p.Lk;
 }
 
+template <bool F16, bool POS>
+cudaError_t launch_fs(const Problem& p, const WaitCtl& wc, cudaStream_t stream) {
+    if (p.cu_seqlens != nullptr) return launch_impl<F16, true, true, POS>(p, wc, stream);
+    if (tail_zero_needed(p)) return launch_impl<F16, false, true, POS>(p, wc, stream);
+    return launch_impl<F16, false, false, POS>(p, wc, stream);
+}
+
 template <bool F16>
 cudaError_t launch_f(const Problem& p, const WaitCtl& wc, cudaStream_t stream) {
-    if (p.cu_seqlens != nullptr) return launch_impl<F16, true, true>(p, wc, stream);
-    if (tail_zero_needed(p)) return launch_impl<F16, false, true>(p, wc, stream);
-    return launch_impl<F16, false, false>(p, wc, stream);
+    return p.scale > 0.f ? launch_fs<F16, true>(p, wc, stream) : launch_fs<F16, false>(p, wc, stream);
 }
 
 }  // namespace

@@ -188,7 +188,9 @@ __device__ __forceinline__ void tile_bar_sync(int t) {
 // consecutive 128-row blocks of one query head.
 // ZT: some query block may need rows of its last V tile zeroed (the host clears it when it can show
 // that none does; the code is then left out, which the heaviest workloads measurably prefer).
-template <int D, int NT, bool F16, int LAYOUT, bool PAIR, bool ZT>
+// POS: the scale is positive (known on the host), so the minimum path for negative scales and the
+// explicit zeroing for scale 0 are left out of the softmax.
+template <int D, int NT, bool F16, int LAYOUT, bool PAIR, bool ZT, bool POS>
 __global__ void __launch_bounds__(threads_for<NT>(), 3 - NT)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV, const PrefillParams p) {
@@ -613,8 +615,8 @@ __global__ void __launch_bounds__(threads_for<NT>(), 3 - NT)
             tmem_ld64(tS + 64 * h, s);
             float hext;
             if (skip) {
-                hext = (sl >= 0.f) ? -INFINITY : INFINITY;
-            } else if (sl >= 0.f) {
+                hext = (POS || sl >= 0.f) ? -INFINITY : INFINITY;
+            } else if (POS || sl >= 0.f) {
                 if (!full) {
 #pragma unroll
                     for (int c = 0; c < 64; ++c) s[c] = (c >= c_lo && c < c_hi) ? s[c] : -INFINITY;
@@ -635,8 +637,8 @@ __global__ void __launch_bounds__(threads_for<NT>(), 3 - NT)
             tile_bar_sync(t);
             if (!ok) continue;
             const float oext = xch[(1 - h) * BM + row];
-            const float ext = (sl >= 0.f) ? fmaxf(hext, oext) : fminf(hext, oext);
-            const bool any = (sl >= 0.f) ? (ext != -INFINITY) : (ext != INFINITY);
+            const float ext = (POS || sl >= 0.f) ? fmaxf(hext, oext) : fminf(hext, oext);
+            const bool any = (POS || sl >= 0.f) ? (ext != -INFINITY) : (ext != INFINITY);
 
             float alpha = 1.f;
             bool rescale = false;
@@ -675,7 +677,7 @@ __global__ void __launch_bounds__(threads_for<NT>(), 3 - NT)
                     // Masked scores hold -inf (or +inf with a negative scale), so their
                     // 2^(s*scale*log2e - m) is already exactly 0; only scale 0 turns them
                     // into NaN (inf * 0) and needs the explicit zero.
-                    if (!full && sl == 0.f) {
+                    if (!POS && !full && sl == 0.f) {
                         p0 = (c >= c_lo && c < c_hi) ? p0 : 0.f;
                         p1 = (c + 1 >= c_lo && c + 1 < c_hi) ? p1 : 0.f;
                     }
@@ -808,7 +810,7 @@ bool encode_16bit_3d_tok(CUtensorMap* map, const void* base, int D, int H, int t
     return r == CUDA_SUCCESS;
 }
 
-template <int D, int NT, bool F16, int LAYOUT, bool PAIR, bool ZT>
+template <int D, int NT, bool F16, int LAYOUT, bool PAIR, bool ZT, bool POS>
 cudaError_t launch_impl(const Problem& pr, const WaitCtl& wc, cudaStream_t stream) {
     using C = Cfg<D, NT>;
     constexpr int kTiles = NT;
@@ -836,7 +838,7 @@ cudaError_t launch_impl(const Problem& pr, const WaitCtl& wc, cudaStream_t strea
     {
         std::lock_guard<std::mutex> g(mu);
         if (dev < 64 && !configured[dev]) {
-            e = cudaFuncSetAttribute(prefill_tc_kernel<D, NT, F16, LAYOUT, PAIR, ZT>,
+            e = cudaFuncSetAttribute(prefill_tc_kernel<D, NT, F16, LAYOUT, PAIR, ZT, POS>,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
             if (e != cudaSuccess) return e;
             configured[dev] = true;
@@ -871,7 +873,7 @@ cudaError_t launch_impl(const Problem& pr, const WaitCtl& wc, cudaStream_t strea
     }
     const long long grid = (long long)p.num_m * pr.B * (PAIR ? pr.Hq / 2 : pr.Hq);
     if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    prefill_tc_kernel<D, NT, F16, LAYOUT, PAIR, ZT><<<(unsigned)grid, threads_for<NT>(), C::kSmem, stream>>>(tq, tk, tv, p);
+    prefill_tc_kernel<D, NT, F16, LAYOUT, PAIR, ZT, POS><<<(unsigned)grid, threads_for<NT>(), C::kSmem, stream>>>(tq, tk, tv, p);
     return cudaGetLastError();
 }
 
@@ -888,9 +890,12 @@ bool tail_zero_needed(const Problem& p) {
 template <int D, int NT, bool F16, int LAYOUT, bool PAIR>
 cudaError_t launch_zt(const Problem& p, const WaitCtl& wc, cudaStream_t stream) {
     if constexpr (LAYOUT == kHeadMajor) {
-        if (!tail_zero_needed(p)) return launch_impl<D, NT, F16, LAYOUT, PAIR, false>(p, wc, stream);
+        if (!tail_zero_needed(p))
+            return p.scale > 0.f ? launch_impl<D, NT, F16, LAYOUT, PAIR, false, true>(p, wc, stream)
+                                 : launch_impl<D, NT, F16, LAYOUT, PAIR, false, false>(p, wc, stream);
     }
-    return launch_impl<D, NT, F16, LAYOUT, PAIR, LAYOUT != kPaged>(p, wc, stream);
+    return p.scale > 0.f ? launch_impl<D, NT, F16, LAYOUT, PAIR, LAYOUT != kPaged, true>(p, wc, stream)
+                         : launch_impl<D, NT, F16, LAYOUT, PAIR, LAYOUT != kPaged, false>(p, wc, stream);
 }
 
 template <int LAYOUT>
