@@ -49,11 +49,16 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM bytes per launch measured by ncu (dram__bytes_read.sum + dram__bytes_write.sum) for a
 # kernel's code state (its hash); the entry stops applying as soon as the kernel's code changes.
 NCU_TRAFFIC = {
-    # prefill_tc_kernel<128, 2, bf16, paired heads>, causal GQA: 355.24 MB read + 102.99 MB written
-    ("prefill", "b7fe52fc2293"): 458225920.0,
-    # decode_tc_kernel<G4, bf16>: 537.09 MB read + 3.62 MB written at batch 16, scaled by the units
+    # prefill_tc_kernel<128, 2, bf16, paired heads, positive scale>, causal GQA: 377.42 MB read +
+    # 119.17 MB written
+    ("prefill", "cb46dbc1a5bf"): 496588288.0,
+    # decode_tc_kernel<G4, bf16>: 537.10 MB read + 3.72 MB written at batch 16, scaled by the units
     # (items) to the bench's batch 64
-    ("decode_tc", "4b4a0f4709ce"): 4 * 540707328.0,
+    ("decode_tc", "07502ca9ea33"): 4 * 540819968.0,
+    # prefill_narrow_kernel<bf16, head-major, positive scale>, per workload: window 151.60 MB read +
+    # 28.62 MB written; key padding 15.78 MB read, 0 written (the output stays in L2)
+    ("prefill_narrow", "0e78ef1275ba", "window128_bf16_4x12x8192x64"): 180222720.0,
+    ("prefill_narrow", "0e78ef1275ba", "bidir_keypad_bf16_8x12x512x64"): 15776000.0,
 }
 
 
@@ -528,6 +533,8 @@ def run_ours(args, rank, world, local):
                  "frac_tensor": round(f_x / xs / 1e12 / peaks["bf16_tflops"], 4), "l2": l2}
         if c_x.dtype == "f32":
             entry["bound"] = "launch latency (1.06 MFLOP); TFLOP/s for the record only"
+        else:
+            entry["traffic"] = NCU_TRAFFIC.get(("prefill_narrow", kernel_source_hash("prefill_narrow"), name))
         per_config.append(entry)
         if name == KEYPAD:
             # the same valid rows through attn_fwd_varlen: the sequences packed, no padded query rows
