@@ -290,6 +290,23 @@ __device__ __forceinline__ void named_bar_sync() {
     asm volatile("bar.sync %0, %1;" ::"n"(ID), "n"(N) : "memory");
 }
 
+// Bit c set for c in [lo, hi), 0 <= lo, hi <= 64: the visible columns of a 64-key slice.
+__device__ __forceinline__ uint64_t range_bits64(int lo, int hi) {
+    const uint64_t below_hi = hi >= 64 ? ~0ull : ((1ull << hi) - 1ull);
+    const uint64_t below_lo = lo >= 64 ? ~0ull : ((1ull << lo) - 1ull);
+    return below_hi & ~below_lo;
+}
+
+// s[c] keeps its value where bit c of vis is set and becomes `fill` elsewhere (a bit test and a
+// select per score).
+__device__ __forceinline__ void mask_scores64(float* s, uint64_t vis, float fill) {
+    const uint32_t v0 = static_cast<uint32_t>(vis), v1 = static_cast<uint32_t>(vis >> 32);
+#pragma unroll
+    for (int c = 0; c < 32; ++c) s[c] = ((v0 >> c) & 1u) ? s[c] : fill;
+#pragma unroll
+    for (int c = 0; c < 32; ++c) s[32 + c] = ((v1 >> c) & 1u) ? s[32 + c] : fill;
+}
+
 // Maximum of three floats (PTX three-input max).
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
     float r;

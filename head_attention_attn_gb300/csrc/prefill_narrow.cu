@@ -354,14 +354,12 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                 float ext;
                 if (POS || sl >= 0.f) {
                     if (!full) {
-#pragma unroll
-                        for (int c = 0; c < 64; ++c) s[c] = (c >= c_lo && c < c_hi) ? s[c] : -INFINITY;
+                        mask_scores64(s, range_bits64(c_lo, c_hi), -INFINITY);
                     }
                     ext = row_max64(s);
                 } else {
                     if (!full) {
-#pragma unroll
-                        for (int c = 0; c < 64; ++c) s[c] = (c >= c_lo && c < c_hi) ? s[c] : INFINITY;
+                        mask_scores64(s, range_bits64(c_lo, c_hi), INFINITY);
                     }
                     ext = row_min64(s);
                 }
