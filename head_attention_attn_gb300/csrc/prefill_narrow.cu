@@ -314,6 +314,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         const int qi = q0 + row;
         long long rlo, rhi;
         key_interval(p.mode, p.window, klen, (long long)p.P + qi, (long long)p.P + qi, &rlo, &rhi);
+        // the row's visible keys relative to its first column of the first block, clamped to the keys
+        // that exist (a band past them is empty either way): 32-bit offsets for the block loop
+        const int rlo_rel = (int)(min(max(rlo, 0LL), (long long)klen) - (kv0));
+        const int rhi_rel = (int)(min(max(rhi, 0LL), (long long)klen) - (kv0));
         const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
         const uint32_t tS = tmem + lane_off + kColS;
         const uint32_t tO = tmem + lane_off + kColO;
@@ -328,9 +332,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar0 + 8 * kBarSFull, (uint32_t)j & 1, p.wc, abort_flag));
             if (!ok) break;
             tc_fence_after();
-            const long long tb = kv0 + (long long)j * BN;  // first key of the block
-            const int c_lo = (int)max(0LL, min(64LL, rlo - tb));
-            const int c_hi = (int)max(0LL, min(64LL, rhi - tb));
+            const int c_lo = min(max(rlo_rel - j * BN, 0), 64);  // my visible columns [c_lo, c_hi)
+            const int c_hi = min(max(rhi_rel - j * BN, 0), 64);
             const bool full = (c_lo == 0 && c_hi == 64);
             // every row of the warp sees none of the block's keys: zeros for its P, no exponentials
             const bool skip = __all_sync(0xffffffffu, c_lo >= c_hi);

@@ -580,6 +580,10 @@ __global__ void __launch_bounds__(threads_for<NT>(), 3 - NT)
         const long long qpos = (long long)P + qi;
         long long rlo, rhi;
         key_interval(p.mode, p.window, klen, qpos, qpos, &rlo, &rhi);
+        // the row's visible keys relative to its first column of the first block, clamped to the keys
+        // that exist (a band past them is empty either way): 32-bit offsets for the block loop
+        const int rlo_rel = (int)(min(max(rlo, 0LL), (long long)klen) - (kv0 + 64 * h));
+        const int rhi_rel = (int)(min(max(rhi, 0LL), (long long)klen) - (kv0 + 64 * h));
         const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
         const uint32_t tS = tmem + lane_off + C::kColS + 128 * t;
         const uint32_t tO = tmem + lane_off + C::kColO + 128 * t;
@@ -598,9 +602,8 @@ __global__ void __launch_bounds__(threads_for<NT>(), 3 - NT)
             // once per key block, so the other warps of the tile never wait for it.
             if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar0 + 8 * (kBarSFull + t), (uint32_t)i & 1, p.wc, abort_flag));
             tc_fence_after();
-            const long long tb = kv0 + (long long)j * BN + 64 * h;  // first key of my 64 columns
-            const int c_lo = (int)max(0LL, min(64LL, rlo - tb));
-            const int c_hi = (int)max(0LL, min(64LL, rhi - tb));
+            const int c_lo = min(max(rlo_rel - j * BN, 0), 64);  // my visible columns [c_lo, c_hi)
+            const int c_hi = min(max(rhi_rel - j * BN, 0), 64);
             const bool full = (c_lo == 0 && c_hi == 64);
             // every row of my warp sees none of my 64 keys (a band edge on a 32-row boundary):
             // no max and no exponentials, just zeros for my half of P.  Only with one tile per
