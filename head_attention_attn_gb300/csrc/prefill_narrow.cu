@@ -4,9 +4,9 @@
 // At head_dim 64 the per-tile chain (S -> softmax -> P -> P V -> next S) is short and its
 // latency, not a throughput, sets the pace: the more independent query tiles an SM holds, the
 // better.  This kernel keeps each tile's tensor memory at 128 columns (S of a 64-key block: 64
-// fp32 columns, P aliasing its first 32; O: 64) and its shared memory near 50 KB, so three CTAs
-// of one 128-row query tile each share an SM (four would fit the memories, but at 80 registers a
-// thread the softmax spills and ran no faster on GB300).
+// fp32 columns, P aliasing its first 32; O: 64) and its shared memory near 50 KB, so four CTAs
+// of one 128-row query tile each share an SM (the tensor memory's limit), at 80 registers a
+// thread.
 //   warp 0       TMA producer: the Q tile, then 64-key K and V tiles through 2-stage rings
 //                (128-byte swizzle).  With key padding or a band that ends inside the tensor
 //                it also zeroes the rows of the last V tile that no query of the sequence sees.
@@ -41,7 +41,7 @@ constexpr int BM = 128;       // query rows per tile
 constexpr int BN = 64;        // keys per block
 constexpr int kStages = 2;    // K/V ring depth
 constexpr int kThreads = 192;  // producer, MMA issuer, 4 softmax warps
-constexpr int kCtasPerSm = 3;
+constexpr int kCtasPerSm = 4;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f;
 
