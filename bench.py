@@ -49,16 +49,13 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM bytes per launch measured by ncu (dram__bytes_read.sum + dram__bytes_write.sum) for a
 # kernel's code state (its hash); the entry stops applying as soon as the kernel's code changes.
 NCU_TRAFFIC = {
-    # prefill_tc_kernel<128, 2, bf16, paired heads, positive scale>, causal GQA: 377.42 MB read +
-    # 119.17 MB written
-    ("prefill", "cb46dbc1a5bf"): 496588288.0,
-    # decode_tc_kernel<G4, bf16>: 537.10 MB read + 3.72 MB written at batch 16, scaled by the units
-    # (items) to the bench's batch 64
-    ("decode_tc", "07502ca9ea33"): 4 * 540819968.0,
-    # prefill_narrow_kernel<bf16, head-major, positive scale>, per workload: window 151.60 MB read +
-    # 28.62 MB written; key padding 15.78 MB read, 0 written (the output stays in L2)
-    ("prefill_narrow", "0e78ef1275ba", "window128_bf16_4x12x8192x64"): 180222720.0,
-    ("prefill_narrow", "0e78ef1275ba", "bidir_keypad_bf16_8x12x512x64"): 15776000.0,
+    # prefill_tc_kernel<128, 2, bf16, paired heads, positive scale>, causal GQA: 380.24 MB read +
+    # 113.04 MB written
+    ("prefill", "99a653b9b8bb"): 493282304.0,
+    # prefill_narrow_kernel<bf16, head-major, positive scale>, per workload: window 151.08 MB read +
+    # 26.55 MB written; key padding 15.77 MB read, 0 written (the output stays in L2)
+    ("prefill_narrow", "9afb070a8394", "window128_bf16_4x12x8192x64"): 177631744.0,
+    ("prefill_narrow", "9afb070a8394", "bidir_keypad_bf16_8x12x512x64"): 15772416.0,
 }
 
 
