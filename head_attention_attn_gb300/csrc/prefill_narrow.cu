@@ -274,18 +274,19 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             constexpr uint32_t kIdescQK = idesc_f16kind_f32(BM, BN, 0, 0, F16);
             constexpr uint32_t kIdescPV = idesc_f16kind_f32(BM, D, 0, 1, F16);
             bool ok = mbar_wait(bar0 + 8 * kBarQFull, 0, p.wc, abort_flag);
+            const uint64_t qd = smem_desc_sw128(sbase + kOffQ, 16, 1024);
             for (int j = 0; ok && j <= nblk; ++j) {
                 if (j > 0) {  // PV(j - 1), once its P is in TMEM
                     const int jp = j - 1, s = jp % kStages;
                     if (!mbar_wait(bar0 + 8 * kBarPFull, (uint32_t)jp & 1, p.wc, abort_flag)) break;
                     if (!mbar_wait(bar0 + 8 * (kBarVFull + s), (uint32_t)(jp / kStages) & 1, p.wc, abort_flag)) break;
                     tc_fence_after();
-                    const uint32_t vbase = sbase + kOffV + s * kKVBytes;
+                    // descriptors: the tile's, plus each step's offset >> 4 in the address field
+                    const uint64_t vd = smem_desc_sw128(sbase + kOffV + s * kKVBytes, BN * 128, 1024);
 #pragma unroll
-                    for (int kk = 0; kk < BN / 16; ++kk) {
-                        const uint64_t bd = smem_desc_sw128(vbase + kk * (16 * 128), BN * 128, 1024);
-                        tc_mma_ts(tmem + kColO, tmem + kColS + kk * 8, bd, kIdescPV, (jp > 0 || kk > 0) ? 1u : 0u);
-                    }
+                    for (int kk = 0; kk < BN / 16; ++kk)
+                        tc_mma_ts(tmem + kColO, tmem + kColS + kk * 8, vd + (uint64_t)((kk * 16 * 128) >> 4), kIdescPV,
+                                  (jp > 0 || kk > 0) ? 1u : 0u);
                     tc_commit(bar0 + 8 * (kBarVEmpty + s));
                     if (jp == nblk - 1) tc_commit(bar0 + 8 * kBarOFull);
                 }
@@ -293,13 +294,11 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                     const int s = j % kStages;
                     if (!mbar_wait(bar0 + 8 * (kBarKFull + s), (uint32_t)(j / kStages) & 1, p.wc, abort_flag)) break;
                     tc_fence_after();
-                    const uint32_t kbase = sbase + kOffK + s * kKVBytes;
+                    const uint64_t kd = smem_desc_sw128(sbase + kOffK + s * kKVBytes, 16, 1024);
 #pragma unroll
-                    for (int ks = 0; ks < D / 16; ++ks) {
-                        const uint64_t a = smem_desc_sw128(sbase + kOffQ + ks * 32, 16, 1024);
-                        const uint64_t bd = smem_desc_sw128(kbase + ks * 32, 16, 1024);
-                        tc_mma_ss(tmem + kColS, a, bd, kIdescQK, ks > 0 ? 1u : 0u);
-                    }
+                    for (int ks = 0; ks < D / 16; ++ks)
+                        tc_mma_ss(tmem + kColS, qd + (uint64_t)((ks * 32) >> 4), kd + (uint64_t)((ks * 32) >> 4), kIdescQK,
+                                  ks > 0 ? 1u : 0u);
                     tc_commit(bar0 + 8 * kBarSFull);
                     tc_commit(bar0 + 8 * (kBarKEmpty + s));
                 }

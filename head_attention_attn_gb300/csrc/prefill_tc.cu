@@ -526,14 +526,14 @@ __global__ void __launch_bounds__(threads_for<NT>(), 3 - NT)
                             v_waited = true;
                         }
                         tc_fence_after();
-                        const uint32_t vbase = sbase + C::kOffV + s * C::kKVBytes;
+                        // descriptors: the tile's, plus each step's offset >> 4 in the address field
+                        const uint64_t vd = smem_desc_sw128(sbase + C::kOffV + s * C::kKVBytes, BN * 128, 1024);
                         const uint32_t tP = tmem + C::kColS + 128 * t;
                         const uint32_t tO = tmem + C::kColO + 128 * t;
 #pragma unroll
-                        for (int kk = 0; kk < BN / 16; ++kk) {
-                            const uint64_t bd = smem_desc_sw128(vbase + kk * (16 * 128), BN * 128, 1024);
-                            tc_mma_ts(tO, tP + kk * 8, bd, kIdescPV, (jp > rng[t].jb || kk > 0) ? 1u : 0u);
-                        }
+                        for (int kk = 0; kk < BN / 16; ++kk)
+                            tc_mma_ts(tO, tP + kk * 8, vd + (uint64_t)((kk * 16 * 128) >> 4), kIdescPV,
+                                      (jp > rng[t].jb || kk > 0) ? 1u : 0u);
                         it[t] += 1;
                         used_v = true;
                         if (jp == rng[t].je - 1) tc_commit(bar0 + 8 * (kBarOFull + t));
@@ -545,15 +545,13 @@ __global__ void __launch_bounds__(threads_for<NT>(), 3 - NT)
                             k_waited = true;
                             tc_fence_after();
                         }
-                        const uint32_t kbase = sbase + C::kOffK + s * C::kKVBytes;
-                        const uint32_t qbase = sbase + C::kOffQ + t * C::kQBytes;
+                        const uint64_t kd = smem_desc_sw128(sbase + C::kOffK + s * C::kKVBytes, 16, 1024);
+                        const uint64_t qd = smem_desc_sw128(sbase + C::kOffQ + t * C::kQBytes, 16, 1024);
                         const uint32_t tS = tmem + C::kColS + 128 * t;
 #pragma unroll
                         for (int ks = 0; ks < D / 16; ++ks) {
-                            const uint32_t off = (ks >> 2) * (BM * 128) + (ks & 3) * 32;
-                            const uint64_t a = smem_desc_sw128(qbase + off, 16, 1024);
-                            const uint64_t bd = smem_desc_sw128(kbase + off, 16, 1024);
-                            tc_mma_ss(tS, a, bd, kIdescQK, ks > 0 ? 1u : 0u);
+                            const uint64_t off = (uint64_t)((((ks >> 2) * (BM * 128)) + (ks & 3) * 32) >> 4);
+                            tc_mma_ss(tS, qd + off, kd + off, kIdescQK, ks > 0 ? 1u : 0u);
                         }
                         tc_commit(bar0 + 8 * (kBarSFull + t));
                         used_k = true;
