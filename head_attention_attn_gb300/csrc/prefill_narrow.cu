@@ -80,6 +80,7 @@ struct NarrowParams {
     const int32_t* cu_seqlens;  // packed token-major sequences [B + 1], or null (head-major batch)
     int total;                  // packed rows
     int out_tok;                // head-major batch: out is [B, Lq, Hq, D]
+    int tma_out;                // out [B, Hq, Lq, D]: the tile is stored by one TMA copy from shared memory
     float scale_log2;
     WaitCtl wc;
 };
@@ -131,7 +132,8 @@ __device__ __forceinline__ float row_min64(const float* s) {
 template <bool F16, bool TOK, bool ZT, bool POS>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     prefill_narrow_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                          const __grid_constant__ CUtensorMap tmV, const NarrowParams p) {
+                          const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+                          const NarrowParams p) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_s = smem_u32(smem_raw);
     uint8_t* smem = smem_raw + ((1024u - (raw_s & 1023u)) & 1023u);
@@ -428,7 +430,51 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         }
         // (the TMEM loads are warp-collective: every lane runs them, and only rows inside the
         // sequence are stored)
-        if (ok) {
+        if (p.tma_out) {
+            // head-major output: each thread writes its normalised row into the Q buffer (free
+            // once the last product has completed; never loaded without key blocks) in the
+            // 128-byte-swizzle layout of a Q tile, and one thread stores the tile with TMA (rows
+            // past Lq are clipped by the copy)
+            if (ok) {
+                const float inv = (l_run > 0.f) ? 1.f / l_run : 0.f;
+                uint8_t* qrow_s = smem + kOffQ + row * 128;
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    float o[32];
+                    if (nblk > 0) {
+                        tmem_ld32(tO + 32 * c, o);
+                    } else {
+#pragma unroll
+                        for (int q = 0; q < 32; ++q) o[q] = 0.f;
+                    }
+#pragma unroll
+                    for (int q = 0; q < 32; q += 8) {
+                        const int unit = (32 * c + q) / 8;  // 16-byte unit of the row
+                        *reinterpret_cast<uint4*>(qrow_s + ((unit ^ (row & 7)) << 4)) =
+                            make_uint4(pack2<F16>(o[q] * inv, o[q + 1] * inv), pack2<F16>(o[q + 2] * inv, o[q + 3] * inv),
+                                       pack2<F16>(o[q + 4] * inv, o[q + 5] * inv), pack2<F16>(o[q + 6] * inv, o[q + 7] * inv));
+                    }
+                }
+                fence_proxy_async_smem();
+            }
+            // the four softmax warps meet (every path reaches this) and agree that all rows are in place
+            uint32_t all_ok;
+            asm volatile(
+                "{\n\t.reg .pred pin, pout;\n\tsetp.ne.u32 pin, %1, 0;\n\t"
+                "bar.red.and.pred pout, 1, 128, pin;\n\tselp.u32 %0, 1, 0, pout;\n\t}"
+                : "=r"(all_ok)
+                : "r"((uint32_t)ok)
+                : "memory");
+            if (all_ok && warp == 2 && lane == 0) {
+                asm volatile(
+                    "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
+                        reinterpret_cast<uint64_t>(&tmO)),
+                    "r"(0), "r"(q0), "r"(b * p.Hq + hq), "r"(sbase + kOffQ)
+                    : "memory");
+                asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+                asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");  // before the CTA may leave
+            }
+        } else if (ok) {
             const float inv = (l_run > 0.f) ? 1.f / l_run : 0.f;
             __nv_bfloat16* orow =
                 p.out + (TOK        ? ((size_t)(row0 + qi) * p.Hq + hq) * D
@@ -503,7 +549,7 @@ bool encode(CUtensorMap* map, const void* base, unsigned long long dim1, unsigne
 
 template <bool F16, bool TOK, bool ZT, bool POS>
 cudaError_t launch_impl(const Problem& pr, const WaitCtl& wc, cudaStream_t stream) {
-    CUtensorMap tq, tk, tv;
+    CUtensorMap tq, tk, tv, to;
     const unsigned long long row = D * 2;
     if (TOK) {
         // [total, H, 64] as (64, H, total): a box is 128 (Q) or 64 (K, V) consecutive rows of one head
@@ -515,6 +561,14 @@ cudaError_t launch_impl(const Problem& pr, const WaitCtl& wc, cudaStream_t strea
                !encode(&tk, pr.k, pr.Lk, (unsigned long long)pr.B * pr.Hkv, row, row * pr.Lk, BN, 1, F16) ||
                !encode(&tv, pr.v, pr.Lk, (unsigned long long)pr.B * pr.Hkv, row, row * pr.Lk, BN, 1, F16)) {
         return cudaErrorInvalidValue;
+    }
+    // head-major output [B, Hq, Lq, 64]: stored a tile at a time by TMA, through the map Q uses
+    const bool tma_out = !TOK && !pr.out_tok;
+    if (tma_out) {
+        if (!encode(&to, pr.out, pr.Lq, (unsigned long long)pr.B * pr.Hq, row, row * pr.Lq, BM, 1, F16))
+            return cudaErrorInvalidValue;
+    } else {
+        to = tq;  // not used
     }
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -545,11 +599,12 @@ cudaError_t launch_impl(const Problem& pr, const WaitCtl& wc, cudaStream_t strea
     p.cu_seqlens = pr.cu_seqlens;
     p.total = pr.total;
     p.out_tok = pr.out_tok ? 1 : 0;
+    p.tma_out = tma_out ? 1 : 0;
     p.scale_log2 = pr.scale * kLog2e;
     p.wc = wc;
     const long long grid = (long long)p.num_m * pr.B * pr.Hq;
     if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    prefill_narrow_kernel<F16, TOK, ZT, POS><<<(unsigned)grid, kThreads, kSmem, stream>>>(tq, tk, tv, p);
+    prefill_narrow_kernel<F16, TOK, ZT, POS><<<(unsigned)grid, kThreads, kSmem, stream>>>(tq, tk, tv, to, p);
     return cudaGetLastError();
 }
 
