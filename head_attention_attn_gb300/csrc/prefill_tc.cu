@@ -103,6 +103,7 @@ struct PrefillParams {
     const int32_t* cu_seqlens;  // packed token-major sequences [B + 1], or null (head-major batch)
     int total;          // packed rows (token-major)
     int out_tok;        // head-major batch: out is [B, Lq, Hq, D] instead of [B, Hq, Lq, D]
+    int tma_out;        // head-major out [B, Hq, Lq, 128]: tiles stored by TMA from shared memory
     float scale_log2;
     WaitCtl wc;
     // kPaged: pools [num_pages, Hkv, page_size, D]; sequence b's position j is row j % page_size of
@@ -193,7 +194,8 @@ __device__ __forceinline__ void tile_bar_sync(int t) {
 template <int D, int NT, bool F16, int LAYOUT, bool PAIR, bool ZT, bool POS>
 __global__ void __launch_bounds__(threads_for<NT>(), 3 - NT)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                      const __grid_constant__ CUtensorMap tmV, const PrefillParams p) {
+                      const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+                      const PrefillParams p) {
     using C = Cfg<D, NT>;
     constexpr int kTiles = NT;
     extern __shared__ uint8_t smem_raw[];
@@ -719,7 +721,57 @@ __global__ void __launch_bounds__(threads_for<NT>(), 3 - NT)
             ok = __all_sync(0xffffffffu, mbar_wait(bar0 + 8 * (kBarOFull + t), 0, p.wc, abort_flag));
             tc_fence_after();
         }
-        if (ok && q0 + tile_dq(t) < Lq) {
+        if (D == 128 && LAYOUT == kHeadMajor && p.tma_out) {
+            // head-major output: each half writes its 64 head dims of the row (one 128-byte chunk)
+            // into the tile's Q buffer in the layout of a Q tile (free once the tile's last product
+            // has completed; without key blocks its copy is waited for), and one thread of the tile
+            // stores both chunks with TMA (rows past Lq are clipped by the copy)
+            if (ok && !has && ntiles > 0) {
+                ok = __all_sync(0xffffffffu, mbar_wait(bar0 + 8 * kBarQFull, 0, p.wc, abort_flag));
+            }
+            if (ok) {
+                const float inv = (l_tot > 0.f) ? 1.f / l_tot : 0.f;
+                uint8_t* srow = smem + C::kOffQ + t * C::kQBytes + h * (BM * 128) + row * 128;
+#pragma unroll
+                for (int c = 0; c < D / 64; ++c) {
+                    float o[32];
+                    if (has) {
+                        tmem_ld32(tO + (D / 2) * h + 32 * c, o);
+                    } else {
+#pragma unroll
+                        for (int q = 0; q < 32; ++q) o[q] = 0.f;
+                    }
+#pragma unroll
+                    for (int q = 0; q < 32; q += 8) {
+                        const int unit = (32 * c + q) / 8;  // 16-byte unit of the 128-byte chunk row
+                        *reinterpret_cast<uint4*>(srow + ((unit ^ (row & 7)) << 4)) =
+                            make_uint4(pack2<F16>(o[q] * inv, o[q + 1] * inv), pack2<F16>(o[q + 2] * inv, o[q + 3] * inv),
+                                       pack2<F16>(o[q + 4] * inv, o[q + 5] * inv), pack2<F16>(o[q + 6] * inv, o[q + 7] * inv));
+                    }
+                }
+                fence_proxy_async_smem();
+            }
+            // the tile's 8 warps meet (every path reaches this) and agree that all rows are in place
+            uint32_t all_ok;
+            asm volatile(
+                "{\n\t.reg .pred pin, pout;\n\tsetp.ne.u32 pin, %1, 0;\n\t"
+                "bar.red.and.pred pout, %2, 256, pin;\n\tselp.u32 %0, 1, 0, pout;\n\t}"
+                : "=r"(all_ok)
+                : "r"((uint32_t)ok), "r"(1 + t)
+                : "memory");
+            if (all_ok && (sw & 7) == 0 && lane == 0 && q0 + tile_dq(t) < Lq) {
+#pragma unroll
+                for (int c = 0; c < 2; ++c)
+                    asm volatile(
+                        "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
+                            reinterpret_cast<uint64_t>(&tmO)),
+                        "r"(c * 64), "r"(q0 + tile_dq(t)), "r"(b * p.Hq + hqt),
+                        "r"(sbase + C::kOffQ + t * C::kQBytes + c * (BM * 128))
+                        : "memory");
+                asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+                asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");  // before the CTA may leave
+            }
+        } else if (ok && q0 + tile_dq(t) < Lq) {
             const float inv = (l_tot > 0.f) ? 1.f / l_tot : 0.f;
             __nv_bfloat16* orow =
                 p.out + (tok        ? ((size_t)(row0 + qi) * p.Hq + hqt) * D
@@ -813,7 +865,7 @@ template <int D, int NT, bool F16, int LAYOUT, bool PAIR, bool ZT, bool POS>
 cudaError_t launch_impl(const Problem& pr, const WaitCtl& wc, cudaStream_t stream) {
     using C = Cfg<D, NT>;
     constexpr int kTiles = NT;
-    CUtensorMap tq, tk, tv;
+    CUtensorMap tq, tk, tv, to;
     if (LAYOUT == kPaged) {
         // only Q is copied by TMA; the K and V rows are gathered through the page table
         if (!encode_16bit_3d_tok(&tq, pr.q, D, pr.Hq, pr.total, F16)) return cudaErrorInvalidValue;
@@ -828,6 +880,13 @@ cudaError_t launch_impl(const Problem& pr, const WaitCtl& wc, cudaStream_t strea
                !encode_16bit_3d(&tk, pr.k, D, pr.Lk, pr.B * pr.Hkv, F16) ||
                !encode_16bit_3d(&tv, pr.v, D, pr.Lk, pr.B * pr.Hkv, F16)) {
         return cudaErrorInvalidValue;
+    }
+    // head-major output [B, Hq, Lq, 128]: tiles stored by TMA through a map shaped like Q's
+    const bool tma_out = D == 128 && LAYOUT == kHeadMajor && !pr.out_tok;
+    if (tma_out) {
+        if (!encode_16bit_3d(&to, pr.out, D, pr.Lq, pr.B * pr.Hq, F16)) return cudaErrorInvalidValue;
+    } else {
+        to = tq;  // not used
     }
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -859,6 +918,7 @@ cudaError_t launch_impl(const Problem& pr, const WaitCtl& wc, cudaStream_t strea
     p.cu_seqlens = pr.cu_seqlens;
     p.total = pr.total;
     p.out_tok = pr.out_tok ? 1 : 0;
+    p.tma_out = tma_out ? 1 : 0;
     p.scale_log2 = pr.scale * kLog2e;
     p.wc = wc;
     if (LAYOUT == kPaged) {
@@ -872,7 +932,7 @@ cudaError_t launch_impl(const Problem& pr, const WaitCtl& wc, cudaStream_t strea
     }
     const long long grid = (long long)p.num_m * pr.B * (PAIR ? pr.Hq / 2 : pr.Hq);
     if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    prefill_tc_kernel<D, NT, F16, LAYOUT, PAIR, ZT, POS><<<(unsigned)grid, threads_for<NT>(), C::kSmem, stream>>>(tq, tk, tv, p);
+    prefill_tc_kernel<D, NT, F16, LAYOUT, PAIR, ZT, POS><<<(unsigned)grid, threads_for<NT>(), C::kSmem, stream>>>(tq, tk, tv, to, p);
     return cudaGetLastError();
 }
 
