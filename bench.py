@@ -49,16 +49,16 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM bytes per launch measured by ncu (dram__bytes_read.sum + dram__bytes_write.sum) for a
 # kernel's code state (its hash); the entry stops applying as soon as the kernel's code changes.
 NCU_TRAFFIC = {
-    # prefill_tc_kernel<128, 2, bf16, paired heads, positive scale>, causal GQA: 373.27 MB read +
-    # 113.31 MB written
-    ("prefill", "d0d8bb113484"): 486578432.0,
+    # prefill_tc_kernel<128, 2, bf16, paired heads, positive scale>, causal GQA: 393.95 MB read +
+    # 117.45 MB written
+    ("prefill", "1fcf40b7e31c"): 511397888.0,
     # decode_tc_kernel<G4, bf16>: 537.09 MB read + 3.42 MB written at batch 16, scaled by the units
     # (items) to the bench's batch 64
     ("decode_tc", "1236c0ea2fcc"): 4 * 540508160.0,
-    # prefill_narrow_kernel<bf16, head-major, positive scale>, per workload: window 151.07 MB read +
-    # 26.30 MB written; key padding 15.77 MB read, 0 written (the output stays in L2)
-    ("prefill_narrow", "99c8ce8da161", "window128_bf16_4x12x8192x64"): 177364992.0,
-    ("prefill_narrow", "99c8ce8da161", "bidir_keypad_bf16_8x12x512x64"): 15771904.0,
+    # prefill_narrow_kernel<bf16, head-major, positive scale>, per workload: window 151.06 MB read +
+    # 27.99 MB written; key padding 15.77 MB read, 0 written (the output stays in L2)
+    ("prefill_narrow", "ce907a89b770", "window128_bf16_4x12x8192x64"): 179046144.0,
+    ("prefill_narrow", "ce907a89b770", "bidir_keypad_bf16_8x12x512x64"): 15774976.0,
 }
 
 
