@@ -49,9 +49,9 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM bytes per launch measured by ncu (dram__bytes_read.sum + dram__bytes_write.sum) for a
 # kernel's code state (its hash); the entry stops applying as soon as the kernel's code changes.
 NCU_TRAFFIC = {
-    # prefill_tc_kernel<128, 2, bf16, paired heads, positive scale>, causal GQA: 393.95 MB read +
-    # 117.45 MB written
-    ("prefill", "1fcf40b7e31c"): 511397888.0,
+    # prefill_tc_kernel<128, 2, bf16, paired heads, positive scale>, causal GQA, with L2 hints
+    # (Q and O evict-first, K/V evict-last): 316.69 MB read + 95.92 MB written
+    ("prefill", "4c37abd2b905"): 412608256.0,
     # decode_tc_kernel<G4, bf16>: 537.09 MB read + 3.42 MB written at batch 16, scaled by the units
     # (items) to the bench's batch 64
     ("decode_tc", "1236c0ea2fcc"): 4 * 540508160.0,

@@ -319,16 +319,19 @@ __global__ void __launch_bounds__(threads_for<NT>(), 3 - NT)
         return ZT && !PAGED && ntiles > 0 && *zhi > *zlo;
     };
     const int kbh = b * p.Hkv + hk;
+    // L2 hints: a Q tile is read by this CTA alone, once; K and V tiles are read again by the
+    // other query blocks of the kv head, so they are the ones to keep in L2
     auto load_q = [&]() {
+        const uint64_t once = l2_policy_evict_first();
         mbar_arrive_expect_tx(bar0 + 8 * kBarQFull, kTiles * C::kQBytes);
         for (int t = 0; t < kTiles; ++t)
             for (int c = 0; c < C::kChunks; ++c)
                 if constexpr (TOK)
-                    tma_load_3d(sbase + C::kOffQ + t * C::kQBytes + c * (BM * 128), &tmQ, bar0 + 8 * kBarQFull,
-                                c * 64, hq + tile_dh(t), row0 + q0 + tile_dq(t));
+                    tma_load_3d_hint(sbase + C::kOffQ + t * C::kQBytes + c * (BM * 128), &tmQ, bar0 + 8 * kBarQFull,
+                                     c * 64, hq + tile_dh(t), row0 + q0 + tile_dq(t), once);
                 else
-                    tma_load_3d(sbase + C::kOffQ + t * C::kQBytes + c * (BM * 128), &tmQ, bar0 + 8 * kBarQFull,
-                                c * 64, q0 + tile_dq(t), b * p.Hq + hq + tile_dh(t));
+                    tma_load_3d_hint(sbase + C::kOffQ + t * C::kQBytes + c * (BM * 128), &tmQ, bar0 + 8 * kBarQFull,
+                                     c * 64, q0 + tile_dq(t), b * p.Hq + hq + tile_dh(t), once);
     };
     // (the tail V tile lands on its own barrier, land_tail, when some of its rows must be zeroed first)
     auto load_kv = [&](const CUtensorMap* map, int off, int bar, int j, bool land_tail) {
@@ -336,10 +339,11 @@ __global__ void __launch_bounds__(threads_for<NT>(), 3 - NT)
         const int krow = (int)kv0 + j * BN;
         const uint32_t done = (land_tail && bar == kBarVFull && j == ntiles - 1) ? bar0 + 8 * kBarVLand
                                                                                  : bar0 + 8 * (bar + s);
+        const uint64_t keep = l2_policy_evict_last();
         mbar_arrive_expect_tx(done, C::kKVBytes);
         for (int c = 0; c < C::kChunks; ++c)
-            tma_load_3d(sbase + off + s * C::kKVBytes + c * (BN * 128), map, done, c * 64,
-                        TOK ? hk : krow, TOK ? row0 + krow : kbh);
+            tma_load_3d_hint(sbase + off + s * C::kKVBytes + c * (BN * 128), map, done, c * 64,
+                             TOK ? hk : krow, TOK ? row0 + krow : kbh, keep);
     };
     // With one tile per CTA (two CTAs per SM) the first copies go out before the CTA
     // synchronises; with two tiles (one CTA per SM) that delays the CTA's start more than
@@ -760,13 +764,14 @@ __global__ void __launch_bounds__(threads_for<NT>(), 3 - NT)
                 : "r"((uint32_t)ok), "r"(1 + t)
                 : "memory");
             if (all_ok && (sw & 7) == 0 && lane == 0 && q0 + tile_dq(t) < Lq) {
+                const uint64_t once = l2_policy_evict_first();  // nothing in this launch reads it back
 #pragma unroll
                 for (int c = 0; c < 2; ++c)
                     asm volatile(
-                        "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
+                        "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group.L2::cache_hint [%0, {%1, %2, %3}], [%4], %5;" ::"l"(
                             reinterpret_cast<uint64_t>(&tmO)),
                         "r"(c * 64), "r"(q0 + tile_dq(t)), "r"(b * p.Hq + hqt),
-                        "r"(sbase + C::kOffQ + t * C::kQBytes + c * (BM * 128))
+                        "r"(sbase + C::kOffQ + t * C::kQBytes + c * (BM * 128)), "l"(once)
                         : "memory");
                 asm volatile("cp.async.bulk.commit_group;" ::: "memory");
                 asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");  // before the CTA may leave
