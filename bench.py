@@ -326,6 +326,49 @@ def decode_forms_leg(args, world, dev, peaks, peak_src, dec_bytes):
     return legs
 
 
+def paged_prefill_leg(args, world, dev, peaks, peak_src):
+    """TFLOP/s of attn_fwd_varlen_paged on a chunked prefill shaped like the causal GQA workload:
+    4 sequences whose newest 512 positions (the queries) follow 3,584 older ones in paged caches
+    (4,096 cached positions each), 32 query / 8 kv heads, head_dim 128, bf16, causal, with pages
+    of 16 and of 128 rows.  Algorithmic FLOPs count the visible (query, key) pairs only."""
+    import head_attention_attn_gb300 as attn
+    B, Hq, Hkv, D, chunk, kv = 4, 32, 8, 128, 512, 4096
+    P = kv - chunk
+    flops = 4.0 * D * Hq * B * sum(P + i + 1 for i in range(chunk))
+    scale = float(torch.tensor(1.0 / math.sqrt(D), dtype=torch.float32))
+    steps = max(3, min(args.steps, 200))
+    g = torch.Generator().manual_seed(1008)
+    legs = []
+    q = torch.empty(B * chunk, Hq, D, dtype=torch.bfloat16, device=dev).normal_()
+    out = torch.empty_like(q)
+    cu = torch.arange(0, (B + 1) * chunk, chunk, dtype=torch.int32, device=dev)
+    kv_lens = torch.full((B,), kv, dtype=torch.int32, device=dev)
+    for ps in (16, 128):
+        max_pages = kv // ps
+        num_pages = B * max_pages
+        k_pool = torch.empty(num_pages, Hkv, ps, D, dtype=torch.bfloat16, device=dev).normal_()
+        v_pool = torch.empty_like(k_pool).normal_()
+        table = torch.randperm(num_pages, generator=g).to(torch.int32).view(B, max_pages).to(dev)
+
+        def call(k_pool=k_pool, v_pool=v_pool, table=table):
+            attn.attn_fwd_varlen_paged(q, k_pool, v_pool, table, cu, kv_lens, chunk, out, scale=scale)
+        sec = time_device(call, steps, args.warmup, world, dev)
+        if attn.sync_status() != attn.ATTN_OK:
+            raise RuntimeError("device status after the paged prefill: " + attn.last_error())
+        tflops = flops / sec / 1e12
+        legs.append({"workload": f"paged_prefill_bf16_{B}x{Hq}q{Hkv}kv_{chunk}of{kv}x{D}_page{ps}",
+                     "value": round(tflops * world, 1), "unit": "TFLOP/s", "steps": steps,
+                     "ms_per_step": round(sec * 1e3, 4), "launch_ms": LAUNCH_STATS.get(call),
+                     "roofline": {"bound": "tensor", "achieved": round(tflops, 1), "peak": peaks["bf16_tflops"],
+                                  "unit": "TFLOP/s", "frac": round(tflops / peaks["bf16_tflops"], 4),
+                                  "peak_source": f"{peak_src} bf16 dense (burst)", "traffic": None,
+                                  "kernel": "prefill_tc_kernel<128, 2, bf16, paged> (K/V copied by TMA a page piece at a time)",
+                                  "algorithmic_flops_per_launch": flops}})
+        del k_pool, v_pool, table
+        torch.cuda.empty_cache()
+    return legs
+
+
 def kernel_source_hash(kernel: str = "prefill") -> str:
     """Identifies a kernel's code: its source, the shared device headers and the nvcc flags
     (comments and blank lines do not count), so a DRAM-traffic figure stays attached to the
@@ -496,6 +539,7 @@ def run_ours(args, rank, world, local):
     # ---- per-item and paged caches at the decode workload's shape (ferrum-kernels
     # flash_attention_batched_per_cache): the same K/V bytes, addressed by the device
     decode_forms = decode_forms_leg(args, world, dev, peaks, peak_src, dec_bytes)
+    paged_prefill = paged_prefill_leg(args, world, dev, peaks, peak_src)
 
     # ---- attention prelude leg: split fused QKV + QK RMS norm + RoPE + head-major transpose for
     # the headline workload's 4 x 4096 tokens (32 q / 8 kv heads, head_dim 128, bf16)
@@ -583,7 +627,7 @@ def run_ours(args, rank, world, local):
                    "parallelism": f"replicas x{world}"},
         "launch_ms": LAUNCH_STATS.get(call),
         "roofline": roof, "e2e": e2e, "gpu_launches": args.steps, "clocks": clocks, "decode": decode,
-        "decode_forms": decode_forms, "prelude": prelude, "per_config": per_config,
+        "decode_forms": decode_forms, "paged_prefill": paged_prefill, "prelude": prelude, "per_config": per_config,
     }
     if rank == 0 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(args.cpu_seconds)

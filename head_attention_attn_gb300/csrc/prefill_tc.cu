@@ -114,6 +114,10 @@ struct PrefillParams {
     const int32_t* page_table;
     const int32_t* kv_lens;
     int page_size, max_pages, num_pages;
+    // kPaged with a page size TMA can place (8 to 128 rows dividing 128, or a multiple of 128):
+    // K/V copied by TMA a page piece at a time through maps of the pools, key tiles starting on
+    // multiples of 128 positions
+    int paged_tma;
 };
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
@@ -288,6 +292,14 @@ __global__ void __launch_bounds__(threads_for<NT>(), 3 - NT)
             kv0 = -1;
         }
     }
+    // the CTA's visible keys (the union of its tiles' bands); with TMA page copies the key-tile
+    // grid starts on a multiple of 128, so that pages never straddle two tiles
+    const long long vis_lo = kv0;
+    long long vis_hi = 0;
+#pragma unroll
+    for (int t = 0; t < kTiles; ++t)
+        if (thi[t] > tlo[t] && thi[t] > vis_hi) vis_hi = thi[t];
+    if (PAGED && p.paged_tma && kv0 > 0) kv0 = (kv0 / BN) * BN;
     TileRange rng[kTiles];
     int ntiles = 0;
 #pragma unroll
@@ -355,8 +367,9 @@ __global__ void __launch_bounds__(threads_for<NT>(), 3 - NT)
             uint32_t count = 1;
             if (i >= kBarPFull && i < kBarPFull + kTiles)
                 count = 8;  // one arrival per softmax warp of the tile
-            if (PAGED && ((i >= kBarKFull && i < kBarKFull + kStages) || (i >= kBarVFull && i < kBarVFull + kStages)))
-                count = 32;  // one arrival per producer lane, after its copies have landed
+            if (PAGED && !p.paged_tma &&
+                ((i >= kBarKFull && i < kBarKFull + kStages) || (i >= kBarVFull && i < kBarVFull + kStages)))
+                count = 32;  // gathered rows: one arrival per producer lane, after its copies have landed
             mbar_init(bar0 + 8 * i, count);
         }
         *abort_flag = 0;
@@ -379,7 +392,7 @@ __global__ void __launch_bounds__(threads_for<NT>(), 3 - NT)
     }
     if (kTiles == 2 && warp == 0 && lane == 0) {
         tma_prefetch_desc(&tmQ);
-        if (!PAGED) {
+        if (!PAGED || p.paged_tma) {
             tma_prefetch_desc(&tmK);
             tma_prefetch_desc(&tmV);
         }
@@ -389,7 +402,98 @@ __global__ void __launch_bounds__(threads_for<NT>(), 3 - NT)
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
 
-    if (PAGED && warp == 0) {
+    if (PAGED && p.paged_tma && warp == 0) {
+        // ------------------------------------------------------------ TMA page producer (paged K/V)
+        // Tile j holds keys [kv0 + 128 j, +128); with kv0 a multiple of 128, no page straddles
+        // two tiles.  Lane 0 posts the tile's bytes, then lane i copies the i-th of the tile's pages
+        // that hold visible keys (one box per 64-column chunk; a page of 128 rows or more gives
+        // its 128-row piece).  V rows outside the CTA's visible keys [vis_lo, vis_hi) -- before
+        // the band in the first tile, past it in the last, never copied or copied from cache rows
+        // no query here sees -- would meet P = 0 on the tensor core, where 0 * NaN is NaN: such
+        // a tile lands on its own barrier, the warp zeroes those rows, and only then releases it.
+        const int ps = p.page_size;
+        const int32_t* pages = p.page_table + (size_t)b * p.max_pages;
+        const uint64_t keep = l2_policy_evict_last();
+        if (lane == 0 && ntiles > 0) load_q();
+        int issued = 0;      // K and V tiles issued
+        int land_uses = 0;   // phases of the landing barrier used
+        bool land_failed = false;
+        for (int j = 0; j < ntiles; ++j) {
+            const int s = j % kStages;
+            const uint32_t n = (uint32_t)(j / kStages);
+            const long long s0 = kv0 + (long long)j * BN;
+            const long long clo = max(s0, vis_lo), chi = min(s0 + BN, vis_hi);  // the tile's visible keys
+            const int zlo = (int)(clo - s0), zhi = (int)(chi - s0);             // V rows kept: [zlo, zhi)
+            const bool zero = zlo > 0 || zhi < BN;
+            const long long f = clo / ps, e = (chi - 1) / ps;                   // pages with visible keys
+            const int npages = (int)(e - f + 1);
+            const uint32_t bytes = (uint32_t)(ps < BN ? npages * ps : BN) * (D * 2);
+            bool ok = true;
+            for (int kind = 0; kind < 2; ++kind) {
+                const int empty = kind ? kBarVEmpty : kBarKEmpty;
+                if (j >= kStages &&
+                    !__all_sync(0xffffffffu, mbar_wait(bar0 + 8 * (empty + s), (n - 1) & 1, p.wc, abort_flag))) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t tile = sbase + (kind ? C::kOffV : C::kOffK) + s * C::kKVBytes;
+                const bool land = kind && zero;
+                const uint32_t done = land ? bar0 + 8 * kBarVLand : bar0 + 8 * ((kind ? kBarVFull : kBarKFull) + s);
+                const CUtensorMap* map = kind ? &tmV : &tmK;
+                if (lane == 0) mbar_arrive_expect_tx(done, bytes);
+                __syncwarp();
+                if (ps < BN) {
+                    for (int x = lane; x < npages; x += 32) {
+                        const long long pgi = f + x;
+                        const int pg = __ldg(pages + pgi);
+                        const uint32_t r = (uint32_t)(pgi * ps - s0);  // a multiple of the page size
+#pragma unroll
+                        for (int c = 0; c < C::kChunks; ++c)
+                            tma_load_3d_hint(tile + c * (BN * 128) + r * 128, map, done, c * 64, 0, pg * p.Hkv + hk, keep);
+                    }
+                } else if (lane == 0) {
+                    const int pg = __ldg(pages + s0 / ps);
+#pragma unroll
+                    for (int c = 0; c < C::kChunks; ++c)
+                        tma_load_3d_hint(tile + c * (BN * 128), map, done, c * 64, (int)(s0 % ps), pg * p.Hkv + hk, keep);
+                }
+                ++issued;
+                if (land) {
+                    const uint32_t par = (uint32_t)land_uses & 1;
+                    ++land_uses;
+                    if (!__all_sync(0xffffffffu, mbar_wait(bar0 + 8 * kBarVLand, par, p.wc, abort_flag))) {
+                        if (lane == 0) drain_wait(bar0 + 8 * kBarVLand, par, p.wc);  // the copies may still be in flight
+                        land_failed = true;
+                        ok = false;
+                        break;
+                    }
+                    uint8_t* vt = smem + C::kOffV + s * C::kKVBytes;
+                    constexpr int kUnits = C::kChunks * 8;  // 16-byte units of a row
+                    const int nz = zlo + (BN - zhi);        // rows to zero: [0, zlo) and [zhi, BN)
+                    for (int u = lane; u < nz * kUnits; u += 32) {
+                        const int i = u / kUnits;
+                        const int r = i < zlo ? i : zhi + (i - zlo);
+                        const int c = (u / 8) % C::kChunks, q = u & 7;
+                        *reinterpret_cast<uint4*>(vt + c * (BN * 128) + r * 128 + q * 16) = make_uint4(0u, 0u, 0u, 0u);
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar0 + 8 * (kBarVFull + s));
+                }
+            }
+            if (!ok) break;
+        }
+        // nothing of this CTA's stays in flight when it leaves, whatever happened above
+        if (lane == 0 && ntiles > 0) {
+            drain_wait(bar0 + 8 * kBarQFull, 0, p.wc);
+            // a V tile whose landing wait gave up was drained above and never released
+            const int nk = (issued + 1) / 2, nv = issued / 2 - (land_failed ? 1 : 0);
+            for (int j = (nk > kStages ? nk - kStages : 0); j < nk; ++j)
+                drain_wait(bar0 + 8 * (kBarKFull + j % kStages), (uint32_t)(j / kStages) & 1, p.wc);
+            for (int j = (nv > kStages ? nv - kStages : 0); j < nv; ++j)
+                drain_wait(bar0 + 8 * (kBarVFull + j % kStages), (uint32_t)(j / kStages) & 1, p.wc);
+        }
+    } else if (PAGED && warp == 0) {
         // ------------------------------------------------------------ gather producer (paged K/V)
         // Q comes by TMA.  For every key tile the lanes write the byte offset of each of its
         // 128 rows in the pools (or ~0 past the visible keys) to shared memory, then copy whole
@@ -835,14 +939,14 @@ EncodeTiledFn get_encode_fn() {
     return fn;
 }
 
-// [rows_outer, L, D] 16-bit tensor (bf16 or fp16) viewed as 3-D (D, L, rows_outer); box 64 x 128 x 1,
-// 128-byte swizzle, out-of-range rows read as zeros.
-bool encode_16bit_3d(CUtensorMap* map, const void* base, int D, int L, int outer, bool f16) {
+// [rows_outer, L, D] 16-bit tensor (bf16 or fp16) viewed as 3-D (D, L, rows_outer); box 64 x rows x 1
+// (128 unless given), 128-byte swizzle, out-of-range rows read as zeros.
+bool encode_16bit_3d(CUtensorMap* map, const void* base, int D, int L, long long outer, bool f16, int rows = 128) {
     EncodeTiledFn fn = get_encode_fn();
     if (!fn) return false;
     cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)L, (cuuint64_t)outer};
     cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)L * D * 2};
-    cuuint32_t box[3] = {64, 128, 1};
+    cuuint32_t box[3] = {64, (cuuint32_t)rows, 1};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = fn(map, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -871,11 +975,22 @@ cudaError_t launch_impl(const Problem& pr, const WaitCtl& wc, cudaStream_t strea
     using C = Cfg<D, NT>;
     constexpr int kTiles = NT;
     CUtensorMap tq, tk, tv, to;
+    // paged K/V by TMA: page sizes of 8 to 128 rows that divide a 128-key tile, or multiples of 128
+    // rows, through the pools seen as [num_pages * Hkv, page_size, D]; other page sizes are gathered
+    const int ps = pr.page_size;
+    const bool paged_tma = LAYOUT == kPaged && ((ps >= 8 && ps <= BN && BN % ps == 0) || (ps > 0 && ps % BN == 0)) &&
+                           (long long)pr.num_pages * pr.Hkv <= 0x7fffffffLL;
     if (LAYOUT == kPaged) {
-        // only Q is copied by TMA; the K and V rows are gathered through the page table
         if (!encode_16bit_3d_tok(&tq, pr.q, D, pr.Hq, pr.total, F16)) return cudaErrorInvalidValue;
-        tk = tq;
-        tv = tq;
+        if (paged_tma) {
+            const long long outer = (long long)pr.num_pages * pr.Hkv;
+            if (!encode_16bit_3d(&tk, pr.k, D, ps, outer, F16, ps < BN ? ps : BN) ||
+                !encode_16bit_3d(&tv, pr.v, D, ps, outer, F16, ps < BN ? ps : BN))
+                return cudaErrorInvalidValue;
+        } else {
+            tk = tq;  // the K and V rows are gathered through the page table
+            tv = tq;
+        }
     } else if (LAYOUT == kPacked) {
         if (!encode_16bit_3d_tok(&tq, pr.q, D, pr.Hq, pr.total, F16) ||
             !encode_16bit_3d_tok(&tk, pr.k, D, pr.Hkv, pr.total, F16) ||
@@ -934,6 +1049,7 @@ cudaError_t launch_impl(const Problem& pr, const WaitCtl& wc, cudaStream_t strea
         p.page_size = pr.page_size;
         p.max_pages = pr.max_pages;
         p.num_pages = pr.num_pages;
+        p.paged_tma = paged_tma ? 1 : 0;
     }
     const long long grid = (long long)p.num_m * pr.B * (PAIR ? pr.Hq / 2 : pr.Hq);
     if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;

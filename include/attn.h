@@ -334,8 +334,10 @@ ATTN_API attn_status attn_qkv_prelude_caches(const void* qkv, const float* q_nor
  *     are written as zeros.
  *
  * The result equals attn_fwd per sequence over the gathered cache (q_len len_b, pos_offset
- * kv_lens[b] - len_b, key_lens kv_lens[b]); at head_dim 128, where both run the same prefill
- * kernel on the same tiles, bit for bit.
+ * kv_lens[b] - len_b, key_lens kv_lens[b]).  At head_dim 128 both run the same prefill kernel;
+ * where they also split the keys into the same 128-key tiles (a causal mask, or a page size
+ * that is gathered row by row: not 8..128 dividing 128, nor a multiple of 128) they agree bit
+ * for bit, otherwise to rounding.
  * The library allocates nothing and keeps no pointer after the call.
  */
 ATTN_API attn_status attn_fwd_varlen_paged(const void* q, const void* k_pool, const void* v_pool,

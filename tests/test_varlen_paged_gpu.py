@@ -4,8 +4,11 @@ Sequence b has len_b packed queries, the newest of its kv_lens[b] cached positio
 prefill, multi-token verification); its cache lives in pages of two pools addressed by
 page_table[b].  Gathering the pages back into one [Hkv, capacity, D] cache and calling attn_fwd
 per sequence (q_len len_b, pos_offset kv_lens[b] - len_b, key_lens kv_lens[b]) runs the same
-prefill kernel on the same shared-memory tiles at head_dim 128, so the two agree bit for bit; both
-are checked against the fp64 oracle.  Pool rows outside every sequence's cached positions hold NaN, which
+prefill kernel at head_dim 128; where both split the keys into the same 128-key tiles (a causal
+mask, whose band starts at key 0, or page sizes gathered row by row) they agree bit for bit.
+Page sizes that TMA copies a page at a time start the tiles on multiples of 128, so with a
+window the split can differ and the results agree to rounding.  Both are checked against the
+fp64 oracle.  Pool rows outside every sequence's cached positions hold NaN, which
 must never reach the output.
 """
 import numpy as np
@@ -94,7 +97,8 @@ def test_paged_chunks_equal_gathered_prefill(D, Hq, Hkv, page_size, mode, window
         P = klen - n
         ref = oracle.attention(qb, kb, vb, pos_offset=P, mask_mode=mode, window=window, key_lens=[klen], scale=sc)
         assert_close(got[s0:s0 + n], ref[0].transpose(1, 0, 2), "bf16", f"seq {b} (len {n}, kv {klen})")
-        if n > 1 and D == 128:  # the same prefill kernel through attn_fwd over the gathered cache: bit for bit
+        same_tiles = mode == MASK_CAUSAL or page_size in (7, 1)
+        if n > 1 and D == 128 and same_tiles:  # the same prefill kernel and key tiles through attn_fwd: bit for bit
             # (at head_dim 64 attn_fwd runs the 64-key-block kernel, a different summation order)
             fwd = attn.attn_fwd(qb.to(DEV), kb.to(DEV), vb.to(DEV), key_lens=torch.tensor([klen], dtype=torch.int32,
                                 device=DEV), pos_offset=P, mask_mode=mode, window=window, scale=sc)
