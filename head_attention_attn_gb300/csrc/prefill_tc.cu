@@ -84,7 +84,8 @@ enum : int {
     kBarOFull = kBarPFull + kTiles,    // + tile: the tile's last P V product completed
     kBarMmaDone = kBarOFull + kTiles,
     kBarVLand = kBarMmaDone + 1,       // the tail V tile's copy, before its invisible rows are zeroed
-    kNumBars = kBarVLand + 1,
+    kBarPHalf = kBarVLand + 1,         // + tile: the first 32 keys of both halves of P are in TMEM
+    kNumBars = kBarPHalf + kTiles,
 };
 static_assert(kNumBars * 8 <= 240, "barrier area");
 
@@ -365,7 +366,7 @@ __global__ void __launch_bounds__(threads_for<NT>(), 3 - NT)
     if (threadIdx.x == 0) {
         for (int i = 0; i < kNumBars; ++i) {
             uint32_t count = 1;
-            if (i >= kBarPFull && i < kBarPFull + kTiles)
+            if ((i >= kBarPFull && i < kBarPFull + kTiles) || (i >= kBarPHalf && i < kBarPHalf + kTiles))
                 count = 8;  // one arrival per softmax warp of the tile
             if (PAGED && !p.paged_tma &&
                 ((i >= kBarKFull && i < kBarKFull + kStages) || (i >= kBarVFull && i < kBarVFull + kStages)))
@@ -630,7 +631,9 @@ __global__ void __launch_bounds__(threads_for<NT>(), 3 - NT)
                     const int jp = j - 1;
                     if (jp >= 0 && jp >= rng[t].jb && jp < rng[t].je) {
                         const int s = jp % kStages;
-                        if (!mbar_wait(bar0 + 8 * (kBarPFull + t), (uint32_t)it[t] & 1, p.wc, abort_flag)) { ok = false; break; }
+                        // P_t arrives in two parts: keys [0, 32) and [64, 96) first, then the rest;
+                        // the product over the first part runs while the softmax packs the second
+                        if (!mbar_wait(bar0 + 8 * (kBarPHalf + t), (uint32_t)it[t] & 1, p.wc, abort_flag)) { ok = false; break; }
                         if (!v_waited) {
                             if (!mbar_wait(bar0 + 8 * (kBarVFull + s), (uint32_t)(jp / kStages) & 1, p.wc, abort_flag)) { ok = false; break; }
                             v_waited = true;
@@ -641,9 +644,20 @@ __global__ void __launch_bounds__(threads_for<NT>(), 3 - NT)
                         const uint32_t tP = tmem + C::kColS + 128 * t;
                         const uint32_t tO = tmem + C::kColO + 128 * t;
 #pragma unroll
-                        for (int kk = 0; kk < BN / 16; ++kk)
-                            tc_mma_ts(tO, tP + kk * 8, vd + (uint64_t)((kk * 16 * 128) >> 4), kIdescPV,
-                                      (jp > rng[t].jb || kk > 0) ? 1u : 0u);
+                        for (int part = 0; part < 2; ++part) {
+                            if (part == 1) {
+                                if (!mbar_wait(bar0 + 8 * (kBarPFull + t), (uint32_t)it[t] & 1, p.wc, abort_flag)) { ok = false; break; }
+                                tc_fence_after();
+                            }
+#pragma unroll
+                            for (int u = 0; u < 4; ++u) {
+                                // 16-key steps kk: part 0 takes 0, 1, 4, 5 and part 1 takes 2, 3, 6, 7
+                                const int kk = (u >> 1) * 4 + part * 2 + (u & 1);
+                                tc_mma_ts(tO, tP + kk * 8, vd + (uint64_t)((kk * 16 * 128) >> 4), kIdescPV,
+                                          (jp > rng[t].jb || kk > 0) ? 1u : 0u);
+                            }
+                        }
+                        if (!ok) break;
                         it[t] += 1;
                         used_v = true;
                         if (jp == rng[t].je - 1) tc_commit(bar0 + 8 * (kBarOFull + t));
@@ -764,6 +778,16 @@ __global__ void __launch_bounds__(threads_for<NT>(), 3 - NT)
             const float neg_m = (m_run == -INFINITY) ? 0.f : -m_run;
             const float2 sl2 = make_float2(sl, sl), negm2 = make_float2(neg_m, neg_m);
 
+            // The product over this block's P starts once every warp of the tile has released the
+            // first 32 of its keys; a warp that must rescale O first (rare) releases them only
+            // after the rescale below, with the rest.
+            const bool warp_rescale = __any_sync(0xffffffffu, rescale);
+            auto release_first_part = [&]() {
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar0 + 8 * (kBarPHalf + t));
+            };
             // P for my 64 keys -> TMEM columns [32h, 32h + 32) of S_t, as bf16 or fp16 pairs; the row
             // sum adds the rounded values the tensor core will multiply into V.
             float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
@@ -772,6 +796,7 @@ __global__ void __launch_bounds__(threads_for<NT>(), 3 - NT)
 #pragma unroll
                 for (int q = 0; q < 16; ++q) z[q] = 0u;
                 tmem_st16_async(tS + 32 * h, z);
+                if (!warp_rescale) release_first_part();
                 tmem_st16_async(tS + 32 * h + 16, z);
             } else {
 #pragma unroll
@@ -796,13 +821,15 @@ __global__ void __launch_bounds__(threads_for<NT>(), 3 - NT)
                     if ((c2 / 2) & 1) acc1 = __fadd2_rn(acc1, r2); else acc0 = __fadd2_rn(acc0, r2);
                 }
                 tmem_st16_async(tS + 32 * h + 16 * k, pk);
+                if (k == 0 && !warp_rescale) release_first_part();
             }
             }
             tmem_st_wait();
             acc0 = __fadd2_rn(acc0, acc1);
             l_run = l_run * alpha + (acc0.x + acc0.y);
-            // O_t is stable here: the commit behind S_t(j) covers the earlier P V product.
-            if (__any_sync(0xffffffffu, rescale)) {
+            // O_t is stable here: the commit behind S_t(j) covers the earlier P V product, and
+            // this block's has not started (this warp has released nothing yet).
+            if (warp_rescale) {
 #pragma unroll
                 for (int c = 0; c < D / 64; ++c) {
                     float o[32];
@@ -811,6 +838,7 @@ __global__ void __launch_bounds__(threads_for<NT>(), 3 - NT)
                     for (int q = 0; q < 32; ++q) o[q] *= alpha;
                     tmem_st32(tO + (D / 2) * h + 32 * c, o);
                 }
+                release_first_part();
             }
             tc_fence_before();
             __syncwarp();
