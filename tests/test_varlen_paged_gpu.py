@@ -78,7 +78,8 @@ CASES = [
 
 
 @pytest.mark.parametrize("D,Hq,Hkv", [(64, 4, 2), (128, 4, 2), (128, 3, 1), (128, 8, 1)])
-@pytest.mark.parametrize("page_size", [16, 7, 1, 256])
+# TMA page pieces: 8 (the smallest), 16, 128 (one key tile), 384 (three tiles a page); gathered: 7, 1, 24
+@pytest.mark.parametrize("page_size", [8, 16, 128, 384, 7, 1, 24])
 @pytest.mark.parametrize("mode,window", [(MASK_CAUSAL, 0), (MASK_CAUSAL_WINDOW, 150)])
 def test_paged_chunks_equal_gathered_prefill(D, Hq, Hkv, page_size, mode, window):
     q_lens, kv_lens = CASES[0]
@@ -97,7 +98,7 @@ def test_paged_chunks_equal_gathered_prefill(D, Hq, Hkv, page_size, mode, window
         P = klen - n
         ref = oracle.attention(qb, kb, vb, pos_offset=P, mask_mode=mode, window=window, key_lens=[klen], scale=sc)
         assert_close(got[s0:s0 + n], ref[0].transpose(1, 0, 2), "bf16", f"seq {b} (len {n}, kv {klen})")
-        same_tiles = mode == MASK_CAUSAL or page_size in (7, 1)
+        same_tiles = mode == MASK_CAUSAL or page_size in (7, 1, 24)
         if n > 1 and D == 128 and same_tiles:  # the same prefill kernel and key tiles through attn_fwd: bit for bit
             # (at head_dim 64 attn_fwd runs the 64-key-block kernel, a different summation order)
             fwd = attn.attn_fwd(qb.to(DEV), kb.to(DEV), vb.to(DEV), key_lens=torch.tensor([klen], dtype=torch.int32,
@@ -107,11 +108,12 @@ def test_paged_chunks_equal_gathered_prefill(D, Hq, Hkv, page_size, mode, window
     assert attn.sync_status() == attn.ATTN_OK, attn.last_error()
 
 
+@pytest.mark.parametrize("D,page_size", [(128, 32), (64, 64), (128, 13)])
 @pytest.mark.parametrize("mode,window", [(MASK_NONE, 0), (MASK_WINDOW, 64)])
-def test_paged_chunks_other_masks_against_oracle(mode, window):
+def test_paged_chunks_other_masks_against_oracle(mode, window, D, page_size):
     q_lens, kv_lens = [50, 200, 7], [90, 200, 400]
-    D, Hq, Hkv = 128, 4, 2
-    q, kp, vp, table, cu, kl, ck, cv = paged_chunks(q_lens, kv_lens, Hq, Hkv, D, 32, seed=11 + mode)
+    Hq, Hkv = 4, 2
+    q, kp, vp, table, cu, kl, ck, cv = paged_chunks(q_lens, kv_lens, Hq, Hkv, D, page_size, seed=11 + mode + D)
     sc = scale_of(D)
     got = to_numpy_f64(run_paged(q, kp, vp, table, cu, kl, mode, window, sc))
     assert attn.sync_status() == attn.ATTN_OK, attn.last_error()
