@@ -43,6 +43,7 @@ DECODE = "decode_bf16_64x32q8kv_8192x128"
 EXTRA_PREFILL = ["causal_mha_f32_1x4x64x32", "bidir_keypad_bf16_8x12x512x64", "window128_bf16_4x12x8192x64"]
 KEYPAD = "bidir_keypad_bf16_8x12x512x64"
 PRELUDE = "qkv_prelude_bf16_16384x32q8kv_128_normrope"
+PAGED_PREFILL = "paged_prefill_bf16_4x32q8kv_512of4096x128_page16"
 L2_BYTES = 129 * 1024 * 1024
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
@@ -50,15 +51,17 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # kernel's code state (its hash); the entry stops applying as soon as the kernel's code changes.
 NCU_TRAFFIC = {
     # prefill_tc_kernel<128, 2, bf16, paired heads, positive scale>, causal GQA, with L2 hints
-    # (Q and O evict-first, K/V evict-last): 316.69 MB read + 95.92 MB written
-    ("prefill", "4c37abd2b905"): 412608256.0,
-    # decode_tc_kernel<G4, bf16>: 537.09 MB read + 3.42 MB written at batch 16, scaled by the units
+    # (Q and O evict-first, K/V evict-last) and P released in two parts: 303.61 MB read + 86.48 MB written
+    ("prefill", "6ee0df80697f"): 390087168.0,
+    # the same kernel, paged layout, chunked prefill with 16-row pages: 118.66 MB read + 11.20 MB written
+    ("prefill", "6ee0df80697f", "paged16"): 129861888.0,
+    # decode_tc_kernel<G4, bf16>: 537.11 MB read + 3.26 MB written at batch 16, scaled by the units
     # (items) to the bench's batch 64
-    ("decode_tc", "1236c0ea2fcc"): 4 * 540508160.0,
-    # prefill_narrow_kernel<bf16, head-major, positive scale>, per workload: window 151.06 MB read +
-    # 27.99 MB written; key padding 15.77 MB read, 0 written (the output stays in L2)
-    ("prefill_narrow", "ce907a89b770", "window128_bf16_4x12x8192x64"): 179046144.0,
-    ("prefill_narrow", "ce907a89b770", "bidir_keypad_bf16_8x12x512x64"): 15774976.0,
+    ("decode_tc", "b900f0549270"): 4 * 540366336.0,
+    # prefill_narrow_kernel<bf16, head-major, positive scale>, per workload: window 151.07 MB read +
+    # 28.00 MB written; key padding 15.78 MB read, 0 written (the output stays in L2)
+    ("prefill_narrow", "3a6262fe1152", "window128_bf16_4x12x8192x64"): 179073280.0,
+    ("prefill_narrow", "3a6262fe1152", "bidir_keypad_bf16_8x12x512x64"): 15775232.0,
 }
 
 
@@ -326,31 +329,40 @@ def decode_forms_leg(args, world, dev, peaks, peak_src, dec_bytes):
     return legs
 
 
+# chunked prefill over paged caches: 4 sequences whose newest 512 positions (the queries) follow
+# 3,584 older ones (4,096 cached positions each), 32 query / 8 kv heads, head_dim 128, bf16, causal
+PAGED_SHAPE = dict(B=4, Hq=32, Hkv=8, D=128, chunk=512, kv=4096)
+
+
+def paged_prefill_inputs(ps, dev, g):
+    """Queries, output, cu_seqlens, kv_lens and shuffled pools with pages of ps rows."""
+    B, Hq, Hkv, D, chunk, kv = (PAGED_SHAPE[k] for k in ("B", "Hq", "Hkv", "D", "chunk", "kv"))
+    q = torch.empty(B * chunk, Hq, D, dtype=torch.bfloat16, device=dev).normal_()
+    cu = torch.arange(0, (B + 1) * chunk, chunk, dtype=torch.int32, device=dev)
+    kv_lens = torch.full((B,), kv, dtype=torch.int32, device=dev)
+    max_pages = kv // ps
+    num_pages = B * max_pages
+    k_pool = torch.empty(num_pages, Hkv, ps, D, dtype=torch.bfloat16, device=dev).normal_()
+    v_pool = torch.empty_like(k_pool).normal_()
+    table = torch.randperm(num_pages, generator=g).to(torch.int32).view(B, max_pages).to(dev)
+    return q, torch.empty_like(q), cu, kv_lens, k_pool, v_pool, table
+
+
 def paged_prefill_leg(args, world, dev, peaks, peak_src):
-    """TFLOP/s of attn_fwd_varlen_paged on a chunked prefill shaped like the causal GQA workload:
-    4 sequences whose newest 512 positions (the queries) follow 3,584 older ones in paged caches
-    (4,096 cached positions each), 32 query / 8 kv heads, head_dim 128, bf16, causal, with pages
-    of 16 and of 128 rows.  Algorithmic FLOPs count the visible (query, key) pairs only."""
+    """TFLOP/s of attn_fwd_varlen_paged on the chunked prefill of PAGED_SHAPE, with pages of 16
+    and of 128 rows.  Algorithmic FLOPs count the visible (query, key) pairs only."""
     import head_attention_attn_gb300 as attn
-    B, Hq, Hkv, D, chunk, kv = 4, 32, 8, 128, 512, 4096
+    B, Hq, Hkv, D, chunk, kv = (PAGED_SHAPE[k] for k in ("B", "Hq", "Hkv", "D", "chunk", "kv"))
     P = kv - chunk
     flops = 4.0 * D * Hq * B * sum(P + i + 1 for i in range(chunk))
     scale = float(torch.tensor(1.0 / math.sqrt(D), dtype=torch.float32))
     steps = max(3, min(args.steps, 200))
     g = torch.Generator().manual_seed(1008)
     legs = []
-    q = torch.empty(B * chunk, Hq, D, dtype=torch.bfloat16, device=dev).normal_()
-    out = torch.empty_like(q)
-    cu = torch.arange(0, (B + 1) * chunk, chunk, dtype=torch.int32, device=dev)
-    kv_lens = torch.full((B,), kv, dtype=torch.int32, device=dev)
     for ps in (16, 128):
-        max_pages = kv // ps
-        num_pages = B * max_pages
-        k_pool = torch.empty(num_pages, Hkv, ps, D, dtype=torch.bfloat16, device=dev).normal_()
-        v_pool = torch.empty_like(k_pool).normal_()
-        table = torch.randperm(num_pages, generator=g).to(torch.int32).view(B, max_pages).to(dev)
+        q, out, cu, kv_lens, k_pool, v_pool, table = paged_prefill_inputs(ps, dev, g)
 
-        def call(k_pool=k_pool, v_pool=v_pool, table=table):
+        def call(q=q, out=out, cu=cu, kv_lens=kv_lens, k_pool=k_pool, v_pool=v_pool, table=table):
             attn.attn_fwd_varlen_paged(q, k_pool, v_pool, table, cu, kv_lens, chunk, out, scale=scale)
         sec = time_device(call, steps, args.warmup, world, dev)
         if attn.sync_status() != attn.ATTN_OK:
@@ -361,10 +373,11 @@ def paged_prefill_leg(args, world, dev, peaks, peak_src):
                      "ms_per_step": round(sec * 1e3, 4), "launch_ms": LAUNCH_STATS.get(call),
                      "roofline": {"bound": "tensor", "achieved": round(tflops, 1), "peak": peaks["bf16_tflops"],
                                   "unit": "TFLOP/s", "frac": round(tflops / peaks["bf16_tflops"], 4),
-                                  "peak_source": f"{peak_src} bf16 dense (burst)", "traffic": None,
+                                  "peak_source": f"{peak_src} bf16 dense (burst)",
+                                  "traffic": NCU_TRAFFIC.get(("prefill", kernel_source_hash("prefill"), f"paged{ps}")),
                                   "kernel": "prefill_tc_kernel<128, 2, bf16, paged> (K/V copied by TMA a page piece at a time)",
                                   "algorithmic_flops_per_launch": flops}})
-        del k_pool, v_pool, table
+        del q, out, k_pool, v_pool, table
         torch.cuda.empty_cache()
     return legs
 
@@ -764,6 +777,14 @@ def run_profile_case(args):
         attn.check_device_status()
         print(json.dumps({"profile": args.profile, "launches": args.warmup + args.steps}))
         return
+    if args.profile == PAGED_PREFILL:
+        q, out, cu, kv_lens, k_pool, v_pool, table = paged_prefill_inputs(16, "cuda:0", torch.Generator().manual_seed(1008))
+        for _ in range(args.warmup + args.steps):
+            attn.attn_fwd_varlen_paged(q, k_pool, v_pool, table, cu, kv_lens, PAGED_SHAPE["chunk"], out)
+        torch.cuda.synchronize()
+        attn.check_device_status()
+        print(json.dumps({"profile": args.profile, "launches": args.warmup + args.steps}))
+        return
     c = WORKLOADS[args.profile] if args.batch is None else case(args.profile, B=args.batch)
     q, k, v, kl = make_inputs(c, device="cuda:0")
     out = torch.empty_like(q)
@@ -783,7 +804,7 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-rows", type=int, default=64)
-    ap.add_argument("--profile", choices=sorted(WORKLOADS) + [PRELUDE], default=None,
+    ap.add_argument("--profile", choices=sorted(WORKLOADS) + [PRELUDE, PAGED_PREFILL], default=None,
                     help="only run --warmup + --steps launches of one workload (for profilers)")
     ap.add_argument("--batch", type=int, default=None, help="batch size override for --profile")
     args = ap.parse_args(argv)
