@@ -9,8 +9,10 @@
 //                                   where the measured routing table prefers it
 //   bf16/fp16, q_len == 1, group 1/2/4/8 -> K2 (split-KV decode, the other shapes)
 //   bf16/fp16 otherwise          -> K1 (tcgen05 + TMA fused prefill); packed queries over
-//                                   paged caches also go to K1, whose producer then gathers
-//                                   the K/V rows through the page table
+//                                   paged caches also go to K1, whose producer copies K/V
+//                                   by TMA a page piece at a time (page sizes of 8..128 rows
+//                                   dividing 128, or multiples of 128) or else gathers the
+//                                   rows through the page table
 // There is no host fallback: an unsupported shape is refused (ferrum-kernels:
 // CUDA ops fail rather than copy data through host memory).
 #include <math.h>

@@ -7,7 +7,8 @@
 // rows (both visit exactly the same key tiles, so neither idles at the end); otherwise they
 // are two consecutive row blocks of one (batch, query head).
 //   warp 0       TMA producer: the Q tiles once, then 128-key K and V tiles
-//                through 2-stage shared-memory rings (128-byte swizzle).
+//                through 2-stage shared-memory rings (128-byte swizzle); over paged
+//                caches one copy per page piece, or a row gather for other page sizes.
 //   warp 1       TMEM owner and single-thread MMA issuer.
 //   warps 2..    softmax, 8 warps per query tile: a row of S is split between two
 //                threads, one per half of the 128 key columns.  Each thread reads its 64
@@ -25,7 +26,9 @@
 // columns of S_t.  With two tiles the MMA order is the ping-pong
 //   PV0(j-1), QK0(j), PV1(j-1), QK1(j)
 // so the tensor core works on one tile while the other tile's softmax runs; with one
-// tile per CTA the two CTAs resident on an SM take turns in the same way.
+// tile per CTA the two CTAs resident on an SM take turns in the same way.  Each tile's P
+// is released in two parts, so the first half of PV_t(j) runs while the softmax packs
+// the rest.
 //   QK_t(j):  S_t  = Q_t K_j^T   (A, B from shared memory, K-major)
 //   PV_t(j):  O_t += P_t V_j     (A = P from TMEM, B = V from shared memory, MN-major)
 // A commit after QK_t(j) completes only after every earlier MMA, PV_t(j-1)
@@ -93,7 +96,8 @@ static_assert(kNumBars * 8 <= 240, "barrier area");
 enum : int {
     kHeadMajor = 0,  // q/out [B, Hq, Lq, D], k/v [B, Hkv, Lk, D]: TMA
     kPacked = 1,     // packed sequences, token-major q/out [total, Hq, D] and k/v [total, Hkv, D]: TMA
-    kPaged = 2,      // packed token-major q/out, K/V in paged pools: Q by TMA, K/V rows gathered
+    kPaged = 2,      // packed token-major q/out, K/V in paged pools: Q by TMA, K/V by TMA per page
+                     // piece where the page size allows it, else rows gathered
 };
 
 struct PrefillParams {
