@@ -187,3 +187,38 @@ def test_bad_cu_seqlens_is_reported_and_not_written():
     assert attn.sync_status() == attn.ATTN_OK
     assert torch.all(out[30:] == 5.0)                     # sequence 1 is not written
     assert torch.isfinite(out[:30].float()).all() and not torch.all(out[:30] == 5.0)
+
+
+def test_paged_chunked_prefill_full_size():
+    """The timed chunked prefill at its full size: 4 sequences, their newest 512 of 4,096 cached
+    positions, 32 query / 8 kv heads, head_dim 128, bf16, causal, 16-row pages in shuffled pool
+    order (the TMA page producer).  Every output element is checked against the fp64 oracle, per
+    (sequence, head) slab too, and the output equals attn_fwd over the gathered caches bit for
+    bit (a causal band starts at key 0, so both split the keys into the same tiles)."""
+    from parity_util import assert_close_per_head
+    B, Hq, Hkv, D, chunk, kv, ps = 4, 32, 8, 128, 512, 4096, 16
+    g = torch.Generator().manual_seed(41)
+    caches_k = torch.randn(B, Hkv, kv, D, generator=g).to(torch.bfloat16)
+    caches_v = torch.randn(B, Hkv, kv, D, generator=g).to(torch.bfloat16)
+    q = torch.randn(B * chunk, Hq, D, generator=g).to(torch.bfloat16)
+    max_pages = kv // ps
+    table = torch.randperm(B * max_pages, generator=g).view(B, max_pages).to(torch.int32)
+
+    def pool(c):  # pool page table[b, j] holds positions [j ps, (j + 1) ps) of sequence b
+        p = torch.empty(B * max_pages, Hkv, ps, D, dtype=torch.bfloat16)
+        p[table.flatten().long()] = c.view(B, Hkv, max_pages, ps, D).permute(0, 2, 1, 3, 4).reshape(-1, Hkv, ps, D)
+        return p
+    cu = torch.arange(0, (B + 1) * chunk, chunk, dtype=torch.int32)
+    kl = torch.full((B,), kv, dtype=torch.int32)
+    sc = scale_of(D)
+    out = run_paged(q, pool(caches_k), pool(caches_v), table, cu, kl, MASK_CAUSAL, 0, sc)
+    assert attn.sync_status() == attn.ATTN_OK, attn.last_error()
+    qh = q.view(B, chunk, Hq, D).permute(0, 2, 1, 3).contiguous()
+    fwd = attn.attn_fwd(qh.to(DEV), caches_k.to(DEV), caches_v.to(DEV), pos_offset=kv - chunk, mask_mode=MASK_CAUSAL,
+                        scale=sc)
+    torch.cuda.synchronize()
+    assert attn.sync_status() == attn.ATTN_OK, attn.last_error()
+    got = out.view(B, chunk, Hq, D).permute(0, 2, 1, 3)
+    assert torch.equal(got.cpu(), fwd.cpu())
+    ref = oracle.attention(qh, caches_k, caches_v, pos_offset=kv - chunk, mask_mode=MASK_CAUSAL, scale=sc)
+    assert_close_per_head(to_numpy_f64(got), ref, "bf16", "paged chunked prefill, full size")
