@@ -176,3 +176,51 @@ def test_tensor_core_paged_decode_splits(G, page_size):
     ref = reference(q, kc, vc, kl, 0, scale)
     assert_close(paged.double().cpu().numpy(), ref, "bf16", f"paged splits G={G} ps={page_size}")
     assert_close(cont.double().cpu().numpy(), ref, "bf16", f"gathered splits G={G} ps={page_size}")
+
+
+@pytest.mark.parametrize("G", [4, 8])
+def test_decode_forms_full_size(G):
+    """The decode legs the bench times, at their full size: 64 items of 8,192 cached positions,
+    8 kv heads, head_dim 128, bf16, 4 or 8 query heads per kv head.  The same caches go in
+    contiguous (attn_fwd), per item (attn_decode_caches) and in 16- and 128-row pages in shuffled
+    pool order (attn_decode_paged).  Forms that run the same kernel as the contiguous decode
+    agree with it bit for bit; every form is checked against the oracle on sampled (item, head)
+    rows (the contiguous decode is compared on every row by its own full-size test)."""
+    m, Hkv, cap, D = 64, 8, 8192, 128
+    Hq = G * Hkv
+    gen = torch.Generator(device=DEV).manual_seed(50 + G)
+    k = torch.randn(m, Hkv, cap, D, generator=gen, device=DEV, dtype=torch.bfloat16)
+    v = torch.randn(m, Hkv, cap, D, generator=gen, device=DEV, dtype=torch.bfloat16)
+    q = torch.randn(m, Hq, D, generator=gen, device=DEV, dtype=torch.bfloat16)
+    kl = torch.full((m,), cap, dtype=torch.int32, device=DEV)
+    scale = float(torch.tensor(1.0 / D ** 0.5, dtype=torch.float32))
+    cont = attn.attn_fwd(q.view(m, Hq, 1, D), k, v, pos_offset=cap - 1, mask_mode=MASK_CAUSAL, scale=scale)[:, :, 0]
+    per_item = attn.attn_decode_caches(q, list(k), list(v), kl, scale=scale)
+    torch.cuda.synchronize()
+    assert attn.sync_status() == attn.ATTN_OK, attn.last_error()
+    assert torch.equal(per_item, cont)  # the tensor-core decode for both, the same tiles
+    forms = {"contiguous": cont, "per-item caches": per_item}
+    g = torch.Generator().manual_seed(60 + G)
+    for ps in (16, 128):
+        pages = cap // ps
+        table = torch.randperm(m * pages, generator=g).view(m, pages).to(torch.int32).to(DEV)
+
+        def pool(c):
+            p = torch.empty(m * pages, Hkv, ps, D, dtype=torch.bfloat16, device=DEV)
+            p[table.flatten().long()] = c.view(m, Hkv, pages, ps, D).permute(0, 2, 1, 3, 4).reshape(-1, Hkv, ps, D)
+            return p
+        paged = attn.attn_decode_paged(q, pool(k), pool(v), table, kl, scale=scale)
+        torch.cuda.synchronize()
+        assert attn.sync_status() == attn.ATTN_OK, attn.last_error()
+        if paged_on_tensor_cores(G, ps):
+            assert torch.equal(paged, cont), f"page {ps}"
+        forms[f"paged {ps}"] = paged
+    rng = np.random.default_rng(70 + G)
+    picks = sorted({(0, 0), (0, Hq - 1), (m - 1, 0), (m - 1, Hq - 1)} |
+                   {(int(rng.integers(m)), int(rng.integers(Hq))) for _ in range(40)})
+    ref = np.stack([oracle.attention(q[b, h].cpu()[None, None, None], k[b:b + 1, h // G:h // G + 1].cpu(),
+                                     v[b:b + 1, h // G:h // G + 1].cpu(), pos_offset=cap - 1, mask_mode=MASK_CAUSAL,
+                                     scale=scale)[0, 0, 0] for b, h in picks])
+    for name, out in forms.items():
+        got = np.stack([out[b, h].double().cpu().numpy() for b, h in picks])
+        assert_close(got, ref, "bf16", f"{name}, G={G}, {len(picks)} sampled rows")
