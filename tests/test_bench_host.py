@@ -108,3 +108,19 @@ def test_kernel_hash_follows_code_not_comments(tmp_path, monkeypatch):
     assert h2 != h1
     monkeypatch.setattr(_build, "NVCC_FLAGS", _build.NVCC_FLAGS + ["-DSOMETHING"])
     assert bench.kernel_source_hash() != h2
+
+
+def test_paged_prefill_inputs_place_every_cached_position_once():
+    """The timed chunked prefill's pools: every (sequence, page) entry names a distinct pool
+    page, so every cached position of every sequence lives in exactly one pool row."""
+    g = torch.Generator().manual_seed(3)
+    for ps in (16, 128):
+        q, out, cu, kv_lens, k_pool, v_pool, table = bench.paged_prefill_inputs(ps, "cpu", g)
+        S = bench.PAGED_SHAPE
+        B, chunk, kv = S["B"], S["chunk"], S["kv"]
+        assert tuple(q.shape) == (B * chunk, S["Hq"], S["D"]) and out.shape == q.shape
+        assert cu.tolist() == [chunk * b for b in range(B + 1)]
+        assert kv_lens.tolist() == [kv] * B
+        assert tuple(k_pool.shape) == (B * kv // ps, S["Hkv"], ps, S["D"]) and v_pool.shape == k_pool.shape
+        assert tuple(table.shape) == (B, kv // ps)
+        assert sorted(table.flatten().tolist()) == list(range(B * kv // ps))
