@@ -222,3 +222,29 @@ def test_paged_chunked_prefill_full_size():
     assert torch.equal(got.cpu(), fwd.cpu())
     ref = oracle.attention(qh, caches_k, caches_v, pos_offset=kv - chunk, mask_mode=MASK_CAUSAL, scale=sc)
     assert_close_per_head(to_numpy_f64(got), ref, "bf16", "paged chunked prefill, full size")
+
+
+@pytest.mark.parametrize("page_size", [16, 32, 7])
+def test_paged_chunks_many_ragged_sequences(page_size):
+    """Forty sequences with random chunk lengths (0 to 200 queries, some a whole prefill) and
+    0 to 600 older cached positions, 8 query / 2 kv heads, head_dim 128, causal with and without
+    a window: every sequence against the oracle."""
+    rng = np.random.default_rng(100 + page_size)
+    n = 40
+    q_lens = [int(x) for x in rng.integers(0, 201, n)]
+    q_lens[0], q_lens[1] = 0, 1
+    kv_lens = [ql + int(x) for ql, x in zip(q_lens, rng.integers(0, 601, n))]
+    kv_lens[2] = q_lens[2]  # a whole prefill: no older positions
+    for mode, window in ((MASK_CAUSAL, 0), (MASK_CAUSAL_WINDOW, 97)):
+        q, kp, vp, table, cu, kl, ck, cv = paged_chunks(q_lens, kv_lens, 8, 2, 128, page_size,
+                                                        seed=200 + page_size + mode)
+        sc = scale_of(128)
+        got = to_numpy_f64(run_paged(q, kp, vp, table, cu, kl, mode, window, sc))
+        assert attn.sync_status() == attn.ATTN_OK, attn.last_error()
+        for b, (m, klen) in enumerate(zip(q_lens, kv_lens)):
+            if m == 0:
+                continue
+            s0 = int(cu[b])
+            ref = oracle.attention(q[s0:s0 + m].permute(1, 0, 2)[None], ck[b:b + 1], cv[b:b + 1], pos_offset=klen - m,
+                                   mask_mode=mode, window=window, key_lens=[klen], scale=sc)
+            assert_close(got[s0:s0 + m], ref[0].transpose(1, 0, 2), "bf16", f"seq {b} (len {m}, kv {klen}), mode {mode}")
