@@ -1,10 +1,10 @@
 """GB300-native (sm_103a) multi-head scaled-dot-product attention.
 
 The compute lives in libattn.so (C ABI, include/attn.h): a tcgen05/TMA fused
-prefill kernel (head-major, packed and paged layouts), a tensor-core decode
-kernel (contiguous, per-item and paged caches), a CUDA-core split-KV decode
-kernel, an fp32 SIMT kernel and the attention prelude (split QKV, QK norm,
-RoPE).  This package is the thin Python binding (ctypes; PyTorch supplies device
+prefill kernel (head-major, packed and paged layouts), a head_dim-64 prefill on
+64-key blocks, a tensor-core decode kernel (contiguous, per-item and paged
+caches), a CUDA-core split-KV decode kernel, an fp32 SIMT kernel and the
+attention prelude (split QKV, QK norm, RoPE).  This package is the thin Python binding (ctypes; PyTorch supplies device
 memory and streams) plus the in-tree build and the seeded synthetic input
 generator.
 """

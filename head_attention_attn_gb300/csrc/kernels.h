@@ -1,6 +1,7 @@
 // kernels.h -- internal (non-exported) launch interface between the C ABI layer
 // and the kernels: the tensor-core prefill (K1), the split-KV decode (K2), the fp32 path
-// (K3), the attention prelude (K4) and the tensor-core decode (K5).
+// (K3), the attention prelude (K4), the tensor-core decode (K5) and the head_dim-64
+// prefill on 64-key blocks (K6).
 #pragma once
 
 #include <cuda_runtime.h>
