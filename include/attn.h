@@ -320,7 +320,9 @@ ATTN_API attn_status attn_qkv_prelude_caches(const void* qkv, const float* q_nor
  * window, scale, dtype (ATTN_BF16 or ATTN_F16), cuda_stream as for attn_fwd.
  *
  * Supported: head_dim 64 or 128; otherwise ATTN_ERR_UNSUPPORTED.  batch 0 or max_seqlen_q 0
- * launches nothing.  Key rows no query sees never reach out, whatever they hold.
+ * launches nothing.  Key rows no query sees never reach out, whatever they hold.  Pages of 8
+ * to 128 rows that divide 128, or of a multiple of 128 rows, are copied a page piece at a time
+ * by TMA; other page sizes are gathered row by row, at about a third of the speed.
  *
  * Errors: host-visible arguments are checked before the launch (ATTN_ERR_INVALID_ARG for
  * negative sizes, page_size < 1, max_pages * page_size above 2^31-1, max_seqlen_q >
