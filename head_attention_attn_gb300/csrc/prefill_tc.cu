@@ -951,6 +951,385 @@ __global__ void __launch_bounds__(threads_for<NT>(), 3 - NT)
     }
 }
 
+// ---------------------------------------------------------------------- persistent form
+// Head-major inputs at head_dim 128 with an even group size and no key row that every query
+// misses (no tail zeroing): one CTA per SM walks the query blocks blockIdx.x, blockIdx.x +
+// gridDim.x, ... of the heaviest-first order (serpentine), each block two query heads of one kv group over
+// the same 128 rows (so both tiles visit the same key tiles).  The next block's Q loads once the
+// last QK^T of the current one has completed, its first K/V tiles as soon as ring slots free up,
+// and its first QK^T runs while the current block's epilogue reads O; the epilogue stores with
+// per-thread 16-byte writes, leaving the Q buffers to the next block.  Every barrier phase
+// counts across blocks.
+enum : int {
+    kPQFull = 0,
+    kPQFree = 1,                   // the block's last QK^T completed: the Q buffers may be refilled
+    kPKFull = 2,                   // + stage
+    kPVFull = kPKFull + kStages,   // + stage
+    kPKEmpty = kPVFull + kStages,  // + stage
+    kPVEmpty = kPKEmpty + kStages, // + stage
+    kPSFull = kPVEmpty + kStages,  // + tile
+    kPPHalf = kPSFull + 2,         // + tile, 8 arrivals
+    kPPFull = kPPHalf + 2,         // + tile, 8 arrivals
+    kPOFull = kPPFull + 2,         // + tile: the block's last P V product completed
+    kPOFree = kPOFull + 2,         // + tile, 8 arrivals: the epilogue has read O_t
+    kPMmaDone = kPOFree + 2,
+    kPNumBars = kPMmaDone + 1,
+};
+static_assert(kPNumBars * 8 <= 240, "barrier area");
+
+template <bool F16, bool POS>
+__global__ void __launch_bounds__(threads_for<2>(), 1)
+    prefill_persist_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                           const __grid_constant__ CUtensorMap tmV, const PrefillParams p) {
+    constexpr int D = 128;
+    using C = Cfg<D, 2>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_s = smem_u32(smem_raw);
+    uint8_t* smem = smem_raw + ((1024u - (raw_s & 1023u)) & 1023u);
+    const uint32_t sbase = smem_u32(smem);
+    const uint32_t bar0 = sbase + C::kOffBar;
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::kOffBar + 240);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffBar + 248);
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int nh = p.Hq / 2;
+    const int num_items = p.num_m * p.B * nh;
+    const int G = p.Hq / p.Hkv;
+
+    // This CTA's k-th query block: the items are in heaviest-first order, taken forwards in even
+    // rounds and backwards in odd ones, so that every CTA's total comes out about the same.
+    const int grid = (int)gridDim.x;
+    const int rounds = (num_items + grid - 1) / grid;
+    auto item_index = [&](int k) { return k * grid + ((k & 1) ? grid - 1 - (int)blockIdx.x : (int)blockIdx.x); };
+    // one query block: heads hq, hq + 1 of batch entry b, rows [q0, q0 + 128); keys from kv0 in
+    // ntiles tiles of 128
+    struct Item {
+        int hq, b, q0, ntiles;
+        long long kv0;
+    };
+    auto item_of = [&](int idx) {
+        Item it;
+        it.hq = (idx % nh) * 2;
+        idx /= nh;
+        it.b = idx % p.B;
+        idx /= p.B;
+        it.q0 = (p.num_m - 1 - idx) * BM;  // heaviest blocks first
+        long long tlo, thi;
+        key_interval(p.mode, p.window, p.Lk, (long long)p.P + it.q0, (long long)p.P + min(it.q0 + BM, p.Lq) - 1, &tlo,
+                     &thi);
+        it.kv0 = thi > tlo ? tlo : 0;
+        it.ntiles = thi > tlo ? (int)((thi - tlo + BN - 1) / BN) : 0;
+        return it;
+    };
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kPNumBars; ++i) {
+            const bool eight = (i >= kPPHalf && i < kPPHalf + 2) || (i >= kPPFull && i < kPPFull + 2) ||
+                               (i >= kPOFree && i < kPOFree + 2);
+            mbar_init(bar0 + 8 * i, eight ? 8u : 1u);
+        }
+        *abort_flag = 0;
+        mbar_fence_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_holder), C::kTmemCols);
+        tmem_relinquish();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmQ);
+        tma_prefetch_desc(&tmK);
+        tma_prefetch_desc(&tmV);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_holder;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            const uint64_t once = l2_policy_evict_first(), keep = l2_policy_evict_last();
+            long long g = 0;     // K/V tiles issued (one global count over the CTA's blocks)
+            long long gv = 0;    // V tiles issued
+            int nq = 0;          // Q pairs issued
+            bool ok = true;
+            for (int k = 0; ok && k < rounds; ++k) {
+                const int idx = item_index(k);
+                if (idx >= num_items) continue;
+                const Item it = item_of(idx);
+                const int kbh = it.b * p.Hkv + it.hq / G;
+                for (int j = 0; j < it.ntiles; ++j) {
+                    const int s = (int)(g & 1);
+                    const uint32_t n = (uint32_t)(g >> 1);
+                    const int krow = (int)it.kv0 + j * BN;
+                    if (g >= kStages && !mbar_wait(bar0 + 8 * (kPKEmpty + s), (n - 1) & 1, p.wc, abort_flag)) { ok = false; break; }
+                    mbar_arrive_expect_tx(bar0 + 8 * (kPKFull + s), C::kKVBytes);
+                    for (int c = 0; c < C::kChunks; ++c)
+                        tma_load_3d_hint(sbase + C::kOffK + s * C::kKVBytes + c * (BN * 128), &tmK, bar0 + 8 * (kPKFull + s),
+                                         c * 64, krow, kbh, keep);
+                    ++g;
+                    if (j == 0) {
+                        // the previous block's last QK^T has read its Q
+                        if (nq > 0 && !mbar_wait(bar0 + 8 * kPQFree, (uint32_t)(nq - 1) & 1, p.wc, abort_flag)) { ok = false; break; }
+                        mbar_arrive_expect_tx(bar0 + 8 * kPQFull, 2 * C::kQBytes);
+                        for (int t = 0; t < 2; ++t)
+                            for (int c = 0; c < C::kChunks; ++c)
+                                tma_load_3d_hint(sbase + C::kOffQ + t * C::kQBytes + c * (BM * 128), &tmQ, bar0 + 8 * kPQFull,
+                                                 c * 64, it.q0, it.b * p.Hq + it.hq + t, once);
+                        ++nq;
+                    }
+                    if (gv >= kStages && !mbar_wait(bar0 + 8 * (kPVEmpty + s), (n - 1) & 1, p.wc, abort_flag)) { ok = false; break; }
+                    mbar_arrive_expect_tx(bar0 + 8 * (kPVFull + s), C::kKVBytes);
+                    for (int c = 0; c < C::kChunks; ++c)
+                        tma_load_3d_hint(sbase + C::kOffV + s * C::kKVBytes + c * (BN * 128), &tmV, bar0 + 8 * (kPVFull + s),
+                                         c * 64, krow, kbh, keep);
+                    ++gv;
+                }
+            }
+            // nothing of this CTA's stays in flight when it leaves, whatever happened above
+            if (nq > 0) drain_wait(bar0 + 8 * kPQFull, (uint32_t)(nq - 1) & 1, p.wc);
+            for (long long j = (g > kStages ? g - kStages : 0); j < g; ++j)
+                drain_wait(bar0 + 8 * (kPKFull + (int)(j & 1)), (uint32_t)(j >> 1) & 1, p.wc);
+            for (long long j = (gv > kStages ? gv - kStages : 0); j < gv; ++j)
+                drain_wait(bar0 + 8 * (kPVFull + (int)(j & 1)), (uint32_t)(j >> 1) & 1, p.wc);
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t kIdescQK = idesc_f16kind_f32(BM, BN, 0, 0, F16);
+            constexpr uint32_t kIdescPV = idesc_f16kind_f32(BM, D, 0, 1, F16);
+            bool ok = true;
+            long long g0 = 0;  // global index of the block's first key tile
+            int nq = 0;        // blocks with key tiles done
+            for (int k = 0; ok && k < rounds; ++k) {
+                const int idx = item_index(k);
+                if (idx >= num_items) continue;
+                const Item it = item_of(idx);
+                if (it.ntiles == 0) continue;
+                if (!mbar_wait(bar0 + 8 * kPQFull, (uint32_t)nq & 1, p.wc, abort_flag)) break;
+                for (int j = 0; ok && j <= it.ntiles; ++j) {
+                    bool v_waited = false, k_waited = false;
+#pragma unroll
+                    for (int t = 0; t < 2; ++t) {
+                        if (j >= 1) {  // PV_t(j - 1), in two parts as P arrives
+                            const long long gp = g0 + j - 1;
+                            const int s = (int)(gp & 1);
+                            if (!mbar_wait(bar0 + 8 * (kPPHalf + t), (uint32_t)gp & 1, p.wc, abort_flag)) { ok = false; break; }
+                            // the first product of a block overwrites O_t: the previous epilogue has read it
+                            if (j == 1 && nq > 0 &&
+                                !mbar_wait(bar0 + 8 * (kPOFree + t), (uint32_t)(nq - 1) & 1, p.wc, abort_flag)) { ok = false; break; }
+                            if (!v_waited) {
+                                if (!mbar_wait(bar0 + 8 * (kPVFull + s), (uint32_t)(gp >> 1) & 1, p.wc, abort_flag)) { ok = false; break; }
+                                v_waited = true;
+                            }
+                            tc_fence_after();
+                            const uint64_t vd = smem_desc_sw128(sbase + C::kOffV + s * C::kKVBytes, BN * 128, 1024);
+                            const uint32_t tP = tmem + C::kColS + 128 * t;
+                            const uint32_t tO = tmem + C::kColO + 128 * t;
+                            for (int part = 0; part < 2; ++part) {
+                                if (part == 1) {
+                                    if (!mbar_wait(bar0 + 8 * (kPPFull + t), (uint32_t)gp & 1, p.wc, abort_flag)) { ok = false; break; }
+                                    tc_fence_after();
+                                }
+#pragma unroll
+                                for (int u = 0; u < 4; ++u) {
+                                    const int kk = (u >> 1) * 4 + part * 2 + (u & 1);
+                                    tc_mma_ts(tO, tP + kk * 8, vd + (uint64_t)((kk * 16 * 128) >> 4), kIdescPV,
+                                              (j > 1 || kk > 0) ? 1u : 0u);
+                                }
+                            }
+                            if (!ok) break;
+                            if (j == it.ntiles) tc_commit(bar0 + 8 * (kPOFull + t));
+                        }
+                        if (j < it.ntiles) {  // QK_t(j)
+                            const long long gk = g0 + j;
+                            const int s = (int)(gk & 1);
+                            if (!k_waited) {
+                                if (!mbar_wait(bar0 + 8 * (kPKFull + s), (uint32_t)(gk >> 1) & 1, p.wc, abort_flag)) { ok = false; break; }
+                                k_waited = true;
+                                tc_fence_after();
+                            }
+                            const uint64_t kd = smem_desc_sw128(sbase + C::kOffK + s * C::kKVBytes, 16, 1024);
+                            const uint64_t qd = smem_desc_sw128(sbase + C::kOffQ + t * C::kQBytes, 16, 1024);
+                            const uint32_t tS = tmem + C::kColS + 128 * t;
+#pragma unroll
+                            for (int ks = 0; ks < D / 16; ++ks) {
+                                const uint64_t off = (uint64_t)((((ks >> 2) * (BM * 128)) + (ks & 3) * 32) >> 4);
+                                tc_mma_ss(tS, qd + off, kd + off, kIdescQK, ks > 0 ? 1u : 0u);
+                            }
+                            tc_commit(bar0 + 8 * (kPSFull + t));
+                        }
+                    }
+                    if (!ok) break;
+                    if (j == it.ntiles - 1) tc_commit(bar0 + 8 * kPQFree);
+                    if (j >= 1) tc_commit(bar0 + 8 * (kPVEmpty + (int)((g0 + j - 1) & 1)));
+                    if (j < it.ntiles) tc_commit(bar0 + 8 * (kPKEmpty + (int)((g0 + j) & 1)));
+                }
+                g0 += it.ntiles;
+                ++nq;
+            }
+            tc_commit(bar0 + 8 * kPMmaDone);
+            drain_wait(bar0 + 8 * kPMmaDone, 0, p.wc);
+        }
+    } else {
+        // ------------------------------------------------------------ softmax + epilogue
+        const int sw = warp - 2;
+        const int t = sw >> 3;
+        const int h = (sw >> 2) & 1;
+        const int wq = warp & 3;
+        const int row = wq * 32 + lane;
+        const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
+        const uint32_t tS = tmem + lane_off + C::kColS + 128 * t;
+        const uint32_t tO = tmem + lane_off + C::kColO + 128 * t;
+        const float sl = p.scale_log2;
+        float* xch = reinterpret_cast<float*>(smem + C::kOffX) + (t * 2) * BM;
+        float* lch = reinterpret_cast<float*>(smem + C::kOffL) + (t * 2) * BM;
+        bool ok = true;
+        long long g0 = 0;
+        int nq = 0;
+        for (int k = 0; k < rounds; ++k) {
+            const int idx = item_index(k);
+            if (idx >= num_items) continue;
+            const Item it = item_of(idx);
+            const int qi = it.q0 + row;
+            const int hqt = it.hq + t;
+            __nv_bfloat16* orow = p.out + ((size_t)(it.b * p.Hq + hqt) * p.Lq + qi) * D + (D / 2) * h;
+            if (it.ntiles == 0) {  // no visible key: zeros (every warp of the tile takes this path)
+                if (qi < p.Lq)
+#pragma unroll
+                    for (int q = 0; q < D / 2; q += 8) *reinterpret_cast<uint4*>(orow + q) = make_uint4(0u, 0u, 0u, 0u);
+                continue;
+            }
+            long long rlo, rhi;
+            key_interval(p.mode, p.window, p.Lk, (long long)p.P + qi, (long long)p.P + qi, &rlo, &rhi);
+            const int rlo_rel = (int)(min(max(rlo, 0LL), (long long)p.Lk) - (it.kv0 + 64 * h));
+            const int rhi_rel = (int)(min(max(rhi, 0LL), (long long)p.Lk) - (it.kv0 + 64 * h));
+            float m_run = -INFINITY;
+            float l_run = 0.f;
+            for (int j = 0; j < it.ntiles; ++j) {
+                const long long g = g0 + j;
+                if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar0 + 8 * (kPSFull + t), (uint32_t)g & 1, p.wc, abort_flag));
+                tc_fence_after();
+                const int c_lo = min(max(rlo_rel - j * BN, 0), 64);
+                const int c_hi = min(max(rhi_rel - j * BN, 0), 64);
+                const bool full = (c_lo == 0 && c_hi == 64);
+                float s[64];
+                tmem_ld64(tS + 64 * h, s);
+                float hext;
+                if (POS || sl >= 0.f) {
+                    if (!full) mask_scores64(s, range_bits64(c_lo, c_hi), -INFINITY);
+                    hext = row_max64(s);
+                } else {
+                    if (!full) mask_scores64(s, range_bits64(c_lo, c_hi), INFINITY);
+                    hext = row_min64(s);
+                }
+                // the half-row extremes meet at the tile's named barrier (every warp of the tile,
+                // every block, on every path)
+                xch[h * BM + row] = hext;
+                tile_bar_sync(t);
+                if (!ok) continue;
+                const float oext = xch[(1 - h) * BM + row];
+                const float ext = (POS || sl >= 0.f) ? fmaxf(hext, oext) : fminf(hext, oext);
+                const bool any = (POS || sl >= 0.f) ? (ext != -INFINITY) : (ext != INFINITY);
+                float alpha = 1.f;
+                bool rescale = false;
+                if (any) {
+                    const float ms = ext * sl;
+                    if (m_run == -INFINITY) {
+                        m_run = ms;
+                    } else if (ms > m_run + kRescaleThreshold) {
+                        alpha = ex2_approx(m_run - ms);
+                        m_run = ms;
+                        rescale = true;
+                    }
+                }
+                const float neg_m = (m_run == -INFINITY) ? 0.f : -m_run;
+                const float2 sl2 = make_float2(sl, sl), negm2 = make_float2(neg_m, neg_m);
+                const bool warp_rescale = __any_sync(0xffffffffu, rescale);
+                auto release_first_part = [&]() {
+                    tmem_st_wait();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar0 + 8 * (kPPHalf + t));
+                };
+                float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+#pragma unroll
+                for (int k = 0; k < 2; ++k) {
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int c2 = 0; c2 < 32; c2 += 2) {
+                        const int c = 32 * k + c2;
+                        const float2 x2 = __ffma2_rn(make_float2(s[c], s[c + 1]), sl2, negm2);
+                        float p0 = ex2_approx(x2.x);
+                        float p1 = ex2_approx(x2.y);
+                        if (!POS && !full && sl == 0.f) {
+                            p0 = (c >= c_lo && c < c_hi) ? p0 : 0.f;
+                            p1 = (c + 1 >= c_lo && c + 1 < c_hi) ? p1 : 0.f;
+                        }
+                        const uint32_t wv = pack2<F16>(p0, p1);
+                        pk[c2 / 2] = wv;
+                        const float2 r2 = unpack2<F16>(wv);
+                        if ((c2 / 2) & 1) acc1 = __fadd2_rn(acc1, r2); else acc0 = __fadd2_rn(acc0, r2);
+                    }
+                    tmem_st16_async(tS + 32 * h + 16 * k, pk);
+                    if (k == 0 && !warp_rescale) release_first_part();
+                }
+                tmem_st_wait();
+                acc0 = __fadd2_rn(acc0, acc1);
+                l_run = l_run * alpha + (acc0.x + acc0.y);
+                if (warp_rescale) {  // O_t is stable: S_t(j) came after the previous P V product
+#pragma unroll
+                    for (int c = 0; c < D / 64; ++c) {
+                        float o[32];
+                        tmem_ld32(tO + (D / 2) * h + 32 * c, o);
+#pragma unroll
+                        for (int q = 0; q < 32; ++q) o[q] *= alpha;
+                        tmem_st32(tO + (D / 2) * h + 32 * c, o);
+                    }
+                    release_first_part();
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar0 + 8 * (kPPFull + t));
+            }
+            // ------------------------------------------------------------ epilogue of the block
+            if (ok) lch[h * BM + row] = l_run;
+            tile_bar_sync(t);
+            float l_tot = l_run;
+            if (ok) l_tot += lch[(1 - h) * BM + row];
+            if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar0 + 8 * (kPOFull + t), (uint32_t)nq & 1, p.wc, abort_flag));
+            tc_fence_after();
+            const float inv = (l_tot > 0.f) ? 1.f / l_tot : 0.f;
+#pragma unroll
+            for (int c = 0; c < D / 64; ++c) {
+                float o[32];
+                tmem_ld32(tO + (D / 2) * h + 32 * c, o);  // (warp-collective; stale after a give-up, then unused)
+                if (ok && qi < p.Lq) {
+#pragma unroll
+                    for (int q = 0; q < 32; q += 8)
+                        *reinterpret_cast<uint4*>(orow + 32 * c + q) =
+                            make_uint4(pack2<F16>(o[q] * inv, o[q + 1] * inv), pack2<F16>(o[q + 2] * inv, o[q + 3] * inv),
+                                       pack2<F16>(o[q + 4] * inv, o[q + 5] * inv), pack2<F16>(o[q + 6] * inv, o[q + 7] * inv));
+                }
+            }
+            // O_t has been read: the next block's first product may overwrite it
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar0 + 8 * (kPOFree + t));
+            g0 += it.ntiles;
+            ++nq;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) {
+        __syncwarp();
+        tmem_dealloc(tmem, C::kTmemCols);
+    }
+}
+
 // ---------------------------------------------------------------------- host side
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -1092,6 +1471,64 @@ cudaError_t launch_impl(const Problem& pr, const WaitCtl& wc, cudaStream_t strea
 // Whether the tail zeroing can matter for a head-major call: only key padding, or a mask whose
 // band (the union over all queries) ends before kv_len, leaves rows inside the tensor that no
 // query sees.
+// SMs of the current device (looked up once per device); 0 if unknown.
+int sm_count() {
+    static std::mutex mu;
+    static int count[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    std::lock_guard<std::mutex> g(mu);
+    if (count[dev] == 0 && cudaDeviceGetAttribute(&count[dev], cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        count[dev] = 0;
+    return count[dev];
+}
+
+// The persistent paired-head kernel: head-major q/k/v/out, head_dim 128, even group size, no
+// key padding and no key row past every query's band.  One CTA per SM (at most one per block).
+template <bool F16, bool POS>
+cudaError_t launch_persist(const Problem& pr, const WaitCtl& wc, cudaStream_t stream) {
+    using C = Cfg<128, 2>;
+    CUtensorMap tq, tk, tv;
+    if (!encode_16bit_3d(&tq, pr.q, 128, pr.Lq, pr.B * pr.Hq, F16) ||
+        !encode_16bit_3d(&tk, pr.k, 128, pr.Lk, pr.B * pr.Hkv, F16) ||
+        !encode_16bit_3d(&tv, pr.v, 128, pr.Lk, pr.B * pr.Hkv, F16))
+        return cudaErrorInvalidValue;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    static std::mutex mu;
+    static bool configured[64] = {};
+    {
+        std::lock_guard<std::mutex> g(mu);
+        if (dev < 64 && !configured[dev]) {
+            e = cudaFuncSetAttribute(prefill_persist_kernel<F16, POS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     C::kSmem);
+            if (e != cudaSuccess) return e;
+            configured[dev] = true;
+        }
+    }
+    PrefillParams p = {};
+    p.out = reinterpret_cast<__nv_bfloat16*>(pr.out);
+    p.B = pr.B;
+    p.Hq = pr.Hq;
+    p.Hkv = pr.Hkv;
+    p.Lq = pr.Lq;
+    p.Lk = pr.Lk;
+    p.P = pr.pos_offset;
+    p.mode = pr.mode;
+    p.window = pr.window;
+    p.num_m = (pr.Lq + BM - 1) / BM;
+    p.scale_log2 = pr.scale * kLog2e;
+    p.wc = wc;
+    const long long items = (long long)p.num_m * pr.B * (pr.Hq / 2);
+    if (items > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    const int sms = sm_count();
+    const long long grid = std::min(items, (long long)(sms > 0 ? sms : 1));
+    if (grid <= 0) return cudaSuccess;
+    prefill_persist_kernel<F16, POS><<<(unsigned)grid, threads_for<2>(), C::kSmem, stream>>>(tq, tk, tv, p);
+    return cudaGetLastError();
+}
+
 bool tail_zero_needed(const Problem& p) {
     if (p.key_lens != nullptr || p.cu_seqlens != nullptr) return true;
     long long slo, shi;
@@ -1123,6 +1560,14 @@ cudaError_t launch_layout(const Problem& p, const WaitCtl& wc, cudaStream_t stre
         return cudaErrorInvalidValue;
     }
     if (p.D == 128) {
+        if constexpr (LAYOUT == kHeadMajor) {
+            if ((p.Hq / p.Hkv) % 2 == 0 && !p.out_tok && !tail_zero_needed(p)) {
+                if (p.f16) return p.scale > 0.f ? launch_persist<true, true>(p, wc, stream)
+                                                : launch_persist<true, false>(p, wc, stream);
+                return p.scale > 0.f ? launch_persist<false, true>(p, wc, stream)
+                                     : launch_persist<false, false>(p, wc, stream);
+            }
+        }
         if ((p.Hq / p.Hkv) % 2 == 0)
             return p.f16 ? launch_zt<128, 2, true, LAYOUT, true>(p, wc, stream)
                          : launch_zt<128, 2, false, LAYOUT, true>(p, wc, stream);
