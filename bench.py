@@ -50,11 +50,9 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM bytes per launch measured by ncu (dram__bytes_read.sum + dram__bytes_write.sum) for a
 # kernel's code state (its hash); the entry stops applying as soon as the kernel's code changes.
 NCU_TRAFFIC = {
-    # prefill_tc_kernel<128, 2, bf16, paired heads, positive scale>, causal GQA, with L2 hints
-    # (Q and O evict-first, K/V evict-last) and P released in two parts: 303.61 MB read + 86.48 MB written
-    ("prefill", "6ee0df80697f"): 390087168.0,
-    # the same kernel, paged layout, chunked prefill with 16-row pages: 118.66 MB read + 11.20 MB written
-    ("prefill", "6ee0df80697f", "paged16"): 129861888.0,
+    # prefill_persist_kernel<bf16, positive scale>, causal GQA (one CTA per SM over the query
+    # blocks, paired heads): 270.78 MB read + 84.46 MB written
+    ("prefill", "5d31cce28617"): 355241728.0,
     # decode_tc_kernel<G4, bf16>: 537.11 MB read + 3.26 MB written at batch 16, scaled by the units
     # (items) to the bench's batch 64
     ("decode_tc", "b900f0549270"): 4 * 540366336.0,
@@ -464,7 +462,8 @@ def run_ours(args, rank, world, local):
     value = tflops * world  # replicas: every rank processes one full workload per step
     roof = {"bound": "tensor", "achieved": round(tflops, 2), "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
             "frac": round(tflops / peaks["bf16_tflops"], 4), "peak_source": f"{peak_src} bf16 dense (burst)",
-            "traffic": NCU_TRAFFIC.get(("prefill", kernel_source_hash("prefill"))), "kernel": "prefill_tc_kernel<128, 2 tiles, bf16>",
+            "traffic": NCU_TRAFFIC.get(("prefill", kernel_source_hash("prefill"))),
+            "kernel": "prefill_persist_kernel<bf16> (one CTA per SM, two query heads of a kv group per block)",
             "algorithmic_flops_per_launch": flops}
 
     # ---- end to end through the public call with pinned host buffers: every step copies its
