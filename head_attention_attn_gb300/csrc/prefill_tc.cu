@@ -1193,7 +1193,9 @@ __global__ void __launch_bounds__(threads_for<2>(), 1)
             const Item it = item_of(idx);
             const int qi = it.q0 + row;
             const int hqt = it.hq + t;
-            __nv_bfloat16* orow = p.out + ((size_t)(it.b * p.Hq + hqt) * p.Lq + qi) * D + (D / 2) * h;
+            __nv_bfloat16* orow = p.out + (D / 2) * h +
+                                  (p.out_tok ? (((size_t)it.b * p.Lq + qi) * p.Hq + hqt) * D   // [B, Lq, Hq, D]
+                                             : ((size_t)(it.b * p.Hq + hqt) * p.Lq + qi) * D); // [B, Hq, Lq, D]
             if (it.ntiles == 0) {  // no visible key: zeros (every warp of the tile takes this path)
                 if (qi < p.Lq)
 #pragma unroll
@@ -1483,8 +1485,9 @@ int sm_count() {
     return count[dev];
 }
 
-// The persistent paired-head kernel: head-major q/k/v/out, head_dim 128, even group size, no
-// key padding and no key row past every query's band.  One CTA per SM (at most one per block).
+// The persistent paired-head kernel: head-major q/k/v, out head-major or token-major, head_dim
+// 128, even group size, no key padding and no key row past every query's band.  One CTA per SM
+// (at most one per block).
 template <bool F16, bool POS>
 cudaError_t launch_persist(const Problem& pr, const WaitCtl& wc, cudaStream_t stream) {
     using C = Cfg<128, 2>;
@@ -1518,6 +1521,7 @@ cudaError_t launch_persist(const Problem& pr, const WaitCtl& wc, cudaStream_t st
     p.mode = pr.mode;
     p.window = pr.window;
     p.num_m = (pr.Lq + BM - 1) / BM;
+    p.out_tok = pr.out_tok ? 1 : 0;
     p.scale_log2 = pr.scale * kLog2e;
     p.wc = wc;
     const long long items = (long long)p.num_m * pr.B * (pr.Hq / 2);
@@ -1561,7 +1565,7 @@ cudaError_t launch_layout(const Problem& p, const WaitCtl& wc, cudaStream_t stre
     }
     if (p.D == 128) {
         if constexpr (LAYOUT == kHeadMajor) {
-            if ((p.Hq / p.Hkv) % 2 == 0 && !p.out_tok && !tail_zero_needed(p)) {
+            if ((p.Hq / p.Hkv) % 2 == 0 && !tail_zero_needed(p)) {
                 if (p.f16) return p.scale > 0.f ? launch_persist<true, true>(p, wc, stream)
                                                 : launch_persist<true, false>(p, wc, stream);
                 return p.scale > 0.f ? launch_persist<false, true>(p, wc, stream)
