@@ -274,3 +274,22 @@ def test_decode_tc_key_padding_multi_split(dtype):
     c = Case("dectcpad", dtype, B=4, Hq=32, Hkv=4, Lq=1, Lk=6000, D=128, pos_offset=5999, mask_mode=MASK_CAUSAL,
              key_len_range=(0, 6000), seed=9700)
     full_check(c)
+
+
+# Windowed masks with more 128-row tiles than the GPU holds at once (four CTAs on each of its
+# 152 SMs), so that tiles run in several waves: every output element is compared, with windows
+# narrower and wider than a tile, an offset query block, GQA and fp16.
+@pytest.mark.parametrize("mode,window,P,extra,dtype", [
+    (MASK_WINDOW, 128, 0, 0, "bf16"),
+    (MASK_WINDOW, 1, 0, 0, "bf16"),
+    (MASK_WINDOW, 300, 0, 0, "bf16"),
+    (MASK_WINDOW, 129, 37, 37, "bf16"),
+    (MASK_CAUSAL_WINDOW, 200, 0, 0, "bf16"),
+    (MASK_CAUSAL_WINDOW, 64, 100, 100, "bf16"),
+    (MASK_WINDOW, 128, 0, 0, "f16"),
+])
+def test_window_band_walk(mode, window, P, extra, dtype):
+    c = Case(f"walk_m{mode}_w{window}", dtype, B=2, Hq=8, Hkv=4, Lq=6000, Lk=6000 + extra, D=64, pos_offset=P,
+             mask_mode=mode, window=window, seed=700 + window + mode)
+    assert (c.Lq + 127) // 128 * c.B * c.Hq > 4 * 152  # more tiles than four CTAs on every SM
+    full_check(c)
