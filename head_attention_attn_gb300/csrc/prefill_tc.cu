@@ -193,6 +193,138 @@ __device__ __forceinline__ void tile_bar_sync(int t) {
     else named_bar_sync<2, 256>();
 }
 
+// One key block of a query tile's softmax, for one thread: half a row of S (64 scores at
+// TMEM columns 64h of tS), the row extreme exchanged with the other half through xch at the
+// tile's named barrier (every warp of the tile meets it once per block on every path, so it
+// cannot hang; a thread that gave up, !ok, stops right after it), P for the 64 keys written to
+// columns [32h, 32h + 32) of tS in two parts (the first released on bar_phalf, all of it on
+// bar_pfull), the running maximum and sum updated and O rescaled in TMEM when the maximum
+// jumps.  MAYSKIP: a warp whose rows see none of its keys writes zeros without exponentials.
+template <int D, bool F16, bool POS, bool MAYSKIP>
+__device__ __forceinline__ void softmax_block(uint32_t tS, uint32_t tO, int h, int row, int lane, int t, float sl,
+                                              int rlo_rel, int rhi_rel, int j, float* xch, bool ok, float& m_run,
+                                              float& l_run, uint32_t bar_phalf, uint32_t bar_pfull) {
+    const int c_lo = min(max(rlo_rel - j * BN, 0), 64);  // my visible columns [c_lo, c_hi)
+    const int c_hi = min(max(rhi_rel - j * BN, 0), 64);
+    const bool full = (c_lo == 0 && c_hi == 64);
+    // every row of my warp sees none of my 64 keys (a band edge on a 32-row boundary):
+    // no max and no exponentials, just zeros for my half of P.  Only with one tile per
+    // CTA (head_dim 64): there every window key tile has such warps, while at two tiles
+    // only diagonal tiles do and the test costs more than it saves.
+    const bool skip = MAYSKIP && __all_sync(0xffffffffu, c_lo >= c_hi);
+
+    // My 64 scores stay in registers for both passes: the other half writes P into
+    // columns 32..63 after the exchange below, so nothing is read back from TMEM.
+    // (after a give-up the load below reads allocated but stale columns; nothing uses them)
+    float s[64];
+    tmem_ld64(tS + 64 * h, s);
+    float hext;
+    if (skip) {
+        hext = (POS || sl >= 0.f) ? -INFINITY : INFINITY;
+    } else if (POS || sl >= 0.f) {
+        if (!full) {
+            mask_scores64(s, range_bits64(c_lo, c_hi), -INFINITY);
+        }
+        hext = row_max64(s);
+    } else {
+        if (!full) {
+            mask_scores64(s, range_bits64(c_lo, c_hi), INFINITY);
+        }
+        hext = row_min64(s);
+    }
+    // exchange the half extremes of each row between the two halves of the tile; every
+    // warp of the tile meets this barrier once per key block on every path, so it
+    // cannot hang (the order of S_t(j+1) after every P_t(j) keeps the slots from
+    // being overwritten before the partner has read them)
+    xch[h * BM + row] = hext;
+    tile_bar_sync(t);
+    if (!ok) return;
+    const float oext = xch[(1 - h) * BM + row];
+    const float ext = (POS || sl >= 0.f) ? fmaxf(hext, oext) : fminf(hext, oext);
+    const bool any = (POS || sl >= 0.f) ? (ext != -INFINITY) : (ext != INFINITY);
+
+    float alpha = 1.f;
+    bool rescale = false;
+    if (any) {
+        const float ms = ext * sl;
+        if (m_run == -INFINITY) {
+            m_run = ms;
+        } else if (ms > m_run + kRescaleThreshold) {
+            alpha = ex2_approx(m_run - ms);
+            m_run = ms;
+            rescale = true;
+        }
+    }
+    const float neg_m = (m_run == -INFINITY) ? 0.f : -m_run;
+    const float2 sl2 = make_float2(sl, sl), negm2 = make_float2(neg_m, neg_m);
+
+    // The product over this block's P starts once every warp of the tile has released the
+    // first 32 of its keys; a warp that must rescale O first (rare) releases them only
+    // after the rescale below, with the rest.
+    const bool warp_rescale = __any_sync(0xffffffffu, rescale);
+    auto release_first_part = [&]() {
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_phalf);
+    };
+    // P for my 64 keys -> TMEM columns [32h, 32h + 32) of S_t, as bf16 or fp16 pairs; the row
+    // sum adds the rounded values the tensor core will multiply into V.
+    float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+    if (skip) {
+        uint32_t z[16];
+#pragma unroll
+        for (int q = 0; q < 16; ++q) z[q] = 0u;
+        tmem_st16_async(tS + 32 * h, z);
+        if (!warp_rescale) release_first_part();
+        tmem_st16_async(tS + 32 * h + 16, z);
+    } else {
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int c2 = 0; c2 < 32; c2 += 2) {
+            const int c = 32 * k + c2;
+            const float2 x2 = __ffma2_rn(make_float2(s[c], s[c + 1]), sl2, negm2);
+            float p0 = ex2_approx(x2.x);  // special-function unit; 2^-inf = 0
+            float p1 = ex2_approx(x2.y);
+            // Masked scores hold -inf (or +inf with a negative scale), so their
+            // 2^(s*scale*log2e - m) is already exactly 0; only scale 0 turns them
+            // into NaN (inf * 0) and needs the explicit zero.
+            if (!POS && !full && sl == 0.f) {
+                p0 = (c >= c_lo && c < c_hi) ? p0 : 0.f;
+                p1 = (c + 1 >= c_lo && c + 1 < c_hi) ? p1 : 0.f;
+            }
+            const uint32_t wv = pack2<F16>(p0, p1);
+            pk[c2 / 2] = wv;
+            const float2 r2 = unpack2<F16>(wv);
+            if ((c2 / 2) & 1) acc1 = __fadd2_rn(acc1, r2); else acc0 = __fadd2_rn(acc0, r2);
+        }
+        tmem_st16_async(tS + 32 * h + 16 * k, pk);
+        if (k == 0 && !warp_rescale) release_first_part();
+    }
+    }
+    tmem_st_wait();
+    acc0 = __fadd2_rn(acc0, acc1);
+    l_run = l_run * alpha + (acc0.x + acc0.y);
+    // O_t is stable here: the commit behind S_t(j) covers the earlier P V product, and
+    // this block's has not started (this warp has released nothing yet).
+    if (warp_rescale) {
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c) {
+            float o[32];
+            tmem_ld32(tO + (D / 2) * h + 32 * c, o);
+#pragma unroll
+            for (int q = 0; q < 32; ++q) o[q] *= alpha;
+            tmem_st32(tO + (D / 2) * h + 32 * c, o);
+        }
+        release_first_part();
+    }
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar_pfull);
+}
+
 // PAIR (two tiles, even group size): the tiles are two query heads of one kv group over the
 // same 128 query rows, so both visit exactly the same key tiles.  Otherwise the tiles are two
 // consecutive 128-row blocks of one query head.
@@ -728,125 +860,8 @@ __global__ void __launch_bounds__(threads_for<NT>(), 3 - NT)
             // once per key block, so the other warps of the tile never wait for it.
             if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar0 + 8 * (kBarSFull + t), (uint32_t)i & 1, p.wc, abort_flag));
             tc_fence_after();
-            const int c_lo = min(max(rlo_rel - j * BN, 0), 64);  // my visible columns [c_lo, c_hi)
-            const int c_hi = min(max(rhi_rel - j * BN, 0), 64);
-            const bool full = (c_lo == 0 && c_hi == 64);
-            // every row of my warp sees none of my 64 keys (a band edge on a 32-row boundary):
-            // no max and no exponentials, just zeros for my half of P.  Only with one tile per
-            // CTA (head_dim 64): there every window key tile has such warps, while at two tiles
-            // only diagonal tiles do and the test costs more than it saves.
-            const bool skip = kTiles == 1 && __all_sync(0xffffffffu, c_lo >= c_hi);
-
-            // My 64 scores stay in registers for both passes: the other half writes P into
-            // columns 32..63 after the exchange below, so nothing is read back from TMEM.
-            // (after a give-up the load below reads allocated but stale columns; nothing uses them)
-            float s[64];
-            tmem_ld64(tS + 64 * h, s);
-            float hext;
-            if (skip) {
-                hext = (POS || sl >= 0.f) ? -INFINITY : INFINITY;
-            } else if (POS || sl >= 0.f) {
-                if (!full) {
-                    mask_scores64(s, range_bits64(c_lo, c_hi), -INFINITY);
-                }
-                hext = row_max64(s);
-            } else {
-                if (!full) {
-                    mask_scores64(s, range_bits64(c_lo, c_hi), INFINITY);
-                }
-                hext = row_min64(s);
-            }
-            // exchange the half extremes of each row between the two halves of the tile; every
-            // warp of the tile meets this barrier once per key block on every path, so it
-            // cannot hang (the order of S_t(j+1) after every P_t(j) keeps the slots from
-            // being overwritten before the partner has read them)
-            xch[h * BM + row] = hext;
-            tile_bar_sync(t);
-            if (!ok) continue;
-            const float oext = xch[(1 - h) * BM + row];
-            const float ext = (POS || sl >= 0.f) ? fmaxf(hext, oext) : fminf(hext, oext);
-            const bool any = (POS || sl >= 0.f) ? (ext != -INFINITY) : (ext != INFINITY);
-
-            float alpha = 1.f;
-            bool rescale = false;
-            if (any) {
-                const float ms = ext * sl;
-                if (m_run == -INFINITY) {
-                    m_run = ms;
-                } else if (ms > m_run + kRescaleThreshold) {
-                    alpha = ex2_approx(m_run - ms);
-                    m_run = ms;
-                    rescale = true;
-                }
-            }
-            const float neg_m = (m_run == -INFINITY) ? 0.f : -m_run;
-            const float2 sl2 = make_float2(sl, sl), negm2 = make_float2(neg_m, neg_m);
-
-            // The product over this block's P starts once every warp of the tile has released the
-            // first 32 of its keys; a warp that must rescale O first (rare) releases them only
-            // after the rescale below, with the rest.
-            const bool warp_rescale = __any_sync(0xffffffffu, rescale);
-            auto release_first_part = [&]() {
-                tmem_st_wait();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar0 + 8 * (kBarPHalf + t));
-            };
-            // P for my 64 keys -> TMEM columns [32h, 32h + 32) of S_t, as bf16 or fp16 pairs; the row
-            // sum adds the rounded values the tensor core will multiply into V.
-            float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
-            if (skip) {
-                uint32_t z[16];
-#pragma unroll
-                for (int q = 0; q < 16; ++q) z[q] = 0u;
-                tmem_st16_async(tS + 32 * h, z);
-                if (!warp_rescale) release_first_part();
-                tmem_st16_async(tS + 32 * h + 16, z);
-            } else {
-#pragma unroll
-            for (int k = 0; k < 2; ++k) {
-                uint32_t pk[16];
-#pragma unroll
-                for (int c2 = 0; c2 < 32; c2 += 2) {
-                    const int c = 32 * k + c2;
-                    const float2 x2 = __ffma2_rn(make_float2(s[c], s[c + 1]), sl2, negm2);
-                    float p0 = ex2_approx(x2.x);  // special-function unit; 2^-inf = 0
-                    float p1 = ex2_approx(x2.y);
-                    // Masked scores hold -inf (or +inf with a negative scale), so their
-                    // 2^(s*scale*log2e - m) is already exactly 0; only scale 0 turns them
-                    // into NaN (inf * 0) and needs the explicit zero.
-                    if (!POS && !full && sl == 0.f) {
-                        p0 = (c >= c_lo && c < c_hi) ? p0 : 0.f;
-                        p1 = (c + 1 >= c_lo && c + 1 < c_hi) ? p1 : 0.f;
-                    }
-                    const uint32_t wv = pack2<F16>(p0, p1);
-                    pk[c2 / 2] = wv;
-                    const float2 r2 = unpack2<F16>(wv);
-                    if ((c2 / 2) & 1) acc1 = __fadd2_rn(acc1, r2); else acc0 = __fadd2_rn(acc0, r2);
-                }
-                tmem_st16_async(tS + 32 * h + 16 * k, pk);
-                if (k == 0 && !warp_rescale) release_first_part();
-            }
-            }
-            tmem_st_wait();
-            acc0 = __fadd2_rn(acc0, acc1);
-            l_run = l_run * alpha + (acc0.x + acc0.y);
-            // O_t is stable here: the commit behind S_t(j) covers the earlier P V product, and
-            // this block's has not started (this warp has released nothing yet).
-            if (warp_rescale) {
-#pragma unroll
-                for (int c = 0; c < D / 64; ++c) {
-                    float o[32];
-                    tmem_ld32(tO + (D / 2) * h + 32 * c, o);
-#pragma unroll
-                    for (int q = 0; q < 32; ++q) o[q] *= alpha;
-                    tmem_st32(tO + (D / 2) * h + 32 * c, o);
-                }
-                release_first_part();
-            }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar0 + 8 * (kBarPFull + t));
+            softmax_block<D, F16, POS, kTiles == 1>(tS, tO, h, row, lane, t, sl, rlo_rel, rhi_rel, j, xch, ok, m_run,
+                                                    l_run, bar0 + 8 * (kBarPHalf + t), bar0 + 8 * (kBarPFull + t));
         }
 
         // ------------------------------------------------------------ epilogue
@@ -1212,87 +1227,8 @@ __global__ void __launch_bounds__(threads_for<2>(), 1)
                 const long long g = g0 + j;
                 if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar0 + 8 * (kPSFull + t), (uint32_t)g & 1, p.wc, abort_flag));
                 tc_fence_after();
-                const int c_lo = min(max(rlo_rel - j * BN, 0), 64);
-                const int c_hi = min(max(rhi_rel - j * BN, 0), 64);
-                const bool full = (c_lo == 0 && c_hi == 64);
-                float s[64];
-                tmem_ld64(tS + 64 * h, s);
-                float hext;
-                if (POS || sl >= 0.f) {
-                    if (!full) mask_scores64(s, range_bits64(c_lo, c_hi), -INFINITY);
-                    hext = row_max64(s);
-                } else {
-                    if (!full) mask_scores64(s, range_bits64(c_lo, c_hi), INFINITY);
-                    hext = row_min64(s);
-                }
-                // the half-row extremes meet at the tile's named barrier (every warp of the tile,
-                // every block, on every path)
-                xch[h * BM + row] = hext;
-                tile_bar_sync(t);
-                if (!ok) continue;
-                const float oext = xch[(1 - h) * BM + row];
-                const float ext = (POS || sl >= 0.f) ? fmaxf(hext, oext) : fminf(hext, oext);
-                const bool any = (POS || sl >= 0.f) ? (ext != -INFINITY) : (ext != INFINITY);
-                float alpha = 1.f;
-                bool rescale = false;
-                if (any) {
-                    const float ms = ext * sl;
-                    if (m_run == -INFINITY) {
-                        m_run = ms;
-                    } else if (ms > m_run + kRescaleThreshold) {
-                        alpha = ex2_approx(m_run - ms);
-                        m_run = ms;
-                        rescale = true;
-                    }
-                }
-                const float neg_m = (m_run == -INFINITY) ? 0.f : -m_run;
-                const float2 sl2 = make_float2(sl, sl), negm2 = make_float2(neg_m, neg_m);
-                const bool warp_rescale = __any_sync(0xffffffffu, rescale);
-                auto release_first_part = [&]() {
-                    tmem_st_wait();
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(bar0 + 8 * (kPPHalf + t));
-                };
-                float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
-#pragma unroll
-                for (int k = 0; k < 2; ++k) {
-                    uint32_t pk[16];
-#pragma unroll
-                    for (int c2 = 0; c2 < 32; c2 += 2) {
-                        const int c = 32 * k + c2;
-                        const float2 x2 = __ffma2_rn(make_float2(s[c], s[c + 1]), sl2, negm2);
-                        float p0 = ex2_approx(x2.x);
-                        float p1 = ex2_approx(x2.y);
-                        if (!POS && !full && sl == 0.f) {
-                            p0 = (c >= c_lo && c < c_hi) ? p0 : 0.f;
-                            p1 = (c + 1 >= c_lo && c + 1 < c_hi) ? p1 : 0.f;
-                        }
-                        const uint32_t wv = pack2<F16>(p0, p1);
-                        pk[c2 / 2] = wv;
-                        const float2 r2 = unpack2<F16>(wv);
-                        if ((c2 / 2) & 1) acc1 = __fadd2_rn(acc1, r2); else acc0 = __fadd2_rn(acc0, r2);
-                    }
-                    tmem_st16_async(tS + 32 * h + 16 * k, pk);
-                    if (k == 0 && !warp_rescale) release_first_part();
-                }
-                tmem_st_wait();
-                acc0 = __fadd2_rn(acc0, acc1);
-                l_run = l_run * alpha + (acc0.x + acc0.y);
-                if (warp_rescale) {  // O_t is stable: S_t(j) came after the previous P V product
-#pragma unroll
-                    for (int c = 0; c < D / 64; ++c) {
-                        float o[32];
-                        tmem_ld32(tO + (D / 2) * h + 32 * c, o);
-#pragma unroll
-                        for (int q = 0; q < 32; ++q) o[q] *= alpha;
-                        tmem_st32(tO + (D / 2) * h + 32 * c, o);
-                    }
-                    release_first_part();
-                }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar0 + 8 * (kPPFull + t));
+                softmax_block<D, F16, POS, false>(tS, tO, h, row, lane, t, sl, rlo_rel, rhi_rel, j, xch, ok, m_run, l_run,
+                                                  bar0 + 8 * (kPPHalf + t), bar0 + 8 * (kPPFull + t));
             }
             // ------------------------------------------------------------ epilogue of the block
             if (ok) lch[h * BM + row] = l_run;
