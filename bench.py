@@ -51,11 +51,11 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # kernel's code state (its hash); the entry stops applying as soon as the kernel's code changes.
 NCU_TRAFFIC = {
     # prefill_persist_kernel<bf16, positive scale>, causal GQA (one CTA per SM over the query
-    # blocks, paired heads): 297.57 MB read + 84.94 MB written
-    ("prefill", "d5f42663039e"): 382511360.0,
+    # blocks, paired heads): 289.54 MB read + 84.92 MB written
+    ("prefill", "20541aa39a87"): 374458112.0,
     # prefill_tc_kernel<128, 2, bf16, paged, paired heads>, chunked prefill with 16-row pages:
-    # 118.64 MB read + 11.19 MB written
-    ("prefill", "d5f42663039e", "paged16"): 129835008.0,
+    # 113.00 MB read + 8.64 MB written
+    ("prefill", "20541aa39a87", "paged16"): 121643264.0,
     # decode_tc_kernel<G4, bf16>: 537.11 MB read + 3.26 MB written at batch 16, scaled by the units
     # (items) to the bench's batch 64
     ("decode_tc", "b900f0549270"): 4 * 540366336.0,
