@@ -8,7 +8,9 @@
 //                                   written on the device), and paged caches of that shape
 //                                   where the measured routing table prefers it
 //   bf16/fp16, q_len == 1, group 1/2/4/8 -> K2 (split-KV decode, the other shapes)
-//   bf16/fp16 otherwise          -> K1 (tcgen05 + TMA fused prefill); packed queries over
+//   bf16/fp16 otherwise          -> K1 (tcgen05 + TMA fused prefill; head-major, head_dim 128,
+//                                   even group, no key padding: its persistent form, one CTA
+//                                   per SM over the query blocks); packed queries over
 //                                   paged caches also go to K1, whose producer copies K/V
 //                                   by TMA a page piece at a time (page sizes of 8..128 rows
 //                                   dividing 128, or multiples of 128) or else gathers the
