@@ -8,6 +8,7 @@
 //                                   written on the device), and paged caches of that shape
 //                                   where the measured routing table prefers it
 //   bf16/fp16, q_len == 1, group 1/2/4/8 -> K2 (split-KV decode, the other shapes)
+//   bf16/fp16, head_dim 64, head-major or packed -> K6 (tcgen05 prefill on 64-key blocks)
 //   bf16/fp16 otherwise          -> K1 (tcgen05 + TMA fused prefill; head-major, head_dim 128,
 //                                   even group, no key padding: its persistent form, one CTA
 //                                   per SM over the query blocks); packed queries over
