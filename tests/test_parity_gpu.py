@@ -135,6 +135,37 @@ def test_prefill_large_scores_force_rescaling():
     full_check(c, scale=0.6)
 
 
+def test_paired_head_prefill_scale_zero_and_negative():
+    """Head_dim 128 with an even group and no key padding (the persistent form, one CTA per SM
+    over the query blocks): scale 0 and a negative scale (the general softmax build)."""
+    c = Case("pair_sc", "bf16", B=2, Hq=4, Hkv=2, Lq=300, Lk=420, D=128, mask_mode=MASK_CAUSAL, pos_offset=120, seed=8)
+    full_check(c, scale=0.0)
+    full_check(c, scale=-0.2)
+
+
+@pytest.mark.parametrize("Hq", [8, 6])  # even group: the persistent form; odd group: one CTA per block
+def test_sharp_softmax_rescaling_within_rounding_bound(Hq):
+    """Scale 0.6 at head_dim 128 (about 7x 1/sqrt(128)) makes the running maximum jump by far
+    more than 2^8 between key tiles, so O is rescaled in TMEM, and leaves each row's weight on a
+    few keys, where the bf16 rounding of P no longer averages out.  bf16 keeps 8 significant
+    bits, so each P is within 2^-8 of its value relative, and the row sum adds the same rounded
+    values: O moves by at most 2^-8 max|v - O|; rounding O to bf16 adds 2^-8 |O|: in all at
+    most 3 * 2^-8 * max|v|.  Both kernels are held to that bound and to the usual relative L2
+    bound."""
+    c = Case(f"sharp_{Hq}", "bf16", B=1, Hq=Hq, Hkv=2, Lq=600, Lk=900, D=128,
+             mask_mode=MASK_NONE, seed=9)
+    q, k, v, kl = make_inputs(c)
+    out = run(c, q, k, v, kl, scale=0.6)
+    ref = oracle.attention(q, k, v, key_lens=kl, mask_mode=c.mask_mode, scale=0.6)
+    got = to_numpy_f64(out)
+    assert np.all(np.isfinite(got))
+    bound = 3 * 2.0 ** -8 * float(v.float().abs().max())
+    max_abs = float(np.max(np.abs(got - ref)))
+    rel_l2 = float(np.linalg.norm(got - ref) / np.linalg.norm(ref))
+    assert max_abs <= bound, f"max-abs {max_abs:.3e} > {bound:.3e}"
+    assert rel_l2 <= 5e-3, f"rel-L2 {rel_l2:.3e}"
+
+
 # ------------------------------------------------------------------------------ decode sweeps (K2)
 
 @pytest.mark.parametrize("D", [64, 128])
